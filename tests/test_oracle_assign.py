@@ -1,0 +1,178 @@
+"""Pins for the oracle's Assign task map (CPU only).
+
+Assign tiles every unit's KV and hands the tiles to N CTAs so each carries an
+equal share of the work ("基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2
+Assign step and 三.3 均分调度); prefill units list only the KV tiles the block
+mask keeps (二.1 active-KV-tile list).  The exact procedure is this project's
+reading and is written out in oracle/pa_oracle.c above oracle_assign().
+
+Pinned by: hand-worked examples (tests/golden/assign_worked_examples.json),
+structural invariants that hold for any input (every tile covered once, in
+ascending contiguous runs; balanced per-CTA cost; slot numbering), and an
+independent brute force written differently (bisect over CTA bounds,
+itertools.groupby for runs).
+"""
+import bisect
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def run_oracle(oracle_mod, ex):
+    bm = None if ex["block_mask"] is None else np.array(ex["block_mask"], dtype=np.uint8)
+    return oracle_mod.assign(ex["mode"], ex["num_seqs"], ex["num_q_heads"], ex["num_kv_heads"],
+                             ex["num_ctas"], ex["kv_tile"], ex["balance_rows"],
+                             np.array(ex["context_lens"], np.int32),
+                             np.array(ex["q_lens"], np.int32), bm)
+
+
+def load_examples():
+    with open(os.path.join(GOLDEN, "assign_worked_examples.json")) as f:
+        return json.load(f)["examples"]
+
+
+@pytest.mark.parametrize("ex", load_examples(), ids=lambda e: e["name"])
+def test_worked_examples(oracle_mod, ex):
+    tm = run_oracle(oracle_mod, ex)
+    e = ex["expect"]
+    assert tm.units.tolist() == e["units"]
+    assert tm.unit_ntiles.tolist() == e["unit_ntiles"]
+    assert tm.cta_ptr.tolist() == e["cta_ptr"]
+    assert tm.tasks.tolist() == e["tasks"]
+    assert tm.unit_nsplit.tolist() == e["unit_nsplit"]
+    assert tm.unit_slot0.tolist() == e["unit_slot0"]
+    assert tm.num_slots == e["num_slots"]
+    if "active" in e:
+        assert [tm.active[u, :n].tolist() for u, n in enumerate(tm.unit_ntiles)] == e["active"]
+
+
+# ------------------------------------------------------- brute force
+
+def brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask=None, mask_tile=128):
+    G = Hq // Hkv
+    units = []
+    for b in range(B):
+        if mode == 0:
+            for hk in range(Hkv):
+                units.append((b, hk, 0, ql[b], ctx[b] if ql[b] > 0 else 0))
+        else:
+            qtok = 128 // G
+            for hk in range(Hkv):
+                for q0 in range(0, ql[b], qtok):
+                    nq = min(qtok, ql[b] - q0)
+                    units.append((b, hk, q0, nq, ctx[b] - ql[b] + q0 + nq))
+    lists = []
+    for (b, hk, q0, nq, L) in units:
+        reach = list(range(-(-L // T)))
+        if mask is not None:
+            reach = [t for t in reach if t < mask.shape[2] and mask[b, q0 // mask_tile, t]]
+        lists.append(reach)
+    weights = [max(1, -(-(G * u[3]) // rbal)) for u in units]
+    costs = list(itertools.accumulate([0] + [len(l) * w for l, w in zip(lists, weights)]))
+    C = costs[-1]
+    bounds = [c * C // N for c in range(N + 1)]
+    owned = []                      # (cta, unit, position)
+    for u, lst in enumerate(lists):
+        for t in range(len(lst)):
+            x = costs[u] + t * weights[u]
+            owned.append((bisect.bisect_right(bounds, x) - 1 if C else 0, u, t))
+    owned = [(min(c, N - 1), u, t) for c, u, t in owned]
+    tasks = []
+    for (c, u), grp in itertools.groupby(owned, key=lambda z: (z[0], z[1])):
+        grp = list(grp)
+        tasks.append([c, u, grp[0][2], grp[-1][2] + 1])
+    nsplit = [0] * len(units)
+    for t in tasks:
+        nsplit[t[1]] += 1
+    slot0, s = [], 0
+    for n in nsplit:
+        slot0.append(s if n > 1 else -1)
+        s += n if n > 1 else 0
+    seen = [0] * len(units)
+    out_tasks = []
+    for c, u, t0, t1 in tasks:
+        out_tasks.append([u, t0, t1, slot0[u] + seen[u] if nsplit[u] > 1 else -1])
+        seen[u] += 1
+    cta_ptr = [sum(1 for t in tasks if t[0] < c) for c in range(N + 1)]
+    return dict(units=[list(u[:4]) for u in units], lists=lists, tasks=out_tasks,
+                cta_ptr=cta_ptr, nsplit=nsplit, slot0=slot0, slots=s, weights=weights,
+                C=C, task_cta=[t[0] for t in tasks])
+
+
+def random_case(rng):
+    mode = int(rng.integers(0, 2))
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    B = int(rng.integers(1, 7))
+    N = int(rng.integers(1, 20))
+    T = int(rng.choice([16, 64, 128])) if mode == 0 else 128
+    rbal = int(rng.choice([16, 64, 128, 288]))
+    ctx, ql = [], []
+    for _ in range(B):
+        c = int(rng.integers(0, 700))
+        q = int(rng.integers(0, min(c, 300) + 1)) if mode == 1 else int(rng.integers(0, min(c, 4) + 1))
+        ctx.append(c)
+        ql.append(q)
+    mask = None
+    if mode == 1 and rng.random() < 0.5:
+        mq = max(1, -(-max(ql) // 128)) if max(ql) > 0 else 1
+        mk = max(1, -(-max(ctx) // 128)) if max(ctx) > 0 else 1
+        mask = (rng.random((B, mq, mk)) < 0.5).astype(np.uint8)
+    return mode, B, G * Hkv, Hkv, N, T, rbal, ctx, ql, mask
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_matches_brute_force_and_invariants(oracle_mod, seed):
+    rng = np.random.default_rng(seed)
+    mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask = random_case(rng)
+    tm = oracle_mod.assign(mode, B, Hq, Hkv, N, T, rbal, np.array(ctx, np.int32),
+                           np.array(ql, np.int32), mask)
+    bf = brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask)
+    assert tm.units.tolist() == bf["units"]
+    assert [tm.active[u, :n].tolist() for u, n in enumerate(tm.unit_ntiles)] == bf["lists"]
+    assert tm.tasks.tolist() == bf["tasks"]
+    assert tm.cta_ptr.tolist() == bf["cta_ptr"]
+    assert tm.unit_nsplit.tolist() == bf["nsplit"]
+    assert tm.unit_slot0.tolist() == bf["slot0"]
+    assert tm.num_slots == bf["slots"]
+
+    # invariant: every unit's list covered exactly once, ascending contiguous runs
+    for u, n in enumerate(tm.unit_ntiles):
+        runs = [t for t in tm.tasks.tolist() if t[0] == u]
+        pos = 0
+        for _, t0, t1, _ in runs:
+            assert t0 == pos and t1 > t0
+            pos = t1
+        assert pos == n
+    # invariant: per-CTA cost within one max weight of C/N
+    wmax = max(bf["weights"]) if bf["weights"] else 1
+    for c in range(N):
+        cost = 0
+        for k in range(tm.cta_ptr[c], tm.cta_ptr[c + 1]):
+            u, t0, t1, _ = tm.tasks[k]
+            cost += (t1 - t0) * bf["weights"][u]
+        assert abs(cost - bf["C"] / N) <= wmax + 1e-9
+    # invariant: slots are 0..n_slots-1, each once, only for split units
+    slots = [int(t[3]) for t in tm.tasks if t[3] >= 0]
+    assert sorted(slots) == list(range(tm.num_slots))
+    # invariant: task count never exceeds units + CTAs
+    assert tm.num_tasks <= tm.num_units + N
+
+
+def test_full_size_decode_map_is_balanced(oracle_mod):
+    from paged_attention_gb300 import workloads as W
+    g = torch.Generator().manual_seed(1)
+    ctx = W._log_uniform_ints(64, 128, 32768, g)
+    tm = oracle_mod.assign(0, 64, 32, 8, 152, 64, 128, np.array(ctx, np.int32),
+                           np.array([2] * 64, np.int32))
+    per_cta = []
+    for c in range(152):
+        per_cta.append(sum(int(t[2] - t[1]) for t in tm.tasks[tm.cta_ptr[c]:tm.cta_ptr[c + 1]]))
+    assert max(per_cta) - min(per_cta) <= 1
+    assert tm.num_tasks <= 512 + 152
