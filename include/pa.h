@@ -1,0 +1,232 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-KV-cache attention forward.
+ *
+ * The operation ("基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2 "Prefill
+ * 与 Decode"): for every new query token of every sequence, softmax attention
+ * over that sequence's cached keys and values, which live in fixed-size
+ * physical pages reached through a per-sequence block table.  Decode runs as
+ * three passes -- Assign (tile the KV, build a load-balanced task map),
+ * Split-K compute (persistent CTAs write final or partial O and LSE),
+ * Combine (LSE-rescale the partials into the exact softmax).  Prefill runs
+ * causal or block-sparse attention over the same paged cache, and also takes
+ * the mixed chunked-prefill + decode batch (xdnf.cn "Chunked Prefill" hybrid
+ * batch article).  The arguments follow the pages' statement of the problem:
+ * Q [tokens, Hq, D]; K/V caches [pages, page_size, Hkv, D] (NHD) or
+ * [pages, Hkv, page_size, D] (HND) ("基于Triton-TLE…", 三.2: both layouts read
+ * through one projected tile descriptor); block_table, context_lens, q_lens,
+ * sm_scale; FP8 (E4M3) K/V with fp32 scales per (page, KV head); a 0/1 block
+ * mask over 128x128 (query, key) tiles.
+ *
+ * Semantics (identical to the fp64 oracle the tests compare against):
+ *   query i of sequence b sits at absolute position p = context_lens[b] -
+ *   q_lens[b] + i and attends to keys j <= p (keys j < context_lens[b]); with
+ *   a block mask also only keys whose tile (i/128, j/128) is kept.  q head h
+ *   reads KV head h / (Hq/Hkv).  out = softmax(sm_scale * q.K^T) V in bf16;
+ *   lse = natural log of sum_j exp(sm_scale * q.k_j) in fp32.  A row with no
+ *   visible key gets out = 0 and lse = -inf.
+ *
+ * Conventions
+ *   - Every pointer argument except those marked "host" is a DEVICE pointer.
+ *     The caller owns every buffer; the library allocates no device memory
+ *     and keeps no per-call state.  (It caches, per device, the SM count and
+ *     per-kernel attributes.)
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All calls
+ *     are asynchronous on that stream except pa_read_task_map and
+ *     pa_last_device_error, which synchronise it.
+ *   - Host-side validation never throws: bad arguments return
+ *     PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED / PA_ERR_WORKSPACE and launch
+ *     nothing.  Launch failures return PA_ERR_CUDA.
+ *   - Faults the device detects (a block-table entry outside [0, num_pages),
+ *     q_lens > context_lens, lengths above the declared maxima, a wait that
+ *     ran out of time) never trap: the kernel records a code in the Assign
+ *     workspace, skips the offending access and finishes; the outputs of that
+ *     call are then unspecified.  Read the code with pa_last_device_error.
+ *   - Tensors are dense and row-major with the shapes given; every base
+ *     pointer must be 16-byte aligned.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null pointer, bad dimension, misaligned buffer       */
+    PA_ERR_UNSUPPORTED = 2,  /* valid but not built (head_dim, page_size, GQA ratio) */
+    PA_ERR_WORKSPACE = 3,    /* a workspace smaller than the *_workspace_size query */
+    PA_ERR_CUDA = 4,         /* a CUDA runtime call failed                           */
+    PA_ERR_DEVICE_CHECK = 5, /* the device recorded a fault (pa_last_device_error)   */
+    PA_ERR_TIMEOUT = 6       /* a bounded device wait ran out                        */
+} pa_status;
+
+/* KV cache layouts ("基于Triton-TLE…", 三.2). */
+enum { PA_NHD = 0, PA_HND = 1 };
+/* KV cache element types.  FP8 is OCP E4M3FN; its fp32 scales are per
+ * (page, KV head) for K and V separately. */
+enum { PA_BF16 = 0, PA_FP8_E4M3 = 1 };
+/* Assign modes.
+ *   PA_MODE_DECODE:  one unit per (sequence, KV head) holding all q_lens[b]
+ *                    queries (G*q_len rows, at most 64); 64-token KV tiles.
+ *   PA_MODE_PREFILL: one unit per (sequence, KV head, q tile of 128/G tokens)
+ *                    = one 128-row tile; 128-token KV tiles; block mask
+ *                    allowed.  Used by pa_prefill for prefill and mixed
+ *                    batches. */
+enum { PA_MODE_DECODE = 0, PA_MODE_PREFILL = 1 };
+
+/* Device error codes written by the kernels (read with pa_last_device_error). */
+enum {
+    PA_DEV_OK = 0,
+    PA_DEV_BAD_LENGTHS = 1,    /* q_lens > context_lens, negative, above the maxima, or
+                                  sum(q_lens) != total_q_tokens: the task map is empty */
+    PA_DEV_BAD_PAGE = 2,       /* a block-table entry used was outside [0, num_pages)  */
+    PA_DEV_WAIT_TIMEOUT = 4    /* a pipeline wait ran out of time                      */
+};
+
+/* Problem description, passed by host pointer and copied by every call. */
+typedef struct pa_problem {
+    int32_t num_seqs;          /* B                                                  */
+    int32_t num_q_heads;       /* Hq                                                 */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0, G = Hq/Hkv                      */
+    int32_t head_dim;          /* D: 64 or 128                                       */
+    int32_t page_size;         /* tokens per page: 16, 32, 64, 128 or 256             */
+    int32_t num_pages;         /* pages in the cache pool (bound for block_table)     */
+    int32_t max_pages_per_seq; /* row stride of block_table                          */
+    int32_t total_q_tokens;    /* sum of q_lens = rows of q / out                    */
+    int32_t max_q_len;         /* >= every q_lens[b]                                 */
+    int32_t max_context_len;   /* >= every context_lens[b]                           */
+    int32_t layout;            /* PA_NHD or PA_HND                                   */
+    int32_t kv_dtype;          /* PA_BF16 or PA_FP8_E4M3                             */
+    int32_t mask_q_tiles;      /* block mask dims per sequence; 0 = no mask          */
+    int32_t mask_kv_tiles;
+    int32_t num_ctas;          /* persistent CTAs; 0 = the library's choice          */
+    int32_t balance_rows;      /* Assign weight divisor; 0 = 128                     */
+    float sm_scale;            /* softmax scale applied to q.k                       */
+} pa_problem;
+
+/* Human-readable name of a pa_status or PA_DEV_* code set. */
+PA_API const char* pa_status_string(int status);
+
+/* Library version string. */
+PA_API const char* pa_version(void);
+
+/* Persistent CTA count that pa_assign and the compute pass of `mode` use for
+ * this problem on the current device (problem->num_ctas if non-zero).
+ * *num_ctas: host out. */
+PA_API pa_status pa_num_ctas(const pa_problem* problem, int mode, int32_t* num_ctas);
+
+/* Bytes of the Assign workspace for (problem, mode).  Its content (task map,
+ * unit table, active-tile lists, error word) is private to the library. */
+PA_API size_t pa_assign_workspace_size(const pa_problem* problem, int mode);
+
+/* Bytes of the split-K partial workspace (fp32 O and LSE per split slot). */
+PA_API size_t pa_partial_workspace_size(const pa_problem* problem, int mode);
+
+/*
+ * Assign ("基于Triton-TLE…", 一.2: tile each sequence's KV and build a
+ * load-balanced task map; 二.1: keep only the KV tiles the block mask keeps,
+ * compacted into an ascending active-tile list).
+ *   context_lens, q_lens: int32 [B]
+ *   block_mask: uint8 [B][mask_q_tiles][mask_kv_tiles] or NULL (prefill mode only)
+ *   assign_ws: >= pa_assign_workspace_size bytes, 256-byte aligned; written.
+ * Clears the device error word.  Units are (b, hk) in decode mode and
+ * (b, hk, q tile of 128/G tokens) in prefill mode; tile t of unit u weighs
+ * w_u = max(1, ceil(G*rows/balance_rows)); CTA c owns the cost interval
+ * [floor(c*C/N), floor((c+1)*C/N)) of the total cost C; a task is a maximal
+ * run of one unit's tiles inside one CTA; split units get partial slots.
+ */
+PA_API pa_status pa_assign(const pa_problem* problem, int mode, const int32_t* context_lens,
+                    const int32_t* q_lens, const uint8_t* block_mask, void* assign_ws,
+                    size_t assign_ws_bytes, void* stream);
+
+/*
+ * Split-K decode compute ("基于Triton-TLE…", 一.2 Split-K Compute; 三.1 small-M
+ * query geometry: the G*q_len rows of one KV head share every K/V tile read).
+ * Persistent CTAs walk the task map of pa_assign(PA_MODE_DECODE): per 64-token
+ * KV tile a page lookup, a TMA load of K and V into a multi-stage shared-memory
+ * ring, S = sm_scale * Q K^T, online softmax (fp32), O += P V.  An unsplit
+ * unit writes out / lse directly; a split unit writes normalised partial O and
+ * its LSE to partial_ws for pa_combine.
+ *   q: bf16 [total_q_tokens][Hq][D]
+ *   k_cache, v_cache: bf16 or E4M3 bytes, NHD or HND (see above)
+ *   block_table: int32 [B][max_pages_per_seq]; only entries of pages holding a
+ *     token < context_lens[b] are read
+ *   k_scale, v_scale: fp32 [num_pages][Hkv] (FP8 only; else may be NULL)
+ *   assign_ws: from pa_assign(..., PA_MODE_DECODE, ...) on the same stream
+ *   partial_ws: >= pa_partial_workspace_size(problem, PA_MODE_DECODE) bytes
+ *   out: bf16 [total_q_tokens][Hq][D];  lse: fp32 [total_q_tokens][Hq] or NULL
+ */
+PA_API pa_status pa_decode_splitk(const pa_problem* problem, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_table,
+                           const int32_t* context_lens, const int32_t* q_lens,
+                           const float* k_scale, const float* v_scale, const void* assign_ws,
+                           size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
+                           void* out, float* lse, void* stream);
+
+/*
+ * Combine ("基于Triton-TLE…", 一.2 Combine; 三.3 merge of partial softmax
+ * states with m = max, w_k = exp(m_k - m)).  For every unit split into S > 1
+ * tasks: m = max_k lse_k, O = sum_k e^(lse_k - m) O_k / sum_k e^(lse_k - m),
+ * lse = m + ln sum_k e^(lse_k - m).  Units with no visible key get O = 0,
+ * lse = -inf.  Units written directly by the compute pass are not touched.
+ *   mode: the mode assign_ws was built with.
+ */
+PA_API pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
+                     size_t assign_ws_bytes, const void* partial_ws, size_t partial_ws_bytes,
+                     void* out, float* lse, void* stream);
+
+/*
+ * Prefill / mixed-batch compute ("基于Triton-TLE…", 一.2 Prefill: tile
+ * scheduling by (batch, head, q tile), pipelined QK / causal mask / fp32 online
+ * softmax / PV, epilogue; 二.1 active-tile list; 二.2 page-aware TMA pipeline;
+ * "vLLM Triton Attention Backend Deep Dive": Q blocks pack the G heads of one
+ * KV head, persistent fixed grid).  Walks the task map of
+ * pa_assign(PA_MODE_PREFILL) with 128-row GQA-packed q tiles and 128-token KV
+ * tiles on the tcgen05 tensor cores (accumulators in tensor memory).
+ * Arguments as pa_decode_splitk, plus block_mask (the one given to pa_assign,
+ * or NULL).  Decode rows (q_len 1) of a mixed batch are ordinary units.
+ */
+PA_API pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cache,
+                     const void* v_cache, const int32_t* block_table,
+                     const int32_t* context_lens, const int32_t* q_lens, const float* k_scale,
+                     const float* v_scale, const uint8_t* block_mask, const void* assign_ws,
+                     size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
+                     void* out, float* lse, void* stream);
+
+/*
+ * Test hook: copy the task map out of assign_ws (synchronises `stream`).
+ * counts (host, int32[4]) = {units, tasks, slots, ctas}.  Each other host
+ * array may be NULL; sizes: cta_ptr [ctas+1], tasks [tasks][4] = {unit, t0,
+ * t1, slot} (t = positions in the unit's tile list), units [units][4] =
+ * {b, hk, q0, nq}, unit_ntiles [units], unit_nsplit [units], unit_slot0
+ * [units], active [units][max_kv_tiles] (only with a block mask; tile lists),
+ * where max_kv_tiles = ceil(max_context_len / kv_tile), kv_tile 64 (decode) or
+ * 128 (prefill).
+ */
+PA_API pa_status pa_read_task_map(const pa_problem* problem, int mode, const void* assign_ws,
+                           size_t assign_ws_bytes, int32_t* counts, int32_t* cta_ptr,
+                           int32_t* tasks, int32_t* units, int32_t* unit_ntiles,
+                           int32_t* unit_nsplit, int32_t* unit_slot0, int32_t* active,
+                           void* stream);
+
+/* Read (and keep) the device error word of assign_ws into *code (host);
+ * synchronises `stream`.  Returns PA_OK when *code == PA_DEV_OK, else
+ * PA_ERR_DEVICE_CHECK (or PA_ERR_TIMEOUT when only the timeout bit is set). */
+PA_API pa_status pa_last_device_error(const void* assign_ws, int32_t* code, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,457 @@
+// pa_api.cu -- the C ABI: argument validation, workspace layout, TMA
+// descriptor encoding and launches.  Declarations and the contract of every
+// entry point are in include/pa.h.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+
+struct DecodeParams;  // pa_decode.cu
+cudaError_t launch_assign(const WsLayout& L, const int32_t* ctx, const int32_t* ql,
+                          const uint8_t* mask, void* ws, cudaStream_t stream);
+cudaError_t launch_combine(const WsLayout& L, const void* ws, const void* partial, void* out,
+                           float* lse, int grid, cudaStream_t stream);
+int decode_smem_bytes(int D, int RT, bool fp8);
+int decode_threads(int RT);
+const void* decode_kernel_ptr(int D, int RT, bool fp8);
+cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int RT,
+                                   const void* q, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const int32_t* block_table, const int32_t* ctx,
+                                   const int32_t* ql, const float* ks, const float* vs,
+                                   void* ws, void* partial, void* out, float* lse,
+                                   cudaStream_t stream);
+int prefill_smem_bytes(int D, bool fp8);
+const void* prefill_kernel_ptr(int D, bool fp8);
+cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, const void* q,
+                                    const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, const int32_t* block_table,
+                                    const int32_t* ctx, const int32_t* ql, const float* ks,
+                                    const float* vs, void* ws, void* partial, void* out,
+                                    float* lse, cudaStream_t stream);
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sm_count[kMaxDevices] = {0};
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return -1;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// rows (query token x head) of one decode unit, rounded up to 16-row tiles
+int decode_row_tiles(const pa_problem& p) {
+    const int rows = (p.num_q_heads / p.num_kv_heads) * p.max_q_len;
+    if (rows <= 16) return 1;
+    if (rows <= 32) return 2;
+    if (rows <= 64) return 4;
+    return -1;
+}
+
+pa_status check_problem(const pa_problem* pp, int mode) {
+    if (!pp) return PA_ERR_INVALID_ARG;
+    const pa_problem& p = *pp;
+    if (mode != PA_MODE_DECODE && mode != PA_MODE_PREFILL) return PA_ERR_INVALID_ARG;
+    if (p.num_seqs < 1 || p.num_q_heads < 1 || p.num_kv_heads < 1 ||
+        p.num_q_heads % p.num_kv_heads != 0 || p.num_pages < 1 || p.max_pages_per_seq < 1 ||
+        p.total_q_tokens < 0 || p.max_q_len < 0 || p.max_context_len < p.max_q_len ||
+        p.mask_q_tiles < 0 || p.mask_kv_tiles < 0 || p.num_ctas < 0 || p.balance_rows < 0 ||
+        !std::isfinite(p.sm_scale))
+        return PA_ERR_INVALID_ARG;
+    if (p.layout != PA_NHD && p.layout != PA_HND) return PA_ERR_INVALID_ARG;
+    if (p.kv_dtype != PA_BF16 && p.kv_dtype != PA_FP8_E4M3) return PA_ERR_INVALID_ARG;
+    if ((p.mask_q_tiles > 0) != (p.mask_kv_tiles > 0)) return PA_ERR_INVALID_ARG;
+    if (p.head_dim != 64 && p.head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (p.page_size != 16 && p.page_size != 32 && p.page_size != 64 && p.page_size != 128 &&
+        p.page_size != 256)
+        return PA_ERR_UNSUPPORTED;
+    if ((int64_t)p.max_pages_per_seq * p.page_size < p.max_context_len) return PA_ERR_INVALID_ARG;
+    const int G = p.num_q_heads / p.num_kv_heads;
+    if (mode == PA_MODE_DECODE) {
+        if (p.mask_q_tiles > 0) return PA_ERR_INVALID_ARG;   // masks are a prefill feature
+        const int RT = decode_row_tiles(p);
+        if (RT < 0) return PA_ERR_UNSUPPORTED;
+        if (p.kv_dtype == PA_FP8_E4M3 && (p.head_dim != 128 || RT > 2)) return PA_ERR_UNSUPPORTED;
+    } else {
+        if (G > 128 || 128 % G != 0) return PA_ERR_UNSUPPORTED;
+        if (p.kv_dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    }
+    return PA_OK;
+}
+
+int resolve_ctas(const pa_problem& p, int mode) {
+    if (p.num_ctas > 0) return p.num_ctas;
+    const int sms = sm_count();
+    if (sms <= 0) return -1;
+    int per_sm = 1;
+    const void* k = nullptr;
+    int smem = 0, threads = 0;
+    if (mode == PA_MODE_DECODE) {
+        const int RT = decode_row_tiles(p);
+        k = decode_kernel_ptr(p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3);
+        smem = decode_smem_bytes(p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3);
+        threads = decode_threads(RT);
+    } else {
+        k = prefill_kernel_ptr(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
+        smem = prefill_smem_bytes(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
+        threads = 256;
+    }
+    if (k && smem > 0) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return -1;
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, threads, smem) == cudaSuccess &&
+            occ > 0)
+            per_sm = occ;
+        else
+            return -1;
+    }
+    return sms * per_sm;
+}
+
+int rows_cap_for(const pa_problem& p, int mode) {
+    if (mode == PA_MODE_PREFILL) return kPrefillRows;
+    return 16 * decode_row_tiles(p);
+}
+
+bool encode_kv_map(const pa_problem& p, const void* base, CUtensorMap* map) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int e = p.kv_dtype == PA_BF16 ? 2 : 1;
+    const cuuint64_t D = p.head_dim, ps = p.page_size, H = p.num_kv_heads, NP = p.num_pages;
+    // logical order (d, slot, head, page); NHD vs HND differ only in strides
+    cuuint64_t dims[4] = {D, ps, H, NP};
+    cuuint64_t strides[3];
+    if (p.layout == PA_NHD) {
+        strides[0] = H * D * e;
+        strides[1] = D * e;
+        strides[2] = ps * H * D * e;
+    } else {
+        strides[0] = D * e;
+        strides[1] = ps * D * e;
+        strides[2] = H * ps * D * e;
+    }
+    const int rows = p.page_size < 64 ? p.page_size : 64;
+    cuuint32_t box[4] = {(cuuint32_t)(128 / e < (int)D ? 128 / e : (int)D), (cuuint32_t)rows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, p.kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                    4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Q viewed as (d, head, token): box = 64 elements x G heads x (128/G) tokens
+bool encode_q_map(const pa_problem& p, const void* base, CUtensorMap* map) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const cuuint64_t D = p.head_dim, Hq = p.num_q_heads;
+    const cuuint64_t T = p.total_q_tokens > 0 ? p.total_q_tokens : 1;
+    cuuint64_t dims[3] = {D, Hq, T};
+    cuuint64_t strides[2] = {D * 2, Hq * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kPrefillRows / G)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+pa_status make_layout(const pa_problem* p, int mode, WsLayout& L) {
+    pa_status st = check_problem(p, mode);
+    if (st != PA_OK) return st;
+    const int N = resolve_ctas(*p, mode);
+    if (N <= 0) return PA_ERR_CUDA;
+    if (!layout_for(*p, mode, N, rows_cap_for(*p, mode), L)) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+}  // namespace
+
+bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L) {
+    std::memset(&L, 0, sizeof(L));
+    const int G = p.num_q_heads / p.num_kv_heads;
+    L.mode = mode;
+    L.B = p.num_seqs;
+    L.Hq = p.num_q_heads;
+    L.Hkv = p.num_kv_heads;
+    L.G = G;
+    L.D = p.head_dim;
+    L.N = N;
+    L.kv_tile = mode == PA_MODE_DECODE ? kDecodeTile : kPrefillTile;
+    L.qtok = mode == PA_MODE_DECODE ? (p.max_q_len > 0 ? p.max_q_len : 1) : kPrefillRows / G;
+    int64_t ucap;
+    if (mode == PA_MODE_DECODE)
+        ucap = (int64_t)p.num_seqs * p.num_kv_heads;
+    else
+        ucap = (int64_t)p.num_kv_heads * (ceil_div(p.total_q_tokens, L.qtok) + p.num_seqs);
+    if (ucap < 1) ucap = 1;
+    if (ucap > (1 << 30)) return false;
+    L.unit_cap = (int32_t)ucap;
+    L.task_cap = L.unit_cap + N;
+    L.max_kv_tiles = ceil_div(p.max_context_len > 0 ? p.max_context_len : 1, L.kv_tile);
+    L.has_mask = p.mask_q_tiles > 0 ? 1 : 0;
+    L.rows_cap = rows_cap;
+    L.balance_rows = p.balance_rows > 0 ? p.balance_rows : kDefaultBalanceRows;
+    L.total_q = p.total_q_tokens;
+    L.max_q_len = p.max_q_len;
+    L.max_ctx = p.max_context_len;
+    L.mask_q_tiles = p.mask_q_tiles;
+    L.mask_kv_tiles = p.mask_kv_tiles;
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) {
+        int64_t o = off;
+        off = align256(off + bytes);
+        return o;
+    };
+    L.off_header = take(kHeaderWords * 4);
+    L.off_cta_ptr = take((int64_t)(N + 1) * 4);
+    L.off_tasks = take((int64_t)L.task_cap * 16);
+    L.off_task_cta = take((int64_t)L.task_cap * 4);
+    L.off_units = take((int64_t)L.unit_cap * 16);
+    L.off_ntiles = take((int64_t)L.unit_cap * 4);
+    L.off_prefix = take((int64_t)L.unit_cap * 8);
+    L.off_nsplit = take((int64_t)L.unit_cap * 4);
+    L.off_slot0 = take((int64_t)L.unit_cap * 4);
+    L.off_task0 = take((int64_t)L.unit_cap * 4);
+    L.off_fix = take((int64_t)L.unit_cap * 4);
+    L.off_active = take(L.has_mask ? (int64_t)L.unit_cap * L.max_kv_tiles * 4 : 4);
+    L.off_cu_q = take((int64_t)(p.num_seqs + 1) * 4);
+    L.off_seq_unit0 = take((int64_t)(p.num_seqs + 1) * 4);
+    L.total_bytes = off;
+    L.partial_slots = L.task_cap;
+    L.partial_bytes = L.partial_slots * (int64_t)L.rows_cap * (L.D + 1) * 4;
+    return true;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_DEVICE_CHECK: return "PA_ERR_DEVICE_CHECK";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+const char* pa_version(void) { return "paged_attention_gb300 0.1 (sm_103a)"; }
+
+pa_status pa_num_ctas(const pa_problem* problem, int mode, int32_t* num_ctas) {
+    if (!num_ctas) return PA_ERR_INVALID_ARG;
+    pa_status st = check_problem(problem, mode);
+    if (st != PA_OK) return st;
+    const int n = resolve_ctas(*problem, mode);
+    if (n <= 0) return PA_ERR_CUDA;
+    *num_ctas = n;
+    return PA_OK;
+}
+
+size_t pa_assign_workspace_size(const pa_problem* problem, int mode) {
+    WsLayout L;
+    if (make_layout(problem, mode, L) != PA_OK) return 0;
+    return (size_t)L.total_bytes;
+}
+
+size_t pa_partial_workspace_size(const pa_problem* problem, int mode) {
+    WsLayout L;
+    if (make_layout(problem, mode, L) != PA_OK) return 0;
+    return (size_t)L.partial_bytes;
+}
+
+pa_status pa_assign(const pa_problem* problem, int mode, const int32_t* context_lens,
+                    const int32_t* q_lens, const uint8_t* block_mask, void* assign_ws,
+                    size_t assign_ws_bytes, void* stream) {
+    WsLayout L;
+    pa_status st = make_layout(problem, mode, L);
+    if (st != PA_OK) return st;
+    if (!context_lens || !q_lens || !assign_ws || !aligned(assign_ws, 256) ||
+        !aligned(context_lens, 4) || !aligned(q_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (L.has_mask && !block_mask) return PA_ERR_INVALID_ARG;
+    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
+    cudaError_t e = launch_assign(L, context_lens, q_lens, L.has_mask ? block_mask : nullptr,
+                                  assign_ws, (cudaStream_t)stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_splitk(const pa_problem* problem, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_table,
+                           const int32_t* context_lens, const int32_t* q_lens,
+                           const float* k_scale, const float* v_scale, const void* assign_ws,
+                           size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
+                           void* out, float* lse, void* stream) {
+    WsLayout L;
+    pa_status st = make_layout(problem, PA_MODE_DECODE, L);
+    if (st != PA_OK) return st;
+    const pa_problem& p = *problem;
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !assign_ws ||
+        !out || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(out, 16) || !aligned(block_table, 4) || !aligned(assign_ws, 256))
+        return PA_ERR_INVALID_ARG;
+    if (p.kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
+    if (partial_ws_bytes < (size_t)L.partial_bytes || (!partial_ws && L.partial_bytes > 0) ||
+        !aligned(partial_ws, 16))
+        return PA_ERR_WORKSPACE;
+    CUtensorMap tk, tv;
+    if (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv))
+        return PA_ERR_INVALID_ARG;
+    cudaError_t e = launch_decode_from_api(p, L, decode_row_tiles(p), q, tk, tv, block_table,
+                                           context_lens, q_lens, k_scale, v_scale,
+                                           const_cast<void*>(assign_ws), partial_ws, out, lse,
+                                           (cudaStream_t)stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
+                     size_t assign_ws_bytes, const void* partial_ws, size_t partial_ws_bytes,
+                     void* out, float* lse, void* stream) {
+    WsLayout L;
+    pa_status st = make_layout(problem, mode, L);
+    if (st != PA_OK) return st;
+    if (!assign_ws || !out || !aligned(out, 16) || !aligned(assign_ws, 256))
+        return PA_ERR_INVALID_ARG;
+    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
+    if (partial_ws_bytes < (size_t)L.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
+        return PA_ERR_WORKSPACE;
+    int grid = 2 * sm_count();
+    if (grid > L.unit_cap) grid = L.unit_cap;
+    if (grid < 1) grid = 1;
+    cudaError_t e = launch_combine(L, assign_ws, partial_ws, out, lse, grid, (cudaStream_t)stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cache,
+                     const void* v_cache, const int32_t* block_table,
+                     const int32_t* context_lens, const int32_t* q_lens, const float* k_scale,
+                     const float* v_scale, const uint8_t* block_mask, const void* assign_ws,
+                     size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
+                     void* out, float* lse, void* stream) {
+    (void)block_mask;  // the active-tile lists in assign_ws already encode the mask
+    WsLayout L;
+    pa_status st = make_layout(problem, PA_MODE_PREFILL, L);
+    if (st != PA_OK) return st;
+    const pa_problem& p = *problem;
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !assign_ws ||
+        !out || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(out, 16) || !aligned(block_table, 4) || !aligned(assign_ws, 256))
+        return PA_ERR_INVALID_ARG;
+    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
+    if (partial_ws_bytes < (size_t)L.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
+        return PA_ERR_WORKSPACE;
+    if (p.total_q_tokens == 0) return PA_OK;
+    CUtensorMap tq, tk, tv;
+    if (!encode_q_map(p, q, &tq) || !encode_kv_map(p, k_cache, &tk) ||
+        !encode_kv_map(p, v_cache, &tv))
+        return PA_ERR_INVALID_ARG;
+    cudaError_t e = launch_prefill_from_api(p, L, q, tq, tk, tv, block_table, context_lens,
+                                            q_lens, k_scale, v_scale, const_cast<void*>(assign_ws),
+                                            partial_ws, out, lse, (cudaStream_t)stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_read_task_map(const pa_problem* problem, int mode, const void* assign_ws,
+                           size_t assign_ws_bytes, int32_t* counts, int32_t* cta_ptr,
+                           int32_t* tasks, int32_t* units, int32_t* unit_ntiles,
+                           int32_t* unit_nsplit, int32_t* unit_slot0, int32_t* active,
+                           void* stream) {
+    WsLayout L;
+    pa_status st = make_layout(problem, mode, L);
+    if (st != PA_OK) return st;
+    if (!assign_ws || !counts) return PA_ERR_INVALID_ARG;
+    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t hdr[kHeaderWords];
+    const char* ws = reinterpret_cast<const char*>(assign_ws);
+    if (cudaMemcpyAsync(hdr, ws + L.off_header, sizeof hdr, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const int U = hdr[H_UNITS], T = hdr[H_TASKS];
+    counts[0] = U;
+    counts[1] = T;
+    counts[2] = hdr[H_SLOTS];
+    counts[3] = hdr[H_CTAS];
+    struct Copy {
+        void* dst;
+        int64_t off;
+        int64_t bytes;
+    } copies[] = {
+        {cta_ptr, L.off_cta_ptr, (int64_t)(L.N + 1) * 4},
+        {tasks, L.off_tasks, (int64_t)T * 16},
+        {units, L.off_units, (int64_t)U * 16},
+        {unit_ntiles, L.off_ntiles, (int64_t)U * 4},
+        {unit_nsplit, L.off_nsplit, (int64_t)U * 4},
+        {unit_slot0, L.off_slot0, (int64_t)U * 4},
+        {active, L.off_active, L.has_mask ? (int64_t)U * L.max_kv_tiles * 4 : 0},
+    };
+    for (const Copy& c : copies) {
+        if (!c.dst || c.bytes <= 0) continue;
+        if (cudaMemcpyAsync(c.dst, ws + c.off, (size_t)c.bytes, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    return cudaStreamSynchronize(s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_last_device_error(const void* assign_ws, int32_t* code, void* stream) {
+    if (!assign_ws || !code) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t v = 0;
+    const char* ws = reinterpret_cast<const char*>(assign_ws);  // header is at offset 0
+    if (cudaMemcpyAsync(&v, ws + H_ERROR * 4, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    *code = v;
+    if (v == PA_DEV_OK) return PA_OK;
+    if (v == PA_DEV_WAIT_TIMEOUT) return PA_ERR_TIMEOUT;
+    return PA_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

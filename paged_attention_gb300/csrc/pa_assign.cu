@@ -1,0 +1,274 @@
+// pa_assign.cu -- the Assign pass: units, tile lists, load-balanced task map.
+//
+// "基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2 (Assign: cut every KV
+// sequence into tiles and build a task map that balances the work per CTA),
+// 三.3 (均分调度: every CTA carries a similar amount of KV work; a GPU-resident
+// task map drives the persistent compute CTAs), 二.1 (the block mask is
+// compacted into an ascending active-KV-tile list with a warp ballot,
+// popcount and prefix rank).
+//
+// Three launches on the caller's stream:
+//   1. assign_seq_kernel   (1 CTA)      validate lengths; cu_q and the first
+//                                       unit of every sequence (block scans)
+//   2. assign_units_kernel (warp/unit)  unit -> (b, hk, q0, nq), tile count,
+//                                       active-tile list (ballot + popc)
+//   3. assign_map_kernel   (1 CTA)      cost prefix, CTA ownership in closed
+//                                       form, tasks, split slots, cta_ptr
+// Closed form used in 3: with C the total cost and N CTAs, CTA c owns
+// [a_c, a_{c+1}), a_c = floor(c*C/N); the owner of cost x (0 <= x < C) is
+// floor(((x+1)*N - 1) / C).
+#include "pa_internal.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+// Block-wide exclusive scan of one int64 per thread; *total gets the sum.
+__device__ int64_t block_exscan(int64_t v, int64_t* total, int64_t* sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sm[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = lane < nwarps ? sm[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        sm[lane] = w;  // inclusive per warp
+    }
+    __syncthreads();
+    int64_t excl = (x - v) + (warp > 0 ? sm[warp - 1] : 0);
+    *total = sm[nwarps - 1];
+    __syncthreads();
+    return excl;
+}
+
+__device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int units_of_seq(const WsLayout& L, int ql) {
+    if (L.mode == PA_MODE_DECODE) return L.Hkv;
+    return L.Hkv * (int)ceil_div64(ql, L.qtok);
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+assign_seq_kernel(WsLayout L, const int32_t* __restrict__ ctx, const int32_t* __restrict__ ql,
+                  void* ws) {
+    __shared__ int64_t sm[32];
+    int32_t* header = ws_ptr<int32_t>(ws, L.off_header);
+    int32_t* cu_q = ws_ptr<int32_t>(ws, L.off_cu_q);
+    int32_t* seq_u0 = ws_ptr<int32_t>(ws, L.off_seq_unit0);
+    const int tid = threadIdx.x;
+    const int chunk = (L.B + kScanThreads - 1) / kScanThreads;
+    const int b0 = min(L.B, tid * chunk), b1 = min(L.B, b0 + chunk);
+    int64_t sq = 0, su = 0;
+    int bad = 0;
+    for (int b = b0; b < b1; ++b) {
+        int q = ql[b], c = ctx[b];
+        if (q < 0 || c < q || c > L.max_ctx || q > L.max_q_len) bad = 1;
+        q = max(0, min(q, L.max_q_len));
+        sq += q;
+        su += units_of_seq(L, q);
+    }
+    int64_t tq, tu;
+    int64_t eq = block_exscan(sq, &tq, sm);
+    int64_t eu = block_exscan(su, &tu, sm);
+    for (int b = b0; b < b1; ++b) {
+        int q = max(0, min(ql[b], L.max_q_len));
+        cu_q[b] = (int32_t)eq;
+        seq_u0[b] = (int32_t)eu;
+        eq += q;
+        eu += units_of_seq(L, q);
+    }
+    bad = __syncthreads_or(bad);
+    if (tid == 0) {
+        cu_q[L.B] = (int32_t)tq;
+        seq_u0[L.B] = (int32_t)tu;
+        bad = bad || tq != L.total_q || tu > L.unit_cap;
+        for (int i = 0; i < kHeaderWords; ++i) header[i] = 0;
+        header[H_UNITS] = bad ? 0 : (int32_t)tu;
+        header[H_ERROR] = bad ? PA_DEV_BAD_LENGTHS : PA_DEV_OK;
+        header[H_CTAS] = L.N;
+        header[H_MODE] = L.mode;
+    }
+}
+
+__global__ void assign_units_kernel(WsLayout L, const int32_t* __restrict__ ctx,
+                                    const int32_t* __restrict__ ql,
+                                    const uint8_t* __restrict__ mask, void* ws) {
+    const int32_t* header = ws_ptr<int32_t>(ws, L.off_header);
+    const int32_t* seq_u0 = ws_ptr<int32_t>(ws, L.off_seq_unit0);
+    int4* units = ws_ptr<int4>(ws, L.off_units);
+    int32_t* ntiles = ws_ptr<int32_t>(ws, L.off_ntiles);
+    int32_t* active = ws_ptr<int32_t>(ws, L.off_active);
+    const int lane = threadIdx.x & 31;
+    const int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int U = header[H_UNITS];
+    if (u >= U) return;
+    // sequence owning unit u: the last b with seq_u0[b] <= u
+    int lo = 0, hi = L.B;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (seq_u0[mid] <= u) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const int q_b = ql[b], c_b = ctx[b];
+    const int nqt = L.mode == PA_MODE_DECODE ? 1 : (int)ceil_div64(q_b, L.qtok);
+    const int local = u - seq_u0[b];
+    const int hk = local / nqt, qt = local % nqt;
+    int q0, nq;
+    int64_t keys;
+    if (L.mode == PA_MODE_DECODE) {
+        q0 = 0;
+        nq = q_b;
+        keys = nq > 0 ? c_b : 0;
+    } else {
+        q0 = qt * L.qtok;
+        nq = min(L.qtok, q_b - q0);
+        keys = (int64_t)c_b - q_b + q0 + nq;
+    }
+    const int nreach = (int)ceil_div64(keys, L.kv_tile);
+    int n = nreach;
+    if (L.has_mask) {
+        // active-KV-tile compaction: ballot the kept predicates of 32 tiles,
+        // popcount them, write each kept tile at its prefix rank
+        const int mq = q0 / kMaskTile;
+        const uint8_t* mrow = mask + ((int64_t)b * L.mask_q_tiles + mq) * L.mask_kv_tiles;
+        int32_t* out = active + (int64_t)u * L.max_kv_tiles;
+        int base = 0;
+        for (int k0 = 0; k0 < nreach; k0 += 32) {
+            const int kt = k0 + lane;
+            const bool keep = kt < nreach && kt < L.mask_kv_tiles && mq < L.mask_q_tiles &&
+                              mrow[kt] != 0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+            if (keep) out[base + __popc(bal & ((1u << lane) - 1u))] = kt;
+            base += __popc(bal);
+        }
+        n = base;
+    }
+    if (lane == 0) {
+        units[u] = make_int4(b, hk, q0, nq);
+        ntiles[u] = n;
+    }
+}
+
+__device__ __forceinline__ int64_t unit_weight(const WsLayout& L, int nq) {
+    int64_t w = ceil_div64((int64_t)L.G * nq, L.balance_rows);
+    return w < 1 ? 1 : w;
+}
+
+// Visit the CTAs owning tiles of a unit (cost prefix P, n tiles of weight w):
+// f(cta, t_lo, t_hi) for every CTA with at least one of them.
+template <typename F>
+__device__ __forceinline__ void for_each_owner(int64_t P, int n, int64_t w, int64_t C, int N,
+                                               F f) {
+    if (n <= 0) return;
+    const int64_t x0 = P, x1 = P + (int64_t)(n - 1) * w;
+    const int c0 = (int)(((x0 + 1) * N - 1) / C);
+    const int c1 = (int)(((x1 + 1) * N - 1) / C);
+    for (int c = c0; c <= c1; ++c) {
+        const int64_t a = (int64_t)c * C / N, a1 = (int64_t)(c + 1) * C / N;
+        const int64_t tlo = a <= P ? 0 : ceil_div64(a - P, w);
+        int64_t thi = ceil_div64(a1 - P, w);
+        if (thi > n) thi = n;
+        if (thi > tlo) f(c, (int)tlo, (int)thi);
+    }
+}
+
+__global__ void __launch_bounds__(kScanThreads) assign_map_kernel(WsLayout L, void* ws) {
+    __shared__ int64_t sm[32];
+    int32_t* header = ws_ptr<int32_t>(ws, L.off_header);
+    const int4* units = ws_ptr<int4>(ws, L.off_units);
+    const int32_t* ntiles = ws_ptr<int32_t>(ws, L.off_ntiles);
+    int64_t* prefix = ws_ptr<int64_t>(ws, L.off_prefix);
+    int32_t* nsplit = ws_ptr<int32_t>(ws, L.off_nsplit);
+    int32_t* slot0 = ws_ptr<int32_t>(ws, L.off_slot0);
+    int4* tasks = ws_ptr<int4>(ws, L.off_tasks);
+    int32_t* task_cta = ws_ptr<int32_t>(ws, L.off_task_cta);
+    int32_t* cta_ptr = ws_ptr<int32_t>(ws, L.off_cta_ptr);
+    int32_t* fix = ws_ptr<int32_t>(ws, L.off_fix);
+    const int U = header[H_UNITS];
+    const int N = L.N;
+    const int tid = threadIdx.x;
+    const int chunk = (U + kScanThreads - 1) / kScanThreads;
+    const int u0 = min(U, tid * chunk), u1 = min(U, u0 + chunk);
+
+    // cost prefix
+    int64_t cost = 0;
+    for (int u = u0; u < u1; ++u) cost += (int64_t)ntiles[u] * unit_weight(L, units[u].w);
+    int64_t C;
+    int64_t run = block_exscan(cost, &C, sm);
+    for (int u = u0; u < u1; ++u) {
+        prefix[u] = run;
+        run += (int64_t)ntiles[u] * unit_weight(L, units[u].w);
+    }
+
+    // tasks per unit, split slots, units the combine pass must finish
+    int64_t nt = 0, ns = 0, nf = 0;
+    for (int u = u0; u < u1; ++u) {
+        int S = 0;
+        for_each_owner(prefix[u], ntiles[u], unit_weight(L, units[u].w), C, N,
+                       [&](int, int, int) { ++S; });
+        nsplit[u] = S;
+        nt += S;
+        ns += S > 1 ? S : 0;
+        nf += (S != 1 && units[u].w > 0) ? 1 : 0;
+    }
+    int64_t T, Sl, F;
+    int64_t t_run = block_exscan(nt, &T, sm);
+    int64_t s_run = block_exscan(ns, &Sl, sm);
+    int64_t f_run = block_exscan(nf, &F, sm);
+    for (int u = u0; u < u1; ++u) {
+        const int S = nsplit[u];
+        const int s0 = S > 1 ? (int)s_run : -1;
+        slot0[u] = s0;
+        int k = 0;
+        for_each_owner(prefix[u], ntiles[u], unit_weight(L, units[u].w), C, N,
+                       [&](int c, int tlo, int thi) {
+                           tasks[t_run + k] = make_int4(u, tlo, thi, S > 1 ? s0 + k : -1);
+                           task_cta[t_run + k] = c;
+                           ++k;
+                       });
+        t_run += S;
+        s_run += S > 1 ? S : 0;
+        if (S != 1 && units[u].w > 0) fix[f_run++] = u;
+    }
+    __syncthreads();
+    // cta_ptr[c] = number of tasks owned by CTAs < c (task_cta is sorted)
+    for (int c = tid; c <= N; c += blockDim.x) {
+        int lo = 0, hi = (int)T;
+        while (lo < hi) {
+            int mid = (lo + hi) >> 1;
+            if (task_cta[mid] < c) lo = mid + 1; else hi = mid;
+        }
+        cta_ptr[c] = lo;
+    }
+    if (tid == 0) {
+        header[H_TASKS] = (int32_t)T;
+        header[H_SLOTS] = (int32_t)Sl;
+        header[H_FIX] = (int32_t)F;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_assign(const WsLayout& L, const int32_t* ctx, const int32_t* ql,
+                          const uint8_t* mask, void* ws, cudaStream_t stream) {
+    assign_seq_kernel<<<1, kScanThreads, 0, stream>>>(L, ctx, ql, ws);
+    const int warps = 8;
+    const int grid = (L.unit_cap + warps - 1) / warps;
+    assign_units_kernel<<<grid > 0 ? grid : 1, warps * 32, 0, stream>>>(L, ctx, ql, mask, ws);
+    assign_map_kernel<<<1, kScanThreads, 0, stream>>>(L, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

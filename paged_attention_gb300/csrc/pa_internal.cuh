@@ -1,0 +1,213 @@
+// pa_internal.cuh -- shared definitions of the CUDA library (not part of the ABI).
+//
+// Workspace layout of the Assign pass, launch-parameter structs and thin
+// inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
+// ldmatrix, mma.sync, tcgen05 and fast exp2/log2.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// ------------------------------------------------------------ constants
+
+constexpr int kDecodeTile = 64;      // KV tokens per decode tile
+constexpr int kPrefillTile = 128;    // KV tokens per prefill tile (= mask tile)
+constexpr int kPrefillRows = 128;    // rows (query token x head) per prefill q tile
+constexpr int kMaskTile = 128;       // block-mask tile edge
+constexpr int kDefaultBalanceRows = 128;
+constexpr int kHeaderWords = 64;
+
+// header word indices inside the Assign workspace
+enum HeaderWord {
+    H_UNITS = 0,
+    H_TASKS = 1,
+    H_SLOTS = 2,
+    H_CTAS = 3,
+    H_ERROR = 4,
+    H_FIX = 5,
+    H_MODE = 6,
+};
+
+// Byte offsets of every array inside the Assign workspace.  Computed on the
+// host from the problem (layout_for) and passed to every kernel by value.
+struct WsLayout {
+    int32_t mode;
+    int32_t B, Hq, Hkv, G, D;
+    int32_t N;            // persistent CTAs
+    int32_t kv_tile;      // 64 decode / 128 prefill
+    int32_t qtok;         // query tokens per unit (prefill: 128/G; decode: all)
+    int32_t unit_cap;
+    int32_t task_cap;
+    int32_t max_kv_tiles; // row stride of the active-tile lists
+    int32_t has_mask;
+    int32_t rows_cap;     // partial rows per slot
+    int32_t balance_rows;
+    int32_t total_q;
+    int32_t max_q_len, max_ctx;
+    int32_t mask_q_tiles, mask_kv_tiles;
+    int64_t off_header, off_cta_ptr, off_tasks, off_task_cta, off_units, off_ntiles,
+        off_prefix, off_nsplit, off_slot0, off_task0, off_fix, off_active, off_cu_q,
+        off_seq_unit0;
+    int64_t total_bytes;
+    int64_t partial_slots;
+    int64_t partial_bytes;
+};
+
+// fills `L` for (problem, mode, N); returns false on invalid dims
+bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L);
+
+template <typename T>
+__host__ __device__ inline T* ws_ptr(void* ws, int64_t off) {
+    return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
+}
+template <typename T>
+__host__ __device__ inline const T* ws_ptr(const void* ws, int64_t off) {
+    return reinterpret_cast<const T*>(reinterpret_cast<const char*>(ws) + off);
+}
+
+// ------------------------------------------------------- device helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void set_device_error(int32_t* header, int code) {
+    atomicOr(header + H_ERROR, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// mbarrier ----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: spins until the phase with `parity` completes or `limit_ns`
+// elapses.  Returns false on timeout (the caller records the error and
+// carries on without the data, so no wait can hang the GPU).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && globaltimer() - t0 > limit_ns) return false;
+    }
+}
+
+// TMA ----------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Named barriers (ids 1..15; id 0 is __syncthreads) -------------------------
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ldmatrix / mma.sync -------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Hardware base-2 exponential / logarithm (MUFU), flushing denormals.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Two E4M3 bytes (low byte first) -> packed bf16x2 (exact: every E4M3 value
+// is representable in bf16).  E4M3 -> f16 is an exact hardware conversion.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+    __half2 hh = *reinterpret_cast<__half2*>(&h2);
+    float2 f = __half22float2(hh);
+    return pack_bf16x2(f.x, f.y);
+}
+
+}  // namespace pa

@@ -1,0 +1,83 @@
+"""The C-ABI library builds, loads on the host and exports every entry point
+declared in include/pa.h; host-side validation works without a GPU (only
+calls that never reach the device are made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_attention_gb300 import binding as B
+from paged_attention_gb300 import build as build_mod
+from paged_attention_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "pa.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("pa_assign", "pa_decode_splitk", "pa_combine", "pa_prefill"):
+        assert name in syms
+    assert set(syms) == set(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert B.status_string(0) == "PA_OK"
+    assert B.status_string(3) == "PA_ERR_WORKSPACE"
+    assert "sm_103a" in B.pa_version()
+
+
+def test_workspace_sizes_host_only(lib):
+    w = W.decode_bf16(mtp=1, shrink=16)
+    p = B.problem_from(w, num_ctas=152)
+    a = B.pa_assign_workspace_size(p, B.PA_MODE_DECODE)
+    part = B.pa_partial_workspace_size(p, B.PA_MODE_DECODE)
+    assert a > 0 and a % 256 == 0
+    # partial slots = units + CTAs, rows rounded to 16, (D + 1) floats per row
+    U = w.num_seqs * w.num_kv_heads
+    assert part == (U + 152) * 16 * (128 + 1) * 4
+    wp = W.prefill_bf16(sparse=True, shrink=32)
+    pp = B.problem_from(wp, num_ctas=152)
+    assert B.pa_assign_workspace_size(pp, B.PA_MODE_PREFILL) > 0
+    assert B.pa_partial_workspace_size(pp, B.PA_MODE_PREFILL) % (128 * 129 * 4) == 0
+
+
+def test_invalid_problems_rejected_on_host(lib):
+    w = W.decode_bf16(mtp=1, shrink=16)
+    p = B.problem_from(w, num_ctas=8)
+    bad = B.PaProblem.from_buffer_copy(p)
+    bad.num_kv_heads = 7                      # Hq % Hkv != 0
+    assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0
+    bad = B.PaProblem.from_buffer_copy(p)
+    bad.head_dim = 96                         # not built
+    assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0
+    bad = B.PaProblem.from_buffer_copy(p)
+    bad.max_context_len = max(bad.max_context_len, 17)
+    bad.max_q_len = 17                        # G * q_len = 68 rows > 64 per decode unit
+    assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0
+    bad = B.PaProblem.from_buffer_copy(p)
+    bad.mask_q_tiles, bad.mask_kv_tiles = 1, 1  # masks are prefill-only
+    assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0
+    bad = B.PaProblem.from_buffer_copy(p)
+    bad.page_size = 48
+    assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0
+    # null device pointers are refused before any CUDA call
+    st = lib.pa_assign(ctypes.byref(p), 0, None, None, None, None, 0, None)
+    assert st == 1

@@ -1,0 +1,74 @@
+"""GPU Assign task maps and active-tile lists are bit-exact with the oracle's.
+
+"基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2 Assign (load-balanced task
+map) and 二.1 (active-KV-tile compaction of the block mask)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_attention_gb300 import binding as B
+from paged_attention_gb300 import workloads as W
+
+from gpu_util import task_map_equal
+
+pytestmark = pytest.mark.gpu
+
+
+def check(w, mode, num_ctas=0, balance_rows=0):
+    wd = w.to("cuda")
+    bufs = B.make_buffers(wd, mode, num_ctas=num_ctas, balance_rows=balance_rows)
+    N = B.pa_num_ctas(bufs.problem, mode)
+    B.pa_assign(bufs.problem, mode, wd.context_lens, wd.q_lens,
+                wd.block_mask if mode == B.PA_MODE_PREFILL else None, bufs.assign_ws)
+    gpu = B.pa_read_task_map(bufs.problem, mode, bufs.assign_ws)
+    assert B.pa_last_device_error(bufs.assign_ws) == 0
+    tm = oracle.assign(mode, w.num_seqs, w.num_q_heads, w.num_kv_heads, N,
+                       64 if mode == B.PA_MODE_DECODE else 128,
+                       balance_rows or 128, w.context_lens, w.q_lens,
+                       w.block_mask if mode == B.PA_MODE_PREFILL else None)
+    task_map_equal(gpu, tm, with_active=(mode == B.PA_MODE_PREFILL and w.block_mask is not None))
+    return gpu
+
+
+@pytest.mark.parametrize("mtp", [1, 2, 3])
+def test_decode_map_full_size(mtp):
+    check(W.decode_bf16(mtp=mtp), B.PA_MODE_DECODE)
+
+
+def test_decode_map_fp8_full_size():
+    check(W.decode_fp8(), B.PA_MODE_DECODE)
+
+
+@pytest.mark.parametrize("n", [1, 7, 152, 1000])
+def test_decode_map_any_cta_count(n):
+    check(W.decode_bf16(mtp=1, shrink=8), B.PA_MODE_DECODE, num_ctas=n)
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_prefill_map_full_size(sparse):
+    check(W.prefill_bf16(sparse=sparse), B.PA_MODE_PREFILL)
+
+
+def test_hybrid_map_full_size():
+    check(W.hybrid_bf16(), B.PA_MODE_PREFILL)
+
+
+@pytest.mark.parametrize("rbal", [16, 64, 288])
+def test_weighted_map(rbal):
+    check(W.hybrid_bf16(shrink=8), B.PA_MODE_PREFILL, balance_rows=rbal)
+
+
+def test_tiny_mixed_map():
+    check(W.tiny_mixed(), B.PA_MODE_PREFILL, num_ctas=5)
+
+
+def test_bad_lengths_flagged():
+    w = W.decode_bf16(mtp=1, shrink=16).to("cuda")
+    bufs = B.make_buffers(w, B.PA_MODE_DECODE)
+    ql = w.q_lens.clone()
+    ql[0] = int(w.context_lens[0]) + 1          # more new tokens than context
+    B.pa_assign(bufs.problem, B.PA_MODE_DECODE, w.context_lens, ql, None, bufs.assign_ws)
+    assert B.pa_last_device_error(bufs.assign_ws) & B.PA_DEV_BAD_LENGTHS
+    gpu = B.pa_read_task_map(bufs.problem, B.PA_MODE_DECODE, bufs.assign_ws)
+    assert gpu["num_units"] == 0 and gpu["num_tasks"] == 0

@@ -1,0 +1,109 @@
+"""GPU split-K decode (Assign + Split-K + Combine) against the fp64 oracle.
+
+"基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2 (Dynamic Split-K decode,
+Combine equal to full attention), 三.1 (GQA x MTP rows share a KV tile).
+Tolerances: bf16 outputs max-abs 2e-2, LSE 1e-3, FP8-KV outputs 6e-2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_attention_gb300 import binding as B
+from paged_attention_gb300 import workloads as W
+
+from gpu_util import compare
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_compare(w, rows=None, num_ctas=0):
+    wd = w.to("cuda")
+    bufs = B.make_buffers(wd, B.PA_MODE_DECODE, num_ctas=num_ctas)
+    B.run_decode(wd, bufs)
+    torch.cuda.synchronize()
+    assert B.pa_last_device_error(bufs.assign_ws) == 0
+    ref_o, ref_l = oracle.attention(w, rows=rows)
+    return compare(w, bufs.out, bufs.lse, ref_o, ref_l, rows=rows), bufs
+
+
+@pytest.mark.parametrize("mtp", [1, 2, 3])
+def test_decode_bf16_shrunk(mtp):
+    run_and_compare(W.decode_bf16(mtp=mtp, shrink=16))
+
+
+def test_decode_fp8_shrunk():
+    run_and_compare(W.decode_fp8(shrink=16))
+
+
+@pytest.mark.parametrize("n", [1, 3, 37, 500])
+def test_decode_any_cta_count(n):
+    """Many / few CTAs change how units split; the result must not change."""
+    run_and_compare(W.decode_bf16(mtp=2, shrink=16), num_ctas=n)
+
+
+def test_decode_mixed_edge_cases():
+    # ctx < page, ctx a page multiple, ctx = ql, one long sequence, q_len 0
+    ctx = [1, 5, 64, 128, 129, 4, 3000, 63]
+    ql = [1, 5, 2, 4, 1, 4, 3, 0]
+    w = W.make_workload("edge", ctx, ql, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                        page_size=64, seed=21)
+    run_and_compare(w, num_ctas=11)
+
+
+@pytest.mark.parametrize("ps,layout", [(16, W.NHD), (32, W.HND), (128, W.NHD), (256, W.HND)])
+def test_decode_page_sizes_and_layouts(ps, layout):
+    w = W.make_workload("pages", [33, 700, 1025, 64, 2], [1, 2, 1, 2, 1], num_q_heads=8,
+                        num_kv_heads=2, head_dim=128, page_size=ps, layout=layout, seed=ps)
+    run_and_compare(w, num_ctas=13)
+
+
+def test_decode_head_dim_64_and_gqa_variants():
+    w = W.make_workload("d64", [300, 17, 4096], [2, 1, 4], num_q_heads=8, num_kv_heads=1,
+                        head_dim=64, page_size=16, seed=5)
+    run_and_compare(w, num_ctas=9)
+    w = W.make_workload("mha", [300, 17], [1, 1], num_q_heads=4, num_kv_heads=4, head_dim=128,
+                        page_size=64, seed=6)
+    run_and_compare(w)
+
+
+def test_decode_rows_up_to_64():
+    w = W.make_workload("rows64", [500, 90], [8, 5], num_q_heads=16, num_kv_heads=2,
+                        head_dim=128, page_size=64, seed=8)
+    run_and_compare(w, num_ctas=10)
+
+
+def test_decode_fp8_mtp4_and_small_pages():
+    w = W.make_workload("fp8b", [100, 1000, 2049], [4, 4, 4], num_q_heads=32, num_kv_heads=4,
+                        head_dim=128, page_size=16, layout=W.NHD, kv_dtype=W.FP8_E4M3, seed=9)
+    run_and_compare(w, num_ctas=7)
+
+
+def test_decode_bf16_full_size_mtp1():
+    """The benchmark workload, in the launch configuration the bench times,
+    checked on every row."""
+    run_and_compare(W.decode_bf16(mtp=1))
+
+
+def test_decode_fp8_full_size_sampled():
+    w = W.decode_fp8()
+    rng = np.random.default_rng(3)
+    rows = np.sort(rng.choice(w.total_q * w.num_q_heads, size=4096, replace=False))
+    run_and_compare(w, rows=rows)
+
+
+def test_decode_is_deterministic():
+    w = W.decode_bf16(mtp=3, shrink=8).to("cuda")
+    a = B.run_decode(w)
+    o1, l1 = a.out.clone(), a.lse.clone()
+    B.run_decode(w, a)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, a.out) and torch.equal(l1, a.lse)
+
+
+def test_bad_page_is_reported_not_faulted():
+    w = W.decode_bf16(mtp=1, shrink=16)
+    w.block_table[1, 0] = w.num_pages + 100   # out of the pool
+    wd = w.to("cuda")
+    bufs = B.run_decode(wd)
+    torch.cuda.synchronize()
+    assert B.pa_last_device_error(bufs.assign_ws) & B.PA_DEV_BAD_PAGE
