@@ -46,18 +46,20 @@ def load_peaks():
 
 
 def make_workload(name: str, rank: int):
+    """The workload's batch for `rank`: every rank draws its own independent
+    batch of the same shape (weak scaling)."""
     from paged_attention_gb300 import workloads as W
-    seed_off = 7919 * rank
+    from paged_attention_gb300.dist import rank_seed
     if name == "decode_bf16":
-        return W.decode_bf16(mtp=1, seed=1002 + seed_off)
+        return W.decode_bf16(mtp=1, seed=rank_seed(1002, rank))
     if name == "decode_fp8":
-        return W.decode_fp8(seed=1003 + seed_off)
+        return W.decode_fp8(seed=rank_seed(1003, rank))
     if name == "prefill_dense":
-        return W.prefill_bf16(sparse=False, seed=1004 + seed_off)
+        return W.prefill_bf16(sparse=False, seed=rank_seed(1004, rank))
     if name == "prefill_sparse":
-        return W.prefill_bf16(sparse=True, seed=1004 + seed_off)
+        return W.prefill_bf16(sparse=True, seed=rank_seed(1004, rank))
     if name == "hybrid":
-        return W.hybrid_bf16(seed=1005 + seed_off)
+        return W.hybrid_bf16(seed=rank_seed(1005, rank))
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -99,7 +101,7 @@ class ClockSampler:
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                   "-lms", "200"]
+                   "-lms", "50"]
             if self.uuid:
                 cmd += ["-i", self.uuid]
             self.fh = open(self.path, "w")
@@ -288,10 +290,8 @@ def run_native(args, rank, world, dist):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     clk = clocks.stop()
     if dist is not None:
-        import torch.distributed as tdist
-        t = torch.tensor([ms, e2e_ms, kern_ms], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms, e2e_ms, kern_ms = (float(x) for x in t)
+        from paged_attention_gb300.dist import max_over_ranks
+        ms, e2e_ms, kern_ms = max_over_ranks([ms, e2e_ms, kern_ms])
     if B.pa_last_device_error(bufs.assign_ws) != 0:
         raise SystemExit("device error during the timed region")
 
@@ -392,7 +392,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode_bf16",

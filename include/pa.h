@@ -78,7 +78,9 @@ enum { PA_NHD = 0, PA_HND = 1 };
 enum { PA_BF16 = 0, PA_FP8_E4M3 = 1 };
 /* Assign modes.
  *   PA_MODE_DECODE:  one unit per (sequence, KV head) holding all q_lens[b]
- *                    queries (G*q_len rows, at most 64); 64-token KV tiles.
+ *                    queries (G*max_q_len rows: at most 32 for head_dim 128,
+ *                    64 for head_dim 64; larger groups use the prefill
+ *                    mode); 64-token KV tiles.
  *   PA_MODE_PREFILL: one unit per (sequence, KV head, q tile of 128/G tokens)
  *                    = one 128-row tile; 128-token KV tiles; block mask
  *                    allowed.  Used by pa_prefill for prefill and mixed

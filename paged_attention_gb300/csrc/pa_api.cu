@@ -17,13 +17,13 @@ cudaError_t launch_assign(const WsLayout& L, const int32_t* ctx, const int32_t* 
 cudaError_t launch_combine(const WsLayout& L, const void* ws, const void* partial, void* out,
                            float* lse, int grid, cudaStream_t stream);
 int decode_smem_bytes(int D, int RT, bool fp8);
-int decode_threads(int RT);
+int decode_threads(int D, int RT, bool fp8);
 const void* decode_kernel_ptr(int D, int RT, bool fp8);
 cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int RT,
-                                   const void* q, const CUtensorMap& tk, const CUtensorMap& tv,
-                                   const int32_t* block_table, const int32_t* ctx,
-                                   const int32_t* ql, const float* ks, const float* vs,
-                                   void* ws, void* partial, void* out, float* lse,
+                                   const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const int32_t* block_table,
+                                   const int32_t* ctx, const int32_t* ql, const float* ks,
+                                   const float* vs, void* ws, void* partial, void* out, float* lse,
                                    cudaStream_t stream);
 int prefill_smem_bytes(int D, bool fp8);
 const void* prefill_kernel_ptr(int D, bool fp8);
@@ -104,8 +104,8 @@ pa_status check_problem(const pa_problem* pp, int mode) {
     if (mode == PA_MODE_DECODE) {
         if (p.mask_q_tiles > 0) return PA_ERR_INVALID_ARG;   // masks are a prefill feature
         const int RT = decode_row_tiles(p);
-        if (RT < 0) return PA_ERR_UNSUPPORTED;
-        if (p.kv_dtype == PA_FP8_E4M3 && (p.head_dim != 128 || RT > 2)) return PA_ERR_UNSUPPORTED;
+        if (RT < 0 || (p.head_dim == 128 && RT > 2)) return PA_ERR_UNSUPPORTED;
+        if (p.kv_dtype == PA_FP8_E4M3 && p.head_dim != 128) return PA_ERR_UNSUPPORTED;
     } else {
         if (G > 128 || 128 % G != 0) return PA_ERR_UNSUPPORTED;
         if (p.kv_dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
@@ -124,11 +124,11 @@ int resolve_ctas(const pa_problem& p, int mode) {
         const int RT = decode_row_tiles(p);
         k = decode_kernel_ptr(p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3);
         smem = decode_smem_bytes(p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3);
-        threads = decode_threads(RT);
+        threads = decode_threads(p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3);
     } else {
         k = prefill_kernel_ptr(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
         smem = prefill_smem_bytes(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
-        threads = 256;
+        threads = 192;
     }
     if (k && smem > 0) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -177,8 +177,8 @@ bool encode_kv_map(const pa_problem& p, const void* base, CUtensorMap* map) {
     return r == CUDA_SUCCESS;
 }
 
-// Q viewed as (d, head, token): box = 64 elements x G heads x (128/G) tokens
-bool encode_q_map(const pa_problem& p, const void* base, CUtensorMap* map) {
+// Q viewed as (d, head, token): box = 64 elements x G heads x box_tokens tokens
+bool encode_q_map(const pa_problem& p, const void* base, int box_tokens, CUtensorMap* map) {
     auto fn = encode_fn();
     if (!fn) return false;
     const int G = p.num_q_heads / p.num_kv_heads;
@@ -186,7 +186,7 @@ bool encode_q_map(const pa_problem& p, const void* base, CUtensorMap* map) {
     const cuuint64_t T = p.total_q_tokens > 0 ? p.total_q_tokens : 1;
     cuuint64_t dims[3] = {D, Hq, T};
     cuuint64_t strides[2] = {D * 2, Hq * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kPrefillRows / G)};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)box_tokens};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -339,10 +339,11 @@ pa_status pa_decode_splitk(const pa_problem* problem, const void* q, const void*
     if (partial_ws_bytes < (size_t)L.partial_bytes || (!partial_ws && L.partial_bytes > 0) ||
         !aligned(partial_ws, 16))
         return PA_ERR_WORKSPACE;
-    CUtensorMap tk, tv;
-    if (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv))
+    CUtensorMap tq, tk, tv;
+    if (!encode_q_map(p, q, p.max_q_len > 0 ? p.max_q_len : 1, &tq) ||
+        !encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv))
         return PA_ERR_INVALID_ARG;
-    cudaError_t e = launch_decode_from_api(p, L, decode_row_tiles(p), q, tk, tv, block_table,
+    cudaError_t e = launch_decode_from_api(p, L, decode_row_tiles(p), tq, tk, tv, block_table,
                                            context_lens, q_lens, k_scale, v_scale,
                                            const_cast<void*>(assign_ws), partial_ws, out, lse,
                                            (cudaStream_t)stream);
@@ -387,7 +388,8 @@ pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cac
         return PA_ERR_WORKSPACE;
     if (p.total_q_tokens == 0) return PA_OK;
     CUtensorMap tq, tk, tv;
-    if (!encode_q_map(p, q, &tq) || !encode_kv_map(p, k_cache, &tk) ||
+    if (!encode_q_map(p, q, kPrefillRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
+        !encode_kv_map(p, k_cache, &tk) ||
         !encode_kv_map(p, v_cache, &tv))
         return PA_ERR_INVALID_ARG;
     cudaError_t e = launch_prefill_from_api(p, L, q, tq, tk, tv, block_table, context_lens,

@@ -10,20 +10,26 @@
 // multi-stage shared-memory ring guarded by full/empty barriers).
 //
 // GB300 design.  One CTA per SM (persistent grid = Assign's CTA count):
-//   warp 0            TMA producer.  Page ids for the next 32 pages are read
-//                     with one coalesced warp load; each 64-token tile is one
-//                     (or, for smaller pages, several) TMA box per 128-byte
-//                     column block of K and of V, landing 128-byte swizzled.
-//   warps 1..4*RT     consumers.  Warp (rt, ts) owns rows [16rt, 16rt+16) of
-//                     the unit and tokens [16ts, 16ts+16) of every tile, and
-//                     keeps its own online-softmax state (m, l, O) in
-//                     registers; S = Q K^T and O += P V run on mma.sync
-//                     (bf16 in, fp32 accumulate), P stays in registers.
-//                     At the end of a task the four token slices of a row
-//                     tile merge their states through shared memory.
-// The work is HBM-bound (<= 48 flop per KV byte at 64 rows of FP8), so
-// tensor-core mma.sync is far from the limit; what matters is keeping enough
-// K/V bytes in flight per SM, which the ring does.
+//   warp 0            TMA producer.  Per task it loads the unit's Q rows
+//                     (G heads x q_len tokens) into one of two Q slots; per
+//                     64-token KV tile it reads the page ids (32 at a time,
+//                     one coalesced warp load) and issues one TMA box per
+//                     page and 128-byte column block of K and of V into a
+//                     multi-stage ring (128-byte swizzle).
+//   warps 1..         consumers, NG groups x RT row tiles x 4 token slices.
+//                     Group g takes the CTA's tiles with index % NG == g, so
+//                     NG tiles are in flight at once.  Warp (g, rt, ts) owns
+//                     rows [16rt, 16rt+16) of the unit and tokens
+//                     [16ts, 16ts+16) of its tiles; S = Q K^T and O += P V run
+//                     on mma.sync (bf16 in, fp32 accumulate, P stays in
+//                     registers), with a lazily moved running max (O is
+//                     rescaled only when the max grows by more than 2^8).  At
+//                     the end of a task the NG x 4 slices of each row tile
+//                     merge their (m, l, O) through shared memory.
+// The work is HBM-bound (<= 48 flop per KV byte even at 64 rows of FP8), so
+// mma.sync is far from its limit; what matters is enough K/V bytes in flight
+// per SM (the ring) and enough independent warps to hide the MMA / shuffle
+// latency chains (the groups).
 // FP8 (E4M3) K/V: each consumer converts its share of the tile to bf16 in a
 // double-buffered per-slice buffer (exact), k_scale folds into the softmax
 // scale, v_scale into P.
@@ -33,7 +39,6 @@ namespace pa {
 
 struct DecodeParams {
     WsLayout L;
-    const __nv_bfloat16* q;
     const int32_t* block_table;
     const int32_t* ctx;
     const int32_t* ql;
@@ -49,55 +54,70 @@ struct DecodeParams {
     int32_t max_pages_per_seq;
     int32_t rows_per_box;     // min(page_size, 64)
     int32_t boxes_per_tile;   // 64 / rows_per_box
+    int32_t q_box_tokens;     // tokens per Q TMA box (max q_len)
     float sm_scale;
     uint64_t wait_limit_ns;
 };
 
-template <int D, int RT, bool FP8, int STAGES>
+template <int D, int RT, bool FP8, int NG, int STAGES>
 struct DecodeCfg {
-    static constexpr int kWarps = 1 + 4 * RT;
+    static constexpr int kGroupWarps = 4 * RT;
+    static constexpr int kConsumerWarps = kGroupWarps * NG;
+    static constexpr int kWarps = 1 + kConsumerWarps;
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int kElem = FP8 ? 1 : 2;
-    static constexpr int kHalves = D * kElem / 128;          // 128-B column blocks of a row
+    static constexpr int kHalves = D * kElem / 128;          // 128-B column blocks of a K/V row
     static constexpr int kHalfBytes = kDecodeTile * 128;      // one column block of a tile
     static constexpr int kKBytes = kHalves * kHalfBytes;
     static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kQRows = 16 * RT;
+    static constexpr int kQHalves = D / 64;                   // Q is bf16
+    static constexpr int kQHalfBytes = kQRows * 128;
+    static constexpr int kQSlotBytes = kQHalves * kQHalfBytes;
     static constexpr int kCvtHalves = D * 2 / 128;           // bf16 column blocks
     static constexpr int kCvtHalfBytes = 16 * 128;
     static constexpr int kCvtKBytes = kCvtHalves * kCvtHalfBytes;
     static constexpr int kCvtBuf = 2 * kCvtKBytes;           // K + V of one slice
     static constexpr int kCvtTotal = FP8 ? 4 * 2 * kCvtBuf : 0;
     static constexpr int kMergeFloats = 16 * D + 32;
-    static constexpr int kMergeBytes = 4 * RT * kMergeFloats * 4;
+    static constexpr int kMergeBytes = kConsumerWarps * kMergeFloats * 4;
     static constexpr int kScaleBytes = FP8 ? STAGES * 2 * 4 * 4 : 0;
-    static constexpr int kOffCvt = STAGES * kStageBytes;
+    static constexpr int kOffQ = STAGES * kStageBytes;
+    static constexpr int kOffCvt = kOffQ + 2 * kQSlotBytes;
     static constexpr int kOffMerge = kOffCvt + kCvtTotal;
     static constexpr int kOffScale = kOffMerge + kMergeBytes;
     static constexpr int kOffBar = (kOffScale + kScaleBytes + 15) / 16 * 16;
-    static constexpr int kSmemBytes = kOffBar + 2 * STAGES * 8 + 16 + 1024;
+    static constexpr int kNumBars = 2 * STAGES + 4;
+    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(!FP8 || D == 128, "FP8 decode is built for head_dim 128");
+    static_assert(!FP8 || NG == 1, "FP8 decode uses one tile group");
+    static_assert(kQHalfBytes % 1024 == 0, "Q slot alignment");
+    static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D, int RT, bool FP8, int STAGES>
-__global__ void __launch_bounds__(32 * (1 + 4 * RT), 1)
-decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap tmk,
-              const __grid_constant__ CUtensorMap tmv) {
-    using Cfg = DecodeCfg<D, RT, FP8, STAGES>;
+template <int D, int RT, bool FP8, int NG, int STAGES>
+__global__ void __launch_bounds__(32 * (1 + 4 * RT * NG), 1)
+decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap tmq,
+              const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    using Cfg = DecodeCfg<D, RT, FP8, NG, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
     uint64_t* empty = full + STAGES;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
+    uint64_t* q_full = empty + STAGES;       // 2 slots
+    uint64_t* q_empty = q_full + 2;          // 2 slots
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
     float* scales = reinterpret_cast<float*>(smem + Cfg::kOffScale);   // [stage][k|v][box]
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t lim = P.wait_limit_ns;
 
     if (header[H_CTAS] != (int)gridDim.x) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(header, PA_DEV_BAD_LENGTHS);
@@ -106,12 +126,24 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 4 * RT);
+            mbar_init(&empty[s], Cfg::kGroupWarps);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], Cfg::kConsumerWarps);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
+
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (*abort_flag) return;
+        if (!mbar_wait(bar, parity, lim)) {
+            *abort_flag = 1;
+            set_device_error(header, PA_DEV_WAIT_TIMEOUT);
+        }
+    };
 
     const int32_t* cta_ptr = ws_ptr<int32_t>(P.ws, L.off_cta_ptr);
     const int4* tasks = ws_ptr<int4>(P.ws, L.off_tasks);
@@ -123,27 +155,41 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     if (warp == 0) {
         // ------------------------------------------------------- producer
         if (lane == 0) {
+            prefetch_tmap(&tmq);
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
         }
         const int ps = P.page_size, rpb = P.rows_per_box, nbox = P.boxes_per_tile;
         const uint32_t box_bytes = (uint32_t)rpb * 128u * Cfg::kHalves;
-        int it = 0;
-        for (int k = k_begin; k < k_end; ++k) {
+        const uint32_t q_bytes = (uint32_t)Cfg::kQHalves * G * P.q_box_tokens * 128u;
+        int it = 0, task_it = 0;
+        for (int k = k_begin; k < k_end; ++k, ++task_it) {
             const int4 tk = tasks[k];
             const int4 un = units[tk.x];
             const int b = un.x, hk = un.y;
             const int ctx_b = P.ctx[b];
             const int npg = (ctx_b + ps - 1) / ps;
             const int32_t* bt_row = P.block_table + (int64_t)b * P.max_pages_per_seq;
+            // Q rows of the unit into slot task_it & 1
+            const int qs = task_it & 1;
+            wait(&q_empty[qs], (uint32_t)((task_it >> 1) & 1) ^ 1u);
+            if (lane == 0) {
+                if (*abort_flag) {
+                    mbar_arrive(&q_full[qs]);
+                } else {
+                    mbar_arrive_expect_tx(&q_full[qs], q_bytes);
+                    uint8_t* qdst = smem + Cfg::kOffQ + qs * Cfg::kQSlotBytes;
+#pragma unroll
+                    for (int h = 0; h < Cfg::kQHalves; ++h)
+                        tma_load_3d(qdst + h * Cfg::kQHalfBytes, &tmq, &q_full[qs], 64 * h, hk * G,
+                                    cu_q[b] + un.z);
+                }
+            }
+            __syncwarp();
             int win_lo = -(1 << 30), win_val = -1;
             for (int t = tk.y; t < tk.z; ++t, ++it) {
                 const int s = it % STAGES;
-                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                if (!*abort_flag && !mbar_wait(&empty[s], ph ^ 1u, P.wait_limit_ns)) {
-                    *abort_flag = 1;
-                    set_device_error(header, PA_DEV_WAIT_TIMEOUT);
-                }
+                wait(&empty[s], (uint32_t)((it / STAGES) & 1) ^ 1u);
                 const int kt = t;
                 int pg[4];
                 uint32_t bytes = 0;
@@ -182,16 +228,16 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                     } else {
                         mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (pg[j] < 0) continue;
-                            const int slot0 = (kt * kDecodeTile + j * rpb) % ps;
+                        for (int kv = 0; kv < 2; ++kv) {
 #pragma unroll
-                            for (int h = 0; h < Cfg::kHalves; ++h) {
-                                const int off = h * Cfg::kHalfBytes + j * rpb * 128;
-                                tma_load_4d(stK + off, &tmk, &full[s], h * (128 / Cfg::kElem),
-                                            slot0, hk, pg[j]);
-                                tma_load_4d(stV + off, &tmv, &full[s], h * (128 / Cfg::kElem),
-                                            slot0, hk, pg[j]);
+                            for (int j = 0; j < 4; ++j) {
+                                if (pg[j] < 0) continue;
+                                const int slot0 = (kt * kDecodeTile + j * rpb) % ps;
+#pragma unroll
+                                for (int h = 0; h < Cfg::kHalves; ++h)
+                                    tma_load_4d((kv ? stV : stK) + h * Cfg::kHalfBytes + j * rpb * 128,
+                                                kv ? &tmv : &tmk, &full[s], h * (128 / Cfg::kElem),
+                                                slot0, hk, pg[j]);
                             }
                         }
                     }
@@ -201,12 +247,14 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         }
     } else {
         // ------------------------------------------------------- consumers
-        const int cw = warp - 1, rt = cw >> 2, ts = cw & 3;
+        const int cw = warp - 1;
+        const int grp = cw / Cfg::kGroupWarps;
+        const int rt = (cw % Cfg::kGroupWarps) >> 2, ts = cw & 3;
         const int g = lane >> 2, q4 = lane & 3;
         const float scale_log2 = P.sm_scale * kLog2e;
         float* merge = reinterpret_cast<float*>(smem + Cfg::kOffMerge);
-        int it = 0;
-        for (int k = k_begin; k < k_end; ++k) {
+        int it = 0, task_it = 0;
+        for (int k = k_begin; k < k_end; ++k, ++task_it) {
             const int4 tk = tasks[k];
             const int4 un = units[tk.x];
             const int b = un.x, hk = un.y, q0 = un.z, nq = un.w;
@@ -218,21 +266,22 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
             const bool v_lo = r_lo < R, v_hi = r_hi < R;
             const int p_lo = pbase + r_lo / G, p_hi = pbase + r_hi / G;
 
+            // Q fragments (A operand, rows x D) from the TMA-filled slot
             uint32_t qf[D / 16][4];
+            {
+                const int qs = task_it & 1;
+                wait(&q_full[qs], (uint32_t)((task_it >> 1) & 1));
+                const uint32_t qbase = smem_u32(smem + Cfg::kOffQ + qs * Cfg::kQSlotBytes);
+                const int mi = lane >> 3;
+                const int row = 16 * rt + 8 * (mi & 1) + (lane & 7);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-                for (int reg = 0; reg < 4; ++reg) {
-                    const int row = (reg & 1) ? r_hi : r_lo;
-                    const int d = 16 * kk + 2 * q4 + ((reg >> 1) ? 8 : 0);
-                    uint32_t v = 0;
-                    if (row < R) {
-                        const int64_t off =
-                            ((int64_t)(tok_base + row / G) * Hq + hk * G + row % G) * D + d;
-                        v = __ldg(reinterpret_cast<const uint32_t*>(P.q + off));
-                    }
-                    qf[kk][reg] = v;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int ch = 2 * kk + (mi >> 1);
+                    ldsm_x4(qbase + (ch >> 3) * Cfg::kQHalfBytes + swz(row, ch & 7), qf[kk][0],
+                            qf[kk][1], qf[kk][2], qf[kk][3]);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_empty[qs]);
             }
             float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
             float o[D / 8][4];
@@ -240,12 +289,9 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
             for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
             for (int t = tk.y; t < tk.z; ++t, ++it) {
+                if (NG > 1 && (it % NG) != grp) continue;
                 const int s = it % STAGES;
-                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                if (!*abort_flag && !mbar_wait(&full[s], ph, P.wait_limit_ns)) {
-                    *abort_flag = 1;
-                    set_device_error(header, PA_DEV_WAIT_TIMEOUT);
-                }
+                wait(&full[s], (uint32_t)((it / STAGES) & 1));
                 const int kt = t;
                 const int tok_s0 = kt * kDecodeTile + 16 * ts;
                 uint8_t* stK = smem + s * Cfg::kStageBytes;
@@ -314,8 +360,9 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                     halfstride = Cfg::kHalfBytes;
                 }
 
-                // S = Q K^T : 16 rows x 16 tokens
-                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // S = Q K^T : 16 rows x 16 tokens, even / odd k-steps in two chains
+                float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 {
                     const int mi = lane >> 3;
                     const int trow = rowbase + 8 * (mi >> 1) + (lane & 7);
@@ -325,11 +372,16 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                         const uint32_t addr = kbase + (dch >> 3) * halfstride + swz(trow, dch & 7);
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4(addr, b0, b1, b2, b3);
-                        mma_bf16_16816(sacc[0], qf[kk], b0, b1);
-                        mma_bf16_16816(sacc[1], qf[kk], b2, b3);
+                        if (kk & 1) {
+                            mma_bf16_16816(sb[0], qf[kk], b0, b1);
+                            mma_bf16_16816(sb[1], qf[kk], b2, b3);
+                        } else {
+                            mma_bf16_16816(sa[0], qf[kk], b0, b1);
+                            mma_bf16_16816(sa[1], qf[kk], b2, b3);
+                        }
                     }
                 }
-                // mask + online softmax (log2 domain)
+                // mask + online softmax (log2 domain, lazily moved max)
                 const float cs = scale_log2 * kscale;
                 float sv[2][4];
 #pragma unroll
@@ -339,8 +391,8 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                         const int tok = tok_s0 + 8 * j + 2 * q4 + e;
                         const bool okl = v_lo && tok < ctx_b && tok <= p_lo;
                         const bool okh = v_hi && tok < ctx_b && tok <= p_hi;
-                        sv[j][e] = okl ? sacc[j][e] * cs : -INFINITY;
-                        sv[j][2 + e] = okh ? sacc[j][2 + e] * cs : -INFINITY;
+                        sv[j][e] = okl ? (sa[j][e] + sb[j][e]) * cs : -INFINITY;
+                        sv[j][2 + e] = okh ? (sa[j][2 + e] + sb[j][2 + e]) * cs : -INFINITY;
                     }
                 }
                 float mx_lo = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
@@ -349,12 +401,24 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                 mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
                 mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
                 mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-                const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-                const float mu_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-                const float mu_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-                const float al_lo = ex2(m_lo - mu_lo), al_hi = ex2(m_hi - mu_hi);
-                m_lo = mn_lo;
-                m_hi = mn_hi;
+                float al_lo = 1.f, al_hi = 1.f;
+                bool resc = false;
+                if (mx_lo > m_lo + 8.f) {
+                    if (m_lo != -INFINITY) {
+                        al_lo = ex2(m_lo - mx_lo);
+                        resc = true;
+                    }
+                    m_lo = mx_lo;
+                }
+                if (mx_hi > m_hi + 8.f) {
+                    if (m_hi != -INFINITY) {
+                        al_hi = ex2(m_hi - mx_hi);
+                        resc = true;
+                    }
+                    m_hi = mx_hi;
+                }
+                const float mu_lo = m_lo == -INFINITY ? 0.f : m_lo;
+                const float mu_hi = m_hi == -INFINITY ? 0.f : m_hi;
                 float p[2][4];
                 float sum_lo = 0.f, sum_hi = 0.f;
 #pragma unroll
@@ -368,12 +432,14 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                 }
                 l_lo = l_lo * al_lo + sum_lo;
                 l_hi = l_hi * al_hi + sum_hi;
+                if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-                for (int j = 0; j < D / 8; ++j) {
-                    o[j][0] *= al_lo;
-                    o[j][1] *= al_lo;
-                    o[j][2] *= al_hi;
-                    o[j][3] *= al_hi;
+                    for (int j = 0; j < D / 8; ++j) {
+                        o[j][0] *= al_lo;
+                        o[j][1] *= al_lo;
+                        o[j][2] *= al_hi;
+                        o[j][3] *= al_hi;
+                    }
                 }
                 uint32_t pa[4];
                 pa[0] = pack_bf16x2(p[0][0] * vscale, p[0][1] * vscale);
@@ -400,12 +466,14 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                 }
             }
 
-            // ---- merge the four token slices of this row tile
+            // ---- merge the NG x 4 slices of this row tile
             l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
             l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
             l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
             l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-            float* mb = merge + cw * Cfg::kMergeFloats;
+            // slice index inside the row tile: (group, token slice)
+            const int slice = grp * 4 + ts;
+            float* mb = merge + (rt * NG * 4 + slice) * Cfg::kMergeFloats;
             if (q4 == 0) {
                 mb[g] = m_lo;
                 mb[g + 8] = m_hi;
@@ -419,23 +487,25 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                 *reinterpret_cast<float2*>(mb + 32 + (g + 8) * D + d) =
                     make_float2(o[j][2], o[j][3]);
             }
-            named_bar_sync(5 + rt, 128);
+            named_bar_sync(5 + rt, 128 * NG);
             {
-                constexpr int DPL = D / 32;   // elements of D per lane
-                const float* m0 = merge + (rt * 4) * Cfg::kMergeFloats;
+                constexpr int DPL = D / 32;            // elements of D per lane
+                constexpr int kSlices = 4 * NG;
+                constexpr int kRowsPerWarp = 16 / kSlices;
+                const float* m0 = merge + (rt * kSlices) * Cfg::kMergeFloats;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int rr = ts * 4 + i;
+                for (int i = 0; i < kRowsPerWarp; ++i) {
+                    const int rr = slice * kRowsPerWarp + i;
                     const int r = 16 * rt + rr;
                     float M = -INFINITY;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) M = fmaxf(M, m0[kk * Cfg::kMergeFloats + rr]);
+                    for (int kk = 0; kk < kSlices; ++kk) M = fmaxf(M, m0[kk * Cfg::kMergeFloats + rr]);
                     float Lsum = 0.f;
                     float acc[DPL];
 #pragma unroll
                     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
+                    for (int kk = 0; kk < kSlices; ++kk) {
                         const float* mk = m0 + kk * Cfg::kMergeFloats;
                         const float w = mk[rr] == -INFINITY ? 0.f : ex2(mk[rr] - M);
                         Lsum += w * mk[16 + rr];
@@ -470,7 +540,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                     }
                 }
             }
-            named_bar_sync(5 + rt, 128);
+            named_bar_sync(5 + rt, 128 * NG);
         }
     }
     __syncthreads();
@@ -482,67 +552,72 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     }
 }
 
-template <int D, int RT, bool FP8, int STAGES>
-static cudaError_t launch_variant(const DecodeParams& P, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, cudaStream_t stream) {
-    using Cfg = DecodeCfg<D, RT, FP8, STAGES>;
-    auto kern = decode_kernel<D, RT, FP8, STAGES>;
+template <int D, int RT, bool FP8, int NG, int STAGES>
+static cudaError_t launch_variant(const DecodeParams& P, const CUtensorMap& tq,
+                                  const CUtensorMap& tk, const CUtensorMap& tv,
+                                  cudaStream_t stream) {
+    using Cfg = DecodeCfg<D, RT, FP8, NG, STAGES>;
+    auto kern = decode_kernel<D, RT, FP8, NG, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<P.L.N, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(P, tk, tv);
+    kern<<<P.L.N, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(P, tq, tk, tv);
     return cudaGetLastError();
 }
 
+// (head_dim, row tiles, fp8, tile groups, stages) built
 #define PA_DECODE_VARIANTS(X) \
-    X(128, 1, false, 5)       \
-    X(128, 2, false, 4)       \
-    X(128, 4, false, 2)       \
-    X(64, 1, false, 8)        \
-    X(64, 2, false, 8)        \
-    X(64, 4, false, 6)        \
-    X(128, 1, true, 6)        \
-    X(128, 2, true, 5)
+    X(128, 1, false, 2, 4)    \
+    X(128, 2, false, 1, 4)    \
+    X(64, 1, false, 2, 8)     \
+    X(64, 2, false, 1, 8)     \
+    X(64, 4, false, 1, 6)     \
+    X(128, 1, true, 1, 6)     \
+    X(128, 2, true, 1, 5)
 
 int decode_smem_bytes(int D, int RT, bool fp8) {
-#define X(d, rt, f8, st) \
-    if (D == d && RT == rt && fp8 == f8) return DecodeCfg<d, rt, f8, st>::kSmemBytes;
+#define X(d, rt, f8, ng, st) \
+    if (D == d && RT == rt && fp8 == f8) return DecodeCfg<d, rt, f8, ng, st>::kSmemBytes;
     PA_DECODE_VARIANTS(X)
 #undef X
     return -1;
 }
 
-int decode_threads(int RT) { return 32 * (1 + 4 * RT); }
+int decode_threads(int D, int RT, bool fp8) {
+#define X(d, rt, f8, ng, st) \
+    if (D == d && RT == rt && fp8 == f8) return DecodeCfg<d, rt, f8, ng, st>::kThreads;
+    PA_DECODE_VARIANTS(X)
+#undef X
+    return -1;
+}
 
 const void* decode_kernel_ptr(int D, int RT, bool fp8) {
-#define X(d, rt, f8, st) \
-    if (D == d && RT == rt && fp8 == f8) return (const void*)decode_kernel<d, rt, f8, st>;
+#define X(d, rt, f8, ng, st) \
+    if (D == d && RT == rt && fp8 == f8) return (const void*)decode_kernel<d, rt, f8, ng, st>;
     PA_DECODE_VARIANTS(X)
 #undef X
     return nullptr;
 }
 
-cudaError_t launch_decode(const DecodeParams& P, int D, int RT, bool fp8, const CUtensorMap& tk,
-                          const CUtensorMap& tv, cudaStream_t stream) {
-#define X(d, rt, f8, st) \
-    if (D == d && RT == rt && fp8 == f8) return launch_variant<d, rt, f8, st>(P, tk, tv, stream);
+static cudaError_t launch_decode(const DecodeParams& P, int D, int RT, bool fp8,
+                                 const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, cudaStream_t stream) {
+#define X(d, rt, f8, ng, st)             \
+    if (D == d && RT == rt && fp8 == f8) \
+        return launch_variant<d, rt, f8, ng, st>(P, tq, tk, tv, stream);
     PA_DECODE_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;
 }
 
-}  // namespace pa
-
-namespace pa {
-
-cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int RT, const void* q,
-                                   const CUtensorMap& tk, const CUtensorMap& tv,
-                                   const int32_t* block_table, const int32_t* ctx,
-                                   const int32_t* ql, const float* ks, const float* vs, void* ws,
-                                   void* partial, void* out, float* lse, cudaStream_t stream) {
+cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int RT,
+                                   const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const int32_t* block_table,
+                                   const int32_t* ctx, const int32_t* ql, const float* ks,
+                                   const float* vs, void* ws, void* partial, void* out, float* lse,
+                                   cudaStream_t stream) {
     DecodeParams P;
     P.L = L;
-    P.q = reinterpret_cast<const __nv_bfloat16*>(q);
     P.block_table = block_table;
     P.ctx = ctx;
     P.ql = ql;
@@ -558,9 +633,10 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int R
     P.max_pages_per_seq = p.max_pages_per_seq;
     P.rows_per_box = p.page_size < kDecodeTile ? p.page_size : kDecodeTile;
     P.boxes_per_tile = kDecodeTile / P.rows_per_box;
+    P.q_box_tokens = p.max_q_len > 0 ? p.max_q_len : 1;
     P.sm_scale = p.sm_scale;
     P.wait_limit_ns = 1000000000ull;
-    return launch_decode(P, p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3, tk, tv, stream);
+    return launch_decode(P, p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3, tq, tk, tv, stream);
 }
 
 }  // namespace pa

@@ -70,8 +70,11 @@ def test_invalid_problems_rejected_on_host(lib):
     assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0
     bad = B.PaProblem.from_buffer_copy(p)
     bad.max_context_len = max(bad.max_context_len, 17)
-    bad.max_q_len = 17                        # G * q_len = 68 rows > 64 per decode unit
+    bad.max_q_len = 9                         # G * q_len = 36 rows > 32 per D=128 decode unit
     assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0
+    ok = B.PaProblem.from_buffer_copy(p)
+    ok.max_q_len = 8                          # 32 rows: built
+    assert B.pa_assign_workspace_size(ok, B.PA_MODE_DECODE) > 0
     bad = B.PaProblem.from_buffer_copy(p)
     bad.mask_q_tiles, bad.mask_kv_tiles = 1, 1  # masks are prefill-only
     assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0

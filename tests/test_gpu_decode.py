@@ -66,9 +66,15 @@ def test_decode_head_dim_64_and_gqa_variants():
     run_and_compare(w)
 
 
-def test_decode_rows_up_to_64():
+def test_decode_rows_up_to_64_head_dim_64():
     w = W.make_workload("rows64", [500, 90], [8, 5], num_q_heads=16, num_kv_heads=2,
-                        head_dim=128, page_size=64, seed=8)
+                        head_dim=64, page_size=64, seed=8)
+    run_and_compare(w, num_ctas=10)
+
+
+def test_decode_rows_32_head_dim_128():
+    w = W.make_workload("rows32", [500, 90, 1200], [4, 3, 4], num_q_heads=16, num_kv_heads=2,
+                        head_dim=128, page_size=64, seed=10)
     run_and_compare(w, num_ctas=10)
 
 
