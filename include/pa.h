@@ -81,8 +81,10 @@ enum { PA_BF16 = 0, PA_FP8_E4M3 = 1 };
  *                    queries (G*max_q_len rows: at most 32 for head_dim 128,
  *                    64 for head_dim 64; larger groups use the prefill
  *                    mode); 64-token KV tiles.
- *   PA_MODE_PREFILL: one unit per (sequence, KV head, q tile of 128/G tokens)
- *                    = one 128-row tile; 128-token KV tiles; block mask
+ *   PA_MODE_PREFILL: one unit per (sequence, KV head, q tile of 256/G tokens;
+ *                    128 tokens when G = 1 with a block mask) = up to 256
+ *                    rows, computed as two 128-row tensor-core tiles that
+ *                    share every K/V tile; 128-token KV tiles; block mask
  *                    allowed.  Used by pa_prefill for prefill and mixed
  *                    batches. */
 enum { PA_MODE_DECODE = 0, PA_MODE_PREFILL = 1 };
@@ -143,7 +145,7 @@ PA_API size_t pa_partial_workspace_size(const pa_problem* problem, int mode);
  *   block_mask: uint8 [B][mask_q_tiles][mask_kv_tiles] or NULL (prefill mode only)
  *   assign_ws: >= pa_assign_workspace_size bytes, 256-byte aligned; written.
  * Clears the device error word.  Units are (b, hk) in decode mode and
- * (b, hk, q tile of 128/G tokens) in prefill mode; tile t of unit u weighs
+ * (b, hk, q tile) in prefill mode; tile t of unit u weighs
  * w_u = max(1, ceil(G*rows/balance_rows)); CTA c owns the cost interval
  * [floor(c*C/N), floor((c+1)*C/N)) of the total cost C; a task is a maximal
  * run of one unit's tiles inside one CTA; split units get partial slots.
@@ -194,7 +196,7 @@ PA_API pa_status pa_combine(const pa_problem* problem, int mode, const void* ass
  * softmax / PV, epilogue; 二.1 active-tile list; 二.2 page-aware TMA pipeline;
  * "vLLM Triton Attention Backend Deep Dive": Q blocks pack the G heads of one
  * KV head, persistent fixed grid).  Walks the task map of
- * pa_assign(PA_MODE_PREFILL) with 128-row GQA-packed q tiles and 128-token KV
+ * pa_assign(PA_MODE_PREFILL) with 256-row GQA-packed q tiles and 128-token KV
  * tiles on the tcgen05 tensor cores (accumulators in tensor memory).
  * Arguments as pa_decode_splitk, plus block_mask (the one given to pa_assign,
  * or NULL).  Decode rows (q_len 1) of a mixed batch are ordinary units.

@@ -212,7 +212,7 @@ def assign(mode, num_seqs, num_q_heads, num_kv_heads, num_ctas, kv_tile, balance
     if mode == 0:
         unit_cap = num_seqs * num_kv_heads
     else:
-        qtok = max(1, 128 // G)
+        qtok = 128 if (bm is not None and G == 1) else max(1, 256 // G)
         unit_cap = num_kv_heads * int(sum((int(x) + qtok - 1) // qtok for x in ql))
     unit_cap = max(unit_cap, 1)
     max_ctx = int(ctx.max()) if ctx.size else 0

@@ -325,8 +325,10 @@ void oracle_combine(int S, int D, const double* o_parts, const double* lse_parts
  *
  *  1. Units.  mode 0 (decode): u = b*Hkv + hk, all ql[b] queries of the
  *     sequence, rows R_u = G*ql[b], key length L_u = ctx[b].
- *     mode 1 (prefill / mixed): q tiles of qtok = 128/G tokens ([VLLM] "Q
- *     Blocks": G heads x qtok tokens = 128 rows); units ordered by b, hk, qt;
+ *     mode 1 (prefill / mixed): q tiles of qtok = 256/G tokens ([VLLM] "Q
+ *     Blocks": G heads x qtok tokens = 256 rows, two 128-row MMA tiles that
+ *     share every K/V tile); with a block mask and G = 1, qtok = 128 so a
+ *     unit never spans two mask rows; units ordered by b, hk, qt;
  *     q0 = qt*qtok, nq = min(qtok, ql-q0), R_u = G*nq,
  *     L_u = ctx - ql + q0 + nq (keys up to the tile's last query).
  *     A sequence with ql = 0 has no units in mode 1 and empty units in mode 0.
@@ -363,7 +365,7 @@ int oracle_assign(int mode, int B, int Hq, int Hkv, int N, int kv_tile, int bala
                   int64_t task_cap, int32_t* unit_nsplit, int32_t* unit_slot0, int32_t* counts,
                   int64_t unit_cap)
 {
-    int G, b, hk, c;
+    int G, qtok, b, hk, c;
     int64_t U = 0, u, C, n_tasks = 0, slots = 0;
     int64_t* prefix;
     int64_t* bound;
@@ -375,10 +377,11 @@ int oracle_assign(int mode, int B, int Hq, int Hkv, int N, int kv_tile, int bala
         return -1;
     if (mask && (mode != 1 || kv_tile != mask_tile))
         return -1;
+    qtok = (mask && G == 1) ? 128 : 256 / G;
 
     /* 1-3: units, tile lists, weights */
     for (b = 0; b < B; ++b) {
-        int nqt = (mode == 0) ? 1 : (ql[b] + (128 / G) - 1) / (128 / G);
+        int nqt = (mode == 0) ? 1 : (ql[b] + qtok - 1) / qtok;
         for (hk = 0; hk < Hkv; ++hk) {
             int qt;
             for (qt = 0; qt < nqt; ++qt) {
@@ -391,8 +394,8 @@ int oracle_assign(int mode, int B, int Hq, int Hkv, int N, int kv_tile, int bala
                     nq = ql[b];
                     L = nq > 0 ? ctx[b] : 0;
                 } else {
-                    q0 = qt * (128 / G);
-                    nq = ql[b] - q0 < 128 / G ? ql[b] - q0 : 128 / G;
+                    q0 = qt * qtok;
+                    nq = ql[b] - q0 < qtok ? ql[b] - q0 : qtok;
                     L = (int64_t)ctx[b] - ql[b] + q0 + nq;
                 }
                 units[U * 4 + 0] = b;

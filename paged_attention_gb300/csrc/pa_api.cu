@@ -21,7 +21,8 @@ int decode_threads(int D, int RT, bool fp8);
 const void* decode_kernel_ptr(int D, int RT, bool fp8);
 cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int RT,
                                    const CUtensorMap& tq, const CUtensorMap& tk,
-                                   const CUtensorMap& tv, const int32_t* block_table,
+                                   const CUtensorMap& tv, bool kv_one_box,
+                                   const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
                                    cudaStream_t stream);
@@ -177,6 +178,34 @@ bool encode_kv_map(const pa_problem& p, const void* base, CUtensorMap* map) {
     return r == CUDA_SUCCESS;
 }
 
+// bf16 K/V with pages of >= 64 tokens as (d % 64, slot, d / 64, head, page): one
+// box of 64 slots x both 64-element column blocks lands as two 128-byte-swizzled
+// [64 x 128 B] regions, i.e. the whole decode tile in one copy.
+bool encode_kv_map_one_box(const pa_problem& p, const void* base, CUtensorMap* map) {
+    auto fn = encode_fn();
+    if (!fn || p.kv_dtype != PA_BF16 || p.head_dim != 128 || p.page_size < 64) return false;
+    const cuuint64_t D = p.head_dim, ps = p.page_size, H = p.num_kv_heads, NP = p.num_pages;
+    cuuint64_t dims[5] = {64, ps, 2, H, NP};
+    cuuint64_t strides[4];
+    if (p.layout == PA_NHD) {
+        strides[0] = H * D * 2;
+        strides[1] = 128;
+        strides[2] = D * 2;
+        strides[3] = ps * H * D * 2;
+    } else {
+        strides[0] = D * 2;
+        strides[1] = 128;
+        strides[2] = ps * D * 2;
+        strides[3] = H * ps * D * 2;
+    }
+    cuuint32_t box[5] = {64, 64, 2, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Q viewed as (d, head, token): box = 64 elements x G heads x box_tokens tokens
 bool encode_q_map(const pa_problem& p, const void* base, int box_tokens, CUtensorMap* map) {
     auto fn = encode_fn();
@@ -216,7 +245,10 @@ bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L)
     L.D = p.head_dim;
     L.N = N;
     L.kv_tile = mode == PA_MODE_DECODE ? kDecodeTile : kPrefillTile;
-    L.qtok = mode == PA_MODE_DECODE ? (p.max_q_len > 0 ? p.max_q_len : 1) : kPrefillRows / G;
+    if (mode == PA_MODE_DECODE)
+        L.qtok = p.max_q_len > 0 ? p.max_q_len : 1;
+    else
+        L.qtok = (p.mask_q_tiles > 0 && G == 1) ? kPrefillHalfRows : kPrefillRows / G;
     int64_t ucap;
     if (mode == PA_MODE_DECODE)
         ucap = (int64_t)p.num_seqs * p.num_kv_heads;
@@ -340,10 +372,12 @@ pa_status pa_decode_splitk(const pa_problem* problem, const void* q, const void*
         !aligned(partial_ws, 16))
         return PA_ERR_WORKSPACE;
     CUtensorMap tq, tk, tv;
-    if (!encode_q_map(p, q, p.max_q_len > 0 ? p.max_q_len : 1, &tq) ||
-        !encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv))
+    if (!encode_q_map(p, q, p.max_q_len > 0 ? p.max_q_len : 1, &tq)) return PA_ERR_INVALID_ARG;
+    bool one_box = encode_kv_map_one_box(p, k_cache, &tk) && encode_kv_map_one_box(p, v_cache, &tv);
+    if (!one_box && (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv)))
         return PA_ERR_INVALID_ARG;
-    cudaError_t e = launch_decode_from_api(p, L, decode_row_tiles(p), tq, tk, tv, block_table,
+    cudaError_t e = launch_decode_from_api(p, L, decode_row_tiles(p), tq, tk, tv, one_box,
+                                           block_table,
                                            context_lens, q_lens, k_scale, v_scale,
                                            const_cast<void*>(assign_ws), partial_ws, out, lse,
                                            (cudaStream_t)stream);
@@ -388,7 +422,7 @@ pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cac
         return PA_ERR_WORKSPACE;
     if (p.total_q_tokens == 0) return PA_OK;
     CUtensorMap tq, tk, tv;
-    if (!encode_q_map(p, q, kPrefillRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
+    if (!encode_q_map(p, q, kPrefillHalfRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
         !encode_kv_map(p, k_cache, &tk) ||
         !encode_kv_map(p, v_cache, &tv))
         return PA_ERR_INVALID_ARG;

@@ -55,6 +55,7 @@ struct DecodeParams {
     int32_t rows_per_box;     // min(page_size, 64)
     int32_t boxes_per_tile;   // 64 / rows_per_box
     int32_t q_box_tokens;     // tokens per Q TMA box (max q_len)
+    int32_t kv_one_box;       // 1: one 5-D TMA box fills both column blocks of a tile
     float sm_scale;
     uint64_t wait_limit_ns;
 };
@@ -93,6 +94,11 @@ struct DecodeCfg {
     static_assert(!FP8 || D == 128, "FP8 decode is built for head_dim 128");
     static_assert(!FP8 || NG == 1, "FP8 decode uses one tile group");
     static_assert(kQHalfBytes % 1024 == 0, "Q slot alignment");
+    // Group g consumes the tiles with index % NG == g.  Every ring stage must
+    // always be consumed by the same group: a group that reused a stage after
+    // the other group could wait on a full barrier two phases ahead, where the
+    // parity test cannot tell the phases apart.
+    static_assert(STAGES % NG == 0, "stages must be a multiple of the tile groups");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -163,11 +169,15 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         const uint32_t box_bytes = (uint32_t)rpb * 128u * Cfg::kHalves;
         const uint32_t q_bytes = (uint32_t)Cfg::kQHalves * G * P.q_box_tokens * 128u;
         int it = 0, task_it = 0;
+        TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
-            const int4 tk = tasks[k];
-            const int4 un = units[tk.x];
+            if (((k - k_begin) & 31) == 0)
+                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            const int4 tk = rec.tk;
+            const int4 un = rec.un;
             const int b = un.x, hk = un.y;
-            const int ctx_b = P.ctx[b];
+            const int ctx_b = rec.ctx;
             const int npg = (ctx_b + ps - 1) / ps;
             const int32_t* bt_row = P.block_table + (int64_t)b * P.max_pages_per_seq;
             // Q rows of the unit into slot task_it & 1
@@ -182,7 +192,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
 #pragma unroll
                     for (int h = 0; h < Cfg::kQHalves; ++h)
                         tma_load_3d(qdst + h * Cfg::kQHalfBytes, &tmq, &q_full[qs], 64 * h, hk * G,
-                                    cu_q[b] + un.z);
+                                    rec.cuq + un.z);
                 }
             }
             __syncwarp();
@@ -227,6 +237,14 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                         mbar_arrive(&full[s]);
                     } else {
                         mbar_arrive_expect_tx(&full[s], bytes);
+                        if (Cfg::kHalves == 2 && P.kv_one_box) {
+                            // pages of >= 64 tokens: one box = both column blocks
+                            const int slot0 = (kt * kDecodeTile) % ps;
+                            if (pg[0] >= 0) {
+                                tma_load_5d(stK, &tmk, &full[s], 0, slot0, 0, hk, pg[0]);
+                                tma_load_5d(stV, &tmv, &full[s], 0, slot0, 0, hk, pg[0]);
+                            }
+                        } else
 #pragma unroll
                         for (int kv = 0; kv < 2; ++kv) {
 #pragma unroll
@@ -254,13 +272,17 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         const float scale_log2 = P.sm_scale * kLog2e;
         float* merge = reinterpret_cast<float*>(smem + Cfg::kOffMerge);
         int it = 0, task_it = 0;
+        TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
-            const int4 tk = tasks[k];
-            const int4 un = units[tk.x];
-            const int b = un.x, hk = un.y, q0 = un.z, nq = un.w;
+            if (((k - k_begin) & 31) == 0)
+                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            const int4 tk = rec.tk;
+            const int4 un = rec.un;
+            const int hk = un.y, q0 = un.z, nq = un.w;
             const int R = G * nq;
-            const int ctx_b = P.ctx[b], ql_b = P.ql[b];
-            const int tok_base = cu_q[b] + q0;
+            const int ctx_b = rec.ctx, ql_b = rec.ql;
+            const int tok_base = rec.cuq + q0;
             const int pbase = ctx_b - ql_b + q0;
             const int r_lo = 16 * rt + g, r_hi = r_lo + 8;
             const bool v_lo = r_lo < R, v_hi = r_hi < R;
@@ -566,8 +588,14 @@ static cudaError_t launch_variant(const DecodeParams& P, const CUtensorMap& tq,
 }
 
 // (head_dim, row tiles, fp8, tile groups, stages) built
-#define PA_DECODE_VARIANTS(X) \
-    X(128, 1, false, 2, 4)    \
+#ifndef PA_DECODE_NG_128_1
+#define PA_DECODE_NG_128_1 2
+#endif
+#ifndef PA_DECODE_ST_128_1
+#define PA_DECODE_ST_128_1 4
+#endif
+#define PA_DECODE_VARIANTS(X)                                             \
+    X(128, 1, false, PA_DECODE_NG_128_1, PA_DECODE_ST_128_1)              \
     X(128, 2, false, 1, 4)    \
     X(64, 1, false, 2, 8)     \
     X(64, 2, false, 1, 8)     \
@@ -612,7 +640,8 @@ static cudaError_t launch_decode(const DecodeParams& P, int D, int RT, bool fp8,
 
 cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int RT,
                                    const CUtensorMap& tq, const CUtensorMap& tk,
-                                   const CUtensorMap& tv, const int32_t* block_table,
+                                   const CUtensorMap& tv, bool kv_one_box,
+                                   const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
                                    cudaStream_t stream) {
@@ -634,6 +663,7 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int R
     P.rows_per_box = p.page_size < kDecodeTile ? p.page_size : kDecodeTile;
     P.boxes_per_tile = kDecodeTile / P.rows_per_box;
     P.q_box_tokens = p.max_q_len > 0 ? p.max_q_len : 1;
+    P.kv_one_box = kv_one_box ? 1 : 0;
     P.sm_scale = p.sm_scale;
     P.wait_limit_ns = 1000000000ull;
     return launch_decode(P, p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3, tq, tk, tv, stream);

@@ -19,7 +19,8 @@ namespace pa {
 
 constexpr int kDecodeTile = 64;      // KV tokens per decode tile
 constexpr int kPrefillTile = 128;    // KV tokens per prefill tile (= mask tile)
-constexpr int kPrefillRows = 128;    // rows (query token x head) per prefill q tile
+constexpr int kPrefillHalfRows = 128;  // rows of one tcgen05 M=128 tile
+constexpr int kPrefillRows = 256;    // rows (query token x head) per prefill unit (2 halves)
 constexpr int kMaskTile = 128;       // block-mask tile edge
 constexpr int kDefaultBalanceRows = 128;
 constexpr int kHeaderWords = 64;
@@ -42,7 +43,8 @@ struct WsLayout {
     int32_t B, Hq, Hkv, G, D;
     int32_t N;            // persistent CTAs
     int32_t kv_tile;      // 64 decode / 128 prefill
-    int32_t qtok;         // query tokens per unit (prefill: 128/G; decode: all)
+    int32_t qtok;         // query tokens per unit (prefill: 256/G, or 128 for G=1 with a
+                          // mask; decode: all)
     int32_t unit_cap;
     int32_t task_cap;
     int32_t max_kv_tiles; // row stride of the active-tile lists
@@ -146,6 +148,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3), "r"(c4)
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -309,6 +320,53 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
         "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
         "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+}  // namespace pa
+
+// ------------------------------------------------------------ task records
+namespace pa {
+
+// One task of the map with its unit and the sequence lengths it needs.
+struct TaskRec {
+    int4 tk;   // {unit, t0, t1, slot}
+    int4 un;   // {b, hk, q0, nq}
+    int ctx, ql, cuq;
+};
+
+// Lane `lane` of a warp loads task k (if k < k_end): the three dependent
+// loads run in parallel across the warp's lanes, once per 32 tasks.
+__device__ __forceinline__ TaskRec load_task_rec(const int4* tasks, const int4* units,
+                                                 const int32_t* ctx, const int32_t* ql,
+                                                 const int32_t* cu_q, int k, int k_end) {
+    TaskRec r;
+    r.tk = make_int4(0, 0, 0, -1);
+    r.un = make_int4(0, 0, 0, 0);
+    r.ctx = r.ql = r.cuq = 0;
+    if (k < k_end) {
+        r.tk = tasks[k];
+        r.un = units[r.tk.x];
+        r.ctx = ctx[r.un.x];
+        r.ql = ql[r.un.x];
+        r.cuq = cu_q[r.un.x];
+    }
+    return r;
+}
+
+__device__ __forceinline__ TaskRec shfl_task_rec(const TaskRec& r, int src) {
+    TaskRec o;
+    o.tk.x = __shfl_sync(0xffffffffu, r.tk.x, src);
+    o.tk.y = __shfl_sync(0xffffffffu, r.tk.y, src);
+    o.tk.z = __shfl_sync(0xffffffffu, r.tk.z, src);
+    o.tk.w = __shfl_sync(0xffffffffu, r.tk.w, src);
+    o.un.x = __shfl_sync(0xffffffffu, r.un.x, src);
+    o.un.y = __shfl_sync(0xffffffffu, r.un.y, src);
+    o.un.z = __shfl_sync(0xffffffffu, r.un.z, src);
+    o.un.w = __shfl_sync(0xffffffffu, r.un.w, src);
+    o.ctx = __shfl_sync(0xffffffffu, r.ctx, src);
+    o.ql = __shfl_sync(0xffffffffu, r.ql, src);
+    o.cuq = __shfl_sync(0xffffffffu, r.cuq, src);
+    return o;
 }
 
 }  // namespace pa

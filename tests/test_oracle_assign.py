@@ -62,7 +62,7 @@ def brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask=None, mask_tile=128)
             for hk in range(Hkv):
                 units.append((b, hk, 0, ql[b], ctx[b] if ql[b] > 0 else 0))
         else:
-            qtok = 128 // G
+            qtok = 128 if (mask is not None and G == 1) else 256 // G
             for hk in range(Hkv):
                 for q0 in range(0, ql[b], qtok):
                     nq = min(qtok, ql[b] - q0)
