@@ -45,21 +45,22 @@ def load_peaks():
             "source": "fallback"}
 
 
-def make_workload(name: str, rank: int):
+def make_workload(name: str, rank: int, shrink: int = 1):
     """The workload's batch for `rank`: every rank draws its own independent
-    batch of the same shape (weak scaling)."""
+    batch of the same shape (weak scaling).  shrink > 1 divides batch and
+    lengths (small profiling cases only; bench lines use shrink = 1)."""
     from paged_attention_gb300 import workloads as W
     from paged_attention_gb300.dist import rank_seed
     if name == "decode_bf16":
-        return W.decode_bf16(mtp=1, seed=rank_seed(1002, rank))
+        return W.decode_bf16(mtp=1, seed=rank_seed(1002, rank), shrink=shrink)
     if name == "decode_fp8":
-        return W.decode_fp8(seed=rank_seed(1003, rank))
+        return W.decode_fp8(seed=rank_seed(1003, rank), shrink=shrink)
     if name == "prefill_dense":
-        return W.prefill_bf16(sparse=False, seed=rank_seed(1004, rank))
+        return W.prefill_bf16(sparse=False, seed=rank_seed(1004, rank), shrink=shrink)
     if name == "prefill_sparse":
-        return W.prefill_bf16(sparse=True, seed=rank_seed(1004, rank))
+        return W.prefill_bf16(sparse=True, seed=rank_seed(1004, rank), shrink=shrink)
     if name == "hybrid":
-        return W.hybrid_bf16(seed=rank_seed(1005, rank))
+        return W.hybrid_bf16(seed=rank_seed(1005, rank), shrink=shrink)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -197,7 +198,7 @@ def run_native(args, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     name = args.workload
-    w_cpu = make_workload(name, rank)
+    w_cpu = make_workload(name, rank, args.shrink)
     w = w_cpu.to(dev)
     work, kind = work_of(w_cpu, name)
     mode = B.PA_MODE_DECODE if is_decode(name) else B.PA_MODE_PREFILL
@@ -323,7 +324,8 @@ def run_native(args, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.kv_dtype == 0 else "e4m3-kv/bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, paged, NaN decoy pages)",
-        "config": dict(workload_config(w_cpu, name), l2="inputs larger than L2",
+        "config": dict(workload_config(w_cpu, name),
+                       l2="inputs larger than L2" if args.shrink == 1 else f"shrink {args.shrink}",
                        parallelism=f"independent batch per GPU x{world}"),
         "e2e": {"value": round(e2e_val, 2), "unit": unit, "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -400,6 +402,8 @@ def main():
                              "hybrid"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shrink", type=int, default=1,
+                    help="divide batch and lengths (profiling of small cases only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -116,7 +116,7 @@ typedef struct pa_problem {
     int32_t mask_kv_tiles;
     int32_t num_ctas;          /* persistent CTAs; 0 = the library's choice          */
     int32_t balance_rows;      /* Assign weight divisor; 0 = 128                     */
-    float sm_scale;            /* softmax scale applied to q.k                       */
+    float sm_scale;            /* softmax scale applied to q.k; finite and >= 0      */
 } pa_problem;
 
 /* Human-readable name of a pa_status or PA_DEV_* code set. */

@@ -91,7 +91,7 @@ pa_status check_problem(const pa_problem* pp, int mode) {
         p.num_q_heads % p.num_kv_heads != 0 || p.num_pages < 1 || p.max_pages_per_seq < 1 ||
         p.total_q_tokens < 0 || p.max_q_len < 0 || p.max_context_len < p.max_q_len ||
         p.mask_q_tiles < 0 || p.mask_kv_tiles < 0 || p.num_ctas < 0 || p.balance_rows < 0 ||
-        !std::isfinite(p.sm_scale))
+        !std::isfinite(p.sm_scale) || p.sm_scale < 0.f)
         return PA_ERR_INVALID_ARG;
     if (p.layout != PA_NHD && p.layout != PA_HND) return PA_ERR_INVALID_ARG;
     if (p.kv_dtype != PA_BF16 && p.kv_dtype != PA_FP8_E4M3) return PA_ERR_INVALID_ARG;
@@ -129,7 +129,7 @@ int resolve_ctas(const pa_problem& p, int mode) {
     } else {
         k = prefill_kernel_ptr(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
         smem = prefill_smem_bytes(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
-        threads = 192;
+        threads = 320;
     }
     if (k && smem > 0) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=

@@ -5,30 +5,38 @@
 // multi-stage shared memory; QK, causal mask, fp32 online softmax, PV;
 // epilogue normalisation), 二.1 (only the KV tiles of the active-tile list
 // are loaded and multiplied), 二.2 (warp specialisation: a producer resolves
-// page ids and issues K then V by TMA while compute runs; K/V buffers are
-// released as soon as the MMAs that read them complete).  "vLLM Triton
-// Attention Backend Deep Dive": Q blocks pack the G q heads of one KV head
-// into one MMA tile; the persistent grid is fixed at the SM count.
+// page ids and issues K then V by TMA while the consumers compute; two
+// consumer groups each own one half of the query tile; K and V buffers are
+// released separately, K right after QK).  "vLLM Triton Attention Backend
+// Deep Dive": Q blocks pack the G q heads of one KV head into one MMA tile;
+// the persistent grid is fixed at the SM count.
 //
-// GB300 design (one CTA per SM, 192 threads):
-//   warp 0      TMA producer: Q tile (128 rows = 128/G tokens x G heads,
-//               128-byte swizzled) once per task, then K and V of every
-//               active 128-token tile page by page into a 2-stage ring.
-//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
-//               S[buf] = Q K^T (M=128, N=128, K=D, both operands K-major in
-//               shared memory) into one of two TMEM S buffers, then
-//               O += P V (M=128, N=D, K=128; P K-major, V MN-major: no
-//               transpose of V is ever made).  Completion is signalled with
-//               tcgen05.commit on mbarriers.  The warp also zeroes V rows past
-//               the context before they are multiplied.
-//   warps 2-5   softmax warpgroup: thread = query row = TMEM lane.  Reads its
-//               S row (tcgen05.ld), applies the causal / context mask, keeps
-//               the running max lazily (O is rescaled in TMEM only when the
-//               max grows by more than 2^8), writes P (bf16) into shared
-//               memory for the PV MMA, and finally normalises O and writes
-//               the output row (or the split partial) and its LSE.
-// While the softmax works on tile j, the tensor cores already compute
-// S_{j+1} into the other TMEM buffer.
+// GB300 design (one CTA per SM, 320 threads).  A unit is up to 256 query
+// rows (G heads x 256/G tokens), computed as two 128-row halves that share
+// every K/V tile:
+//   warp 0      TMA producer: the unit's Q halves once per task, then for
+//               every active 128-token KV tile its K and its V, page by page,
+//               each into its own entry of a ring (128-byte swizzle).
+//   warp 1      allocates the 512 TMEM columns; lane 0 issues every MMA:
+//               S_h = Q_h K^T (M=128, N=128, K=D, both operands K-major in
+//               shared memory) into TMEM, and O_h += P_h V (M=128, N=D,
+//               K=128) with P_h read from TMEM (written over S_h by the
+//               softmax) and V read MN-major from shared memory, so V is
+//               never transposed.  Issue order per tile j:
+//                 PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1)
+//               so the tensor cores work on one half while the other half's
+//               softmax runs; MMAs of one thread execute in issue order,
+//               which keeps QK_h(j+1) from overwriting P_h(j) before PV_h(j)
+//               has read it.  Also zeroes V rows past the context.
+//   warps 2-5   softmax for half 0, warps 6-9 for half 1: thread = query row
+//               = TMEM lane.  Reads its S row (tcgen05.ld), applies the
+//               causal / context mask, keeps the running max lazily (O is
+//               rescaled in TMEM only when the max grows by more than 2^8),
+//               writes P (bf16) back into TMEM, and at the end of the task
+//               normalises O and writes the output row (or split partial)
+//               and its LSE.
+// TMEM columns: half h uses [256h, 256h+128) for S (and P over its first 64
+// columns) and [256h+128, 256h+128+D) for O.
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -56,60 +64,45 @@ template <int D>
 struct PrefillCfg {
     static constexpr int kHalves = D / 64;           // 128-byte column blocks of a row
     static constexpr int kRegion = 128 * 128;        // 128 rows x 128 bytes
-    static constexpr int kQBytes = kHalves * kRegion;
-    static constexpr int kPBytes = 2 * kRegion;      // 128 keys = 2 column blocks
+    static constexpr int kQTileBytes = kHalves * kRegion;
+    static constexpr int kQBytes = 2 * kQTileBytes;  // two 128-row halves
     static constexpr int kKVBytes = kHalves * kRegion;
-    static constexpr int kStages = 2;
-    static constexpr int kStageBytes = 2 * kKVBytes;
+    static constexpr int kEntries = D == 128 ? 5 : 8;  // ring entries (each a K or a V tile)
     static constexpr int kOffQ = 0;
-    static constexpr int kOffP = kOffQ + kQBytes;
-    static constexpr int kOffStage = kOffP + kPBytes;
-    static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
-    static constexpr int kSlack = 16384;             // guard space after the data
-    static constexpr int kSmemBytes = kOffBar + 256 + kSlack + 1024;
-    static constexpr int kThreads = 192;
+    static constexpr int kOffKV = kOffQ + kQBytes;
+    static constexpr int kOffBar = kOffKV + kEntries * kKVBytes;
+    static constexpr int kNumBars = 2 + 2 * kEntries + 9;
+    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+    static constexpr int kThreads = 320;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kOCol = 256;                // S buffers at columns 0 and 128
-};
-
-enum PrefillBar {
-    B_Q_FULL = 0,
-    B_Q_EMPTY = 1,
-    B_KV_FULL = 2,   // 2 stages
-    B_KV_EMPTY = 4,  // 2 stages
-    B_S_FULL = 6,    // 2 buffers
-    B_S_FREE = 8,    // 2 buffers
-    B_P_FULL = 10,
-    B_O_DONE = 11,
-    B_O_FREE = 12,
-    B_MMA_DONE = 13,
-    B_COUNT = 14
+    static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* header, uint64_t limit) {
-    if (*abort_flag) return;
-    if (!mbar_wait(bar, parity, limit)) {
-        *abort_flag = 1;
-        set_device_error(header, PA_DEV_WAIT_TIMEOUT);
-    }
-}
-
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ CUtensorMap tmq,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     using Cfg = PrefillCfg<D>;
+    constexpr int E = Cfg::kEntries;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 128);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffBar + 132);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
+    uint64_t* q_full = bars + 0;
+    uint64_t* q_empty = bars + 1;
+    uint64_t* kv_full = bars + 2;             // [E]
+    uint64_t* kv_empty = kv_full + E;         // [E]
+    uint64_t* s_full = kv_empty + E;          // [2]
+    uint64_t* p_full = s_full + 2;            // [2]
+    uint64_t* o_done = p_full + 2;            // [2]
+    uint64_t* o_free = o_done + 2;            // [2]
+    uint64_t* mma_done = o_free + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -120,18 +113,19 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         return;
     }
     if (threadIdx.x == 0) {
-        mbar_init(&bar[B_Q_FULL], 1);
-        mbar_init(&bar[B_Q_EMPTY], 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar[B_KV_FULL + s], 1);
-            mbar_init(&bar[B_KV_EMPTY + s], 1);
-            mbar_init(&bar[B_S_FULL + s], 1);
-            mbar_init(&bar[B_S_FREE + s], 128);
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int e = 0; e < E; ++e) {
+            mbar_init(&kv_full[e], 1);
+            mbar_init(&kv_empty[e], 1);
         }
-        mbar_init(&bar[B_P_FULL], 128);
-        mbar_init(&bar[B_O_DONE], 1);
-        mbar_init(&bar[B_O_FREE], 128);
-        mbar_init(&bar[B_MMA_DONE], 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&s_full[h], 1);
+            mbar_init(&p_full[h], 128);
+            mbar_init(&o_done[h], 1);
+            mbar_init(&o_free[h], 128);
+        }
+        mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -144,6 +138,14 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (*abort_flag) return;
+        if (!mbar_wait(bar, parity, lim)) {
+            *abort_flag = 1;
+            set_device_error(header, PA_DEV_WAIT_TIMEOUT);
+        }
+    };
+
     const int32_t* cta_ptr = ws_ptr<int32_t>(P.ws, L.off_cta_ptr);
     const int4* tasks = ws_ptr<int4>(P.ws, L.off_tasks);
     const int4* units = ws_ptr<int4>(P.ws, L.off_units);
@@ -151,6 +153,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     const int32_t* active = ws_ptr<int32_t>(P.ws, L.off_active);
     const int k_begin = cta_ptr[blockIdx.x], k_end = cta_ptr[blockIdx.x + 1];
     const int G = L.G, Hq = L.Hq;
+    const int half_tokens = kPrefillHalfRows / G;   // query tokens per 128-row half
 
     auto tile_of = [&](int u, int t) -> int {
         return L.has_mask ? active[(int64_t)u * L.max_kv_tiles + t] : t;
@@ -165,35 +168,34 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         }
         const int ps = P.page_size, rpb = P.rows_per_box, nbox = P.boxes_per_tile;
         const uint32_t box_bytes = (uint32_t)rpb * 128u * Cfg::kHalves;
-        int kv_it = 0, task_it = 0;
+        int e_it = 0, task_it = 0;
+        TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
-            const int4 tk = tasks[k];
-            const int4 un = units[tk.x];
-            const int b = un.x, hk = un.y, q0 = un.z;
-            const int ctx_b = P.ctx[b];
+            if (((k - k_begin) & 31) == 0)
+                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            const int u = rec.tk.x, b = rec.un.x, hk = rec.un.y, q0 = rec.un.z;
+            const int H = G * rec.un.w > kPrefillHalfRows ? 2 : 1;
+            const int ctx_b = rec.ctx;
             const int npg = (ctx_b + ps - 1) / ps;
             const int32_t* bt_row = P.block_table + (int64_t)b * P.max_pages_per_seq;
-            wait_or_abort(&bar[B_Q_EMPTY], (uint32_t)(task_it & 1) ^ 1u, abort_flag, header, lim);
+            wait(q_empty, (uint32_t)(task_it & 1) ^ 1u);
             if (lane == 0) {
                 if (*abort_flag) {
-                    mbar_arrive(&bar[B_Q_FULL]);
+                    mbar_arrive(q_full);
                 } else {
-                    mbar_arrive_expect_tx(&bar[B_Q_FULL], Cfg::kQBytes);
+                    mbar_arrive_expect_tx(q_full, (uint32_t)H * Cfg::kQTileBytes);
+                    for (int h = 0; h < H; ++h)
 #pragma unroll
-                    for (int h = 0; h < Cfg::kHalves; ++h)
-                        tma_load_3d(smem + Cfg::kOffQ + h * Cfg::kRegion, &tmq, &bar[B_Q_FULL],
-                                    64 * h, hk * G, cu_q[b] + q0);
+                        for (int c = 0; c < Cfg::kHalves; ++c)
+                            tma_load_3d(smem + Cfg::kOffQ + h * Cfg::kQTileBytes + c * Cfg::kRegion,
+                                        &tmq, q_full, 64 * c, hk * G, rec.cuq + q0 + h * half_tokens);
                 }
             }
             __syncwarp();
             int win_lo = -(1 << 30), win_val = -1;
-            for (int t = tk.y; t < tk.z; ++t, ++kv_it) {
-                const int st = kv_it & 1;
-                wait_or_abort(&bar[B_KV_EMPTY + st], (uint32_t)((kv_it >> 1) & 1) ^ 1u, abort_flag,
-                              header, lim);
-                const int kt = tile_of(tk.x, t);
-                uint8_t* sK = smem + Cfg::kOffStage + st * Cfg::kStageBytes;
-                uint8_t* sV = sK + Cfg::kKVBytes;
+            for (int t = rec.tk.y; t < rec.tk.z; ++t) {
+                const int kt = tile_of(u, t);
                 uint32_t bytes = 0;
                 int pg[8];
 #pragma unroll
@@ -213,30 +215,33 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         page = -1;
                     }
                     pg[j] = page;
-                    if (page >= 0) bytes += 2u * box_bytes;
+                    if (page >= 0) bytes += box_bytes;
                 }
-                if (lane == 0) {
-                    if (*abort_flag) {
-                        mbar_arrive(&bar[B_KV_FULL + st]);
-                    } else {
-                        mbar_arrive_expect_tx(&bar[B_KV_FULL + st], bytes);
-                        // all K boxes first (QK needs them first), then V
+                // K first (QK needs it first), then V, each into its own ring entry
 #pragma unroll
-                        for (int kv = 0; kv < 2; ++kv) {
+                for (int kv = 0; kv < 2; ++kv, ++e_it) {
+                    const int e = e_it % E;
+                    wait(&kv_empty[e], (uint32_t)((e_it / E) & 1) ^ 1u);
+                    if (lane == 0) {
+                        if (*abort_flag) {
+                            mbar_arrive(&kv_full[e]);
+                        } else {
+                            mbar_arrive_expect_tx(&kv_full[e], bytes);
+                            uint8_t* dst = smem + Cfg::kOffKV + e * Cfg::kKVBytes;
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 if (pg[j] < 0) continue;
                                 const int slot0 = (kt * kPrefillTile + j * rpb) % ps;
 #pragma unroll
-                                for (int h = 0; h < Cfg::kHalves; ++h)
-                                    tma_load_4d((kv ? sV : sK) + h * Cfg::kRegion + j * rpb * 128,
-                                                kv ? &tmv : &tmk, &bar[B_KV_FULL + st], 64 * h,
-                                                slot0, hk, pg[j]);
+                                for (int c = 0; c < Cfg::kHalves; ++c)
+                                    tma_load_4d(dst + c * Cfg::kRegion + j * rpb * 128,
+                                                kv ? &tmv : &tmk, &kv_full[e], 64 * c, slot0, hk,
+                                                pg[j]);
                             }
                         }
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
     } else if (warp == 1) {
@@ -244,122 +249,166 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
         const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
-        const uint32_t sP = smem_u32(smem + Cfg::kOffP);
-        int kv_it = 0, s_it = 0, p_it = 0, task_it = 0;
+        const uint32_t sKV = smem_u32(smem + Cfg::kOffKV);
+        int e_it = 0, task_it = 0;
+        int p_cnt[2] = {0, 0}, of_cnt[2] = {0, 0};
+        TaskRec mine;
 
-        auto issue_pv = [&](int st, bool first) {
-            wait_or_abort(&bar[B_P_FULL], (uint32_t)(p_it & 1), abort_flag, header, lim);
-            ++p_it;
-            if (first)
-                wait_or_abort(&bar[B_O_FREE], (uint32_t)(task_it & 1) ^ 1u, abort_flag, header, lim);
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t sV =
-                    smem_u32(smem + Cfg::kOffStage + st * Cfg::kStageBytes + Cfg::kKVBytes);
+        auto issue_qk = [&](int h, int e) {   // S_h = Q_h K^T from ring entry e
+            const uint32_t sK = sKV + e * Cfg::kKVBytes;
+            const uint32_t sQh = sQ + h * Cfg::kQTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kPrefillTile / 16; ++kk) {
-                    const uint64_t a = smem_desc_sw128(
-                        sP + (kk >> 2) * Cfg::kRegion + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(sV + kk * 16 * 128, Cfg::kRegion, 1024);
-                    tc_mma_ss(tmem + Cfg::kOCol, a, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(&bar[B_O_DONE]);
-                tc_commit(&bar[B_KV_EMPTY + st]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t koff = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
+                tc_mma_ss(tmem + h * 256, smem_desc_sw128(sQh + koff, 16, 1024),
+                          smem_desc_sw128(sK + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
             }
-            __syncwarp();
+            tc_commit(&s_full[h]);
+        };
+        auto issue_pv = [&](int h, int e, bool first) {   // O_h += P_h V from ring entry e
+            const uint32_t sV = sKV + e * Cfg::kKVBytes;
+#pragma unroll
+            for (int kk = 0; kk < kPrefillTile / 16; ++kk)
+                tc_mma_ts(tmem + h * 256 + 128, tmem + h * 256 + kk * 8,
+                          smem_desc_sw128(sV + kk * 16 * 128, Cfg::kRegion, 1024), idesc_pv,
+                          (!first || kk > 0) ? 1u : 0u);
+            tc_commit(&o_done[h]);
         };
 
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
-            const int4 tk = tasks[k];
-            const int4 un = units[tk.x];
-            const int ctx_b = P.ctx[un.x];
-            const int n = tk.z - tk.y;
-            wait_or_abort(&bar[B_Q_FULL], (uint32_t)(task_it & 1), abort_flag, header, lim);
-            int prev_st = 0;
-            for (int j = 0; j < n; ++j, ++kv_it, ++s_it) {
-                const int st = kv_it & 1;
-                const int kt = tile_of(tk.x, tk.y + j);
-                wait_or_abort(&bar[B_KV_FULL + st], (uint32_t)((kv_it >> 1) & 1), abort_flag, header,
-                              lim);
-                uint8_t* sK = smem + Cfg::kOffStage + st * Cfg::kStageBytes;
-                const int first_bad = ctx_b - kt * kPrefillTile;   // first key row past the context
-                if (first_bad < kPrefillTile) {
-                    uint8_t* sV = sK + Cfg::kKVBytes;
-                    const int r0 = first_bad < 0 ? 0 : first_bad;
-                    for (int idx = lane; idx < (kPrefillTile - r0) * Cfg::kHalves * 8; idx += 32) {
-                        const int r = r0 + idx / (Cfg::kHalves * 8);
-                        const int rem = idx % (Cfg::kHalves * 8);
-                        *reinterpret_cast<uint4*>(sV + (rem >> 3) * Cfg::kRegion + swz128(r, rem & 7)) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                const int sb = s_it & 1;
-                wait_or_abort(&bar[B_S_FREE + sb], (uint32_t)((s_it >> 1) & 1) ^ 1u, abort_flag,
-                              header, lim);
+            if (((k - k_begin) & 31) == 0)
+                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            const int u = rec.tk.x;
+            const int H = G * rec.un.w > kPrefillHalfRows ? 2 : 1;
+            const int n = rec.tk.z - rec.tk.y;
+            const int ctx_b = rec.ctx;
+            wait(q_full, (uint32_t)(task_it & 1));
+            // prologue: QK of tile 0
+            {
+                const int eK = e_it;
+                wait(&kv_full[eK % E], (uint32_t)((eK / E) & 1));
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint32_t sKa = smem_u32(sK);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-                        tc_mma_ss(tmem + sb * 128, smem_desc_sw128(sQ + koff, 16, 1024),
-                                  smem_desc_sw128(sKa + koff, 16, 1024), idesc_qk,
-                                  kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&bar[B_S_FULL + sb]);
-                    if (j == n - 1) tc_commit(&bar[B_Q_EMPTY]);
+                    for (int h = 0; h < H; ++h) issue_qk(h, eK % E);
+                    tc_commit(&kv_empty[eK % E]);
+                    if (n == 1) tc_commit(q_empty);
                 }
                 __syncwarp();
-                if (j > 0) issue_pv(prev_st, j - 1 == 0);
-                prev_st = st;
             }
-            if (n > 0) issue_pv(prev_st, n == 1);
+            for (int j = 0; j < n; ++j) {
+                const int eV = e_it + 2 * j + 1, eKn = e_it + 2 * j + 2;
+                wait(&kv_full[eV % E], (uint32_t)((eV / E) & 1));
+                {
+                    // zero V rows of keys past the context (P is 0 there, 0 * NaN is not)
+                    const int kt = tile_of(u, rec.tk.y + j);
+                    const int first_bad = ctx_b - kt * kPrefillTile;
+                    if (first_bad < kPrefillTile) {
+                        uint8_t* sVp = smem + Cfg::kOffKV + (eV % E) * Cfg::kKVBytes;
+                        const int r0 = first_bad < 0 ? 0 : first_bad;
+                        for (int idx = lane; idx < (kPrefillTile - r0) * Cfg::kHalves * 8; idx += 32) {
+                            const int r = r0 + idx / (Cfg::kHalves * 8);
+                            const int rem = idx % (Cfg::kHalves * 8);
+                            *reinterpret_cast<uint4*>(sVp + (rem >> 3) * Cfg::kRegion +
+                                                      swz128(r, rem & 7)) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    __syncwarp();
+                }
+                for (int h = 0; h < H; ++h) {
+                    wait(&p_full[h], (uint32_t)(p_cnt[h] & 1));
+                    ++p_cnt[h];
+                    if (j == 0) {
+                        wait(&o_free[h], (uint32_t)(of_cnt[h] & 1) ^ 1u);
+                        ++of_cnt[h];
+                    }
+                    if (j + 1 < n && h == 0) wait(&kv_full[eKn % E], (uint32_t)((eKn / E) & 1));
+                    if (lane == 0) {
+                        tc_fence_after();
+                        issue_pv(h, eV % E, j == 0);
+                        if (j + 1 < n) issue_qk(h, eKn % E);
+                    }
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    tc_commit(&kv_empty[eV % E]);
+                    if (j + 1 < n) tc_commit(&kv_empty[eKn % E]);
+                    if (j + 1 == n - 1) tc_commit(q_empty);
+                }
+                __syncwarp();
+            }
+            e_it += 2 * n;
         }
         if (lane == 0) {
-            tc_commit(&bar[B_MMA_DONE]);
-            mbar_wait(&bar[B_MMA_DONE], 0, lim);
+            tc_commit(mma_done);
+            mbar_wait(mma_done, 0, lim);
         }
         __syncwarp();
     } else {
-        // -------------------------------------------------- softmax warpgroup
+        // --------------------------------------------------- softmax (2 halves)
+        const int h = (warp - 2) >> 2;
         const int wq = warp & 3;
-        const int row = wq * 32 + lane;
+        const int row = wq * 32 + lane;              // row inside the half = TMEM lane
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + h * 256, tO = tS + 128;
         const float scale_log2 = P.sm_scale * kLog2e;
-        uint8_t* sPb = smem + Cfg::kOffP;
-        int s_it = 0, o_it = 0, task_it = 0;
-        for (int k = k_begin; k < k_end; ++k, ++task_it) {
-            const int4 tk = tasks[k];
-            const int4 un = units[tk.x];
-            const int b = un.x, hk = un.y, q0 = un.z, nq = un.w;
-            const int R = G * nq;
-            const int ctx_b = P.ctx[b], ql_b = P.ql[b];
-            const bool row_ok = row < R;
-            const int p_row = ctx_b - ql_b + q0 + row / G;           // last key this row sees
+        int s_cnt = 0, o_cnt = 0;
+        TaskRec mine;
+        for (int k = k_begin; k < k_end; ++k) {
+            if (((k - k_begin) & 31) == 0)
+                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            const int u = rec.tk.x, hk = rec.un.y, q0 = rec.un.z;
+            const int R = G * rec.un.w;
+            if (h == 1 && R <= kPrefillHalfRows) continue;   // half 1 idle for this unit
+            const int r = h * kPrefillHalfRows + row;        // row inside the unit
+            const bool row_ok = r < R;
+            const int ctx_b = rec.ctx;
+            const int p_row = ctx_b - rec.ql + q0 + r / G;   // last key this row sees
             const int key_last = p_row < ctx_b - 1 ? p_row : ctx_b - 1;
+            const int n = rec.tk.z - rec.tk.y;
+            // a warp whose 32 rows are all padding (decode units fill a few rows)
+            // keeps the barrier protocol but skips the math: MMA rows are
+            // independent and padding rows are never written
+            const bool warp_live = __any_sync(0xffffffffu, row_ok);
             float m = -INFINITY, l = 0.f;
-            const int n = tk.z - tk.y;
-            for (int j = 0; j < n; ++j, ++s_it) {
-                const int kt = tile_of(tk.x, tk.y + j);
-                const int sb = s_it & 1;
-                wait_or_abort(&bar[B_S_FULL + sb], (uint32_t)((s_it >> 1) & 1), abort_flag, header,
-                              lim);
+            for (int j = 0; j < n; ++j) {
+                const int kt = tile_of(u, rec.tk.y + j);
+                wait(&s_full[h], (uint32_t)(s_cnt & 1));
+                ++s_cnt;
                 tc_fence_after();
-                float s[128];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + lane_off + sb * 128 + c4 * 32, s + c4 * 32);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&bar[B_S_FREE + sb]);
-                const int limc = row_ok ? key_last - kt * kPrefillTile : -1;   // valid: c <= limc
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    s[c] = c <= limc ? s[c] * scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, s[c]);
+                if (!warp_live) {
+                    if (j > 0) {
+                        wait(&o_done[h], (uint32_t)(o_cnt & 1));
+                        ++o_cnt;
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&p_full[h]);
+                    continue;
                 }
+                const int limc = row_ok ? key_last - kt * kPrefillTile : -1;   // valid: c <= limc
+                // pass 1: row max over the tile, 64 columns at a time.  Fully
+                // visible chunks take the max of the raw scores (sm_scale >= 0).
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float s[64];
+                    tmem_ld32(tS + hh * 64, s);
+                    tmem_ld32(tS + hh * 64 + 32, s + 32);
+                    tmem_wait_ld();
+                    const int lim = limc - hh * 64;
+                    if (lim >= 63) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            mx4[c & 3] = fmaxf(mx4[c & 3], c <= lim ? s[c] : -INFINITY);
+                    }
+                }
+                const float mx =
+                    fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
                 // lazy max: move m (and rescale O, l) only when it grows by > 2^8
                 float alpha = 1.f;
                 bool resc = false;
@@ -372,58 +421,73 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 }
                 const float mu = m == -INFINITY ? 0.f : m;
                 if (j > 0) {
-                    wait_or_abort(&bar[B_O_DONE], (uint32_t)(o_it & 1), abort_flag, header, lim);
-                    ++o_it;
+                    wait(&o_done[h], (uint32_t)(o_cnt & 1));   // PV of the previous tile
+                    ++o_cnt;
                 }
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, resc)) {
                     const float f = resc ? alpha : 1.f;
-#pragma unroll
+#pragma unroll 1
                     for (int c4 = 0; c4 < D / 32; ++c4) {
                         float o[32];
-                        tmem_ld32(tmem + lane_off + Cfg::kOCol + c4 * 32, o);
+                        tmem_ld32(tO + c4 * 32, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= f;
-                        tmem_st32(tmem + lane_off + Cfg::kOCol + c4 * 32, o);
+                        tmem_st32(tO + c4 * 32, o);
                     }
-                    tmem_wait_st();
                 }
-                float sum = 0.f;
+                // pass 2: P = exp2(s * scale - m) in bf16, written over the S columns
+                // already read
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float s[64];
+                    tmem_ld32(tS + hh * 64, s);
+                    tmem_ld32(tS + hh * 64 + 32, s + 32);
+                    tmem_wait_ld();
+                    const int lim = limc - hh * 64;
+                    uint32_t pk[32];
+                    if (lim >= 63) {
 #pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    uint32_t w[4];
+                        for (int c = 0; c < 64; c += 2) {
+                            const float p0 = ex2(fmaf(s[c], scale_log2, -mu));
+                            const float p1 = ex2(fmaf(s[c + 1], scale_log2, -mu));
+                            sum4[(c >> 1) & 3] += p0 + p1;
+                            pk[c >> 1] = pack_bf16x2(p0, p1);
+                        }
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = ex2(s[ch * 8 + 2 * e] - mu);
-                        const float p1 = ex2(s[ch * 8 + 2 * e + 1] - mu);
-                        sum += p0 + p1;
-                        w[e] = pack_bf16x2(p0, p1);
+                        for (int c = 0; c < 64; c += 2) {
+                            const float p0 = c <= lim ? ex2(fmaf(s[c], scale_log2, -mu)) : 0.f;
+                            const float p1 = c + 1 <= lim ? ex2(fmaf(s[c + 1], scale_log2, -mu)) : 0.f;
+                            sum4[(c >> 1) & 3] += p0 + p1;
+                            pk[c >> 1] = pack_bf16x2(p0, p1);
+                        }
                     }
-                    *reinterpret_cast<uint4*>(sPb + (ch >> 3) * Cfg::kRegion + swz128(row, ch & 7)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                    tmem_st32(tS + hh * 32, reinterpret_cast<const float*>(pk));
                 }
-                l = l * alpha + sum;
-                fence_proxy_async_smem();
+                l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&bar[B_P_FULL]);
+                mbar_arrive(&p_full[h]);
             }
             // ---- epilogue: O / l -> output row (or split partial), LSE
             if (n > 0) {
-                wait_or_abort(&bar[B_O_DONE], (uint32_t)(o_it & 1), abort_flag, header, lim);
-                ++o_it;
+                wait(&o_done[h], (uint32_t)(o_cnt & 1));
+                ++o_cnt;
             }
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float lse_nat = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
-            const int token = cu_q[b] + q0 + row / G, head = hk * G + row % G;
-#pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
+            const int token = rec.cuq + q0 + r / G, head = hk * G + r % G;
+#pragma unroll 1
+            for (int c4 = 0; c4 < (warp_live ? D / 32 : 0); ++c4) {
                 float o[32];
-                tmem_ld32(tmem + lane_off + Cfg::kOCol + c4 * 32, o);
+                tmem_ld32(tO + c4 * 32, o);
                 tmem_wait_ld();
                 if (row_ok) {
-                    if (tk.w < 0) {
+                    if (rec.tk.w < 0) {
                         uint4* dst = reinterpret_cast<uint4*>(
                             P.out + ((int64_t)token * Hq + head) * D + c4 * 32);
 #pragma unroll
@@ -434,7 +498,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                                                 pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
                     } else {
                         float4* dst = reinterpret_cast<float4*>(
-                            P.part_o + ((int64_t)tk.w * L.rows_cap + row) * D + c4 * 32);
+                            P.part_o + ((int64_t)rec.tk.w * L.rows_cap + r) * D + c4 * 32);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
                             dst[q] = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv,
@@ -443,14 +507,14 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 }
             }
             if (row_ok) {
-                if (tk.w < 0) {
+                if (rec.tk.w < 0) {
                     if (P.lse != nullptr) P.lse[(int64_t)token * Hq + head] = lse_nat;
                 } else {
-                    P.part_lse[(int64_t)tk.w * L.rows_cap + row] = lse_nat;
+                    P.part_lse[(int64_t)rec.tk.w * L.rows_cap + r] = lse_nat;
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bar[B_O_FREE]);
+            mbar_arrive(&o_free[h]);
         }
     }
 
@@ -466,6 +530,8 @@ int prefill_smem_bytes(int D, bool fp8) {
     if (D == 64) return PrefillCfg<64>::kSmemBytes;
     return -1;
 }
+
+int prefill_threads() { return 320; }
 
 const void* prefill_kernel_ptr(int D, bool fp8) {
     if (fp8) return nullptr;
@@ -506,9 +572,9 @@ cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (p.head_dim == 128)
-        prefill_kernel<128><<<L.N, 192, smem, stream>>>(P, tq, tk, tv);
+        prefill_kernel<128><<<L.N, PrefillCfg<128>::kThreads, smem, stream>>>(P, tq, tk, tv);
     else
-        prefill_kernel<64><<<L.N, 192, smem, stream>>>(P, tq, tk, tv);
+        prefill_kernel<64><<<L.N, PrefillCfg<64>::kThreads, smem, stream>>>(P, tq, tk, tv);
     return cudaGetLastError();
 }
 
