@@ -11,6 +11,7 @@ import concurrent.futures as cf
 import glob
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 
@@ -26,6 +27,32 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-I", INCLUDE, "-I", CSRC]
+
+
+# Kernels that move registers between warpgroups with setmaxnreg: the block
+# must be launched with exactly this many registers per thread, or the
+# warpgroups' requests would not add up to what the block holds and
+# setmaxnreg.inc could wait forever.  Checked on every build from ptxas -v.
+REGISTER_BUDGETS = {"pa_prefill.cu": ("prefill_kernel", 168)}
+
+
+def check_register_budget(src: str, ptxas_log: str) -> None:
+    kernel, want = REGISTER_BUDGETS[src]
+    current = None
+    seen = 0
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current and kernel in current:
+            seen += 1
+            if int(m.group(1)) != want:
+                raise RuntimeError(f"{current}: ptxas allocated {m.group(1)} registers, the "
+                                   f"setmaxnreg split assumes {want}")
+    if seen == 0:
+        raise RuntimeError(f"{src}: no ptxas register report for {kernel}")
 
 
 def nvcc() -> str:
@@ -68,10 +95,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
-        cmd = [cc, *flags, "-c", src, "-o", obj]
+        extra = ["-Xptxas", "-v"] if os.path.basename(src) in REGISTER_BUDGETS else []
+        cmd = [cc, *flags, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        if extra:
+            check_register_budget(os.path.basename(src), r.stdout + r.stderr)
         if verbose and (r.stdout or r.stderr):
             print(r.stdout, r.stderr)
         return obj

@@ -129,7 +129,7 @@ int resolve_ctas(const pa_problem& p, int mode) {
     } else {
         k = prefill_kernel_ptr(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
         smem = prefill_smem_bytes(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
-        threads = 320;
+        threads = 384;
     }
     if (k && smem > 0) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=

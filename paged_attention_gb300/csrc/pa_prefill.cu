@@ -11,24 +11,28 @@
 // Deep Dive": Q blocks pack the G q heads of one KV head into one MMA tile;
 // the persistent grid is fixed at the SM count.
 //
-// GB300 design (one CTA per SM, 320 threads).  A unit is up to 256 query
-// rows (G heads x 256/G tokens), computed as two 128-row halves that share
-// every K/V tile:
+// GB300 design (one CTA per SM, 384 threads = 3 warpgroups).  A unit is up
+// to 256 query rows (G heads x 256/G tokens), computed as two 128-row halves
+// that share every K/V tile.  Registers: of the 168 per thread the block is
+// launched with, setmaxnreg leaves warpgroup 0 with 88 and gives the two
+// softmax warpgroups 200 each: 128*88 + 256*200 <= 384*168.
 //   warp 0      TMA producer: the unit's Q halves once per task, then for
 //               every active 128-token KV tile its K and its V, page by page,
 //               each into its own entry of a ring (128-byte swizzle).
-//   warp 1      allocates the 512 TMEM columns; lane 0 issues every MMA:
+//   warps 1-2   warp 1 allocates the 512 TMEM columns; lane 0 of warp 1+h
+//               issues every MMA of half h:
 //               S_h = Q_h K^T (M=128, N=128, K=D, both operands K-major in
 //               shared memory) into TMEM, and O_h += P_h V (M=128, N=D,
 //               K=128) with P_h read from TMEM (written over S_h by the
 //               softmax) and V read MN-major from shared memory, so V is
-//               never transposed.  Issue order per tile j:
-//                 PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1)
+//               never transposed.  Per tile j each issuer runs
+//                 PV_h(j), QK_h(j+1)
 //               so the tensor cores work on one half while the other half's
 //               softmax runs; MMAs of one thread execute in issue order,
 //               which keeps QK_h(j+1) from overwriting P_h(j) before PV_h(j)
-//               has read it.  Also zeroes V rows past the context.
-//   warps 2-5   softmax for half 0, warps 6-9 for half 1: thread = query row
+//               has read it.  Warp 1 also zeroes V rows past the context.
+//   warp 3      idle.
+//   warps 4-7   softmax for half 0, warps 8-11 for half 1: thread = query row
 //               = TMEM lane.  Reads its S row (tcgen05.ld), applies the
 //               causal / context mask, keeps the running max lazily (O is
 //               rescaled in TMEM only when the max grows by more than 2^8),
@@ -73,7 +77,12 @@ struct PrefillCfg {
     static constexpr int kOffBar = kOffKV + kEntries * kKVBytes;
     static constexpr int kNumBars = 2 + 2 * kEntries + 9;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = 384;
+    static constexpr int kRegsLaunch = 168;          // 65536 / 384, rounded down to 8
+    static constexpr int kRegsProducer = 88;
+    static constexpr int kRegsSoftmax = 200;
+    static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+                  "register split exceeds the launch allocation");
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -83,7 +92,7 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
 prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ CUtensorMap tmq,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     using Cfg = PrefillCfg<D>;
@@ -114,10 +123,10 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     }
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        mbar_init(q_empty, 2);                 // one commit from each MMA warp
         for (int e = 0; e < E; ++e) {
             mbar_init(&kv_full[e], 1);
-            mbar_init(&kv_empty[e], 1);
+            mbar_init(&kv_empty[e], 2);
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(&s_full[h], 1);
@@ -125,7 +134,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             mbar_init(&o_done[h], 1);
             mbar_init(&o_free[h], 128);
         }
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -159,7 +168,9 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         return L.has_mask ? active[(int64_t)u * L.max_kv_tiles + t] : t;
     };
 
-    if (warp == 0) {
+    if (warp < 4) {
+      regs_dec<Cfg::kRegsProducer>();
+      if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             prefetch_tmap(&tmq);
@@ -244,43 +255,67 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------ MMA issuers
+        // warp 1 issues every MMA of half 0, warp 2 those of half 1: each
+        // issue blocks until the tensor pipe nearly drains it, so with one
+        // issuer per half one warp does its waits while the other issues.
+        // A token passed through two named barriers keeps the segments in
+        // the order half 0, half 1, half 0, ...: without it both halves'
+        // MMAs interleave on the pipe, finish together, and the two softmax
+        // groups then run at the same time while the tensor pipe idles.
+        // Both warps release each ring entry and the Q buffer (two commits
+        // per barrier phase).
         constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-        const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
-        const uint32_t sKV = smem_u32(smem + Cfg::kOffKV);
+        // Descriptor bases: the start-address field is the low bits of a
+        // descriptor, so a byte offset within the buffer is added as offset >> 4.
+        const uint64_t dQ = smem_desc_sw128(smem_u32(smem + Cfg::kOffQ), 16, 1024);
+        const uint64_t dK = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), 16, 1024);
+        const uint64_t dV = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), Cfg::kRegion, 1024);
         int e_it = 0, task_it = 0;
         int p_cnt[2] = {0, 0}, of_cnt[2] = {0, 0};
         TaskRec mine;
 
         auto issue_qk = [&](int h, int e) {   // S_h = Q_h K^T from ring entry e
-            const uint32_t sK = sKV + e * Cfg::kKVBytes;
-            const uint32_t sQh = sQ + h * Cfg::kQTileBytes;
+            const uint64_t a0 = dQ + (uint64_t)((h * Cfg::kQTileBytes) >> 4);
+            const uint64_t b0 = dK + (uint64_t)((e * Cfg::kKVBytes) >> 4);
+            const uint32_t d = tmem + h * 256;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t koff = (kk >> 2) * Cfg::kRegion + (kk & 3) * 32;
-                tc_mma_ss(tmem + h * 256, smem_desc_sw128(sQh + koff, 16, 1024),
-                          smem_desc_sw128(sK + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                const uint64_t koff = (uint64_t)((((kk >> 2) * Cfg::kRegion) + (kk & 3) * 32) >> 4);
+                tc_mma_ss(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
             }
             tc_commit(&s_full[h]);
         };
         auto issue_pv = [&](int h, int e, bool first) {   // O_h += P_h V from ring entry e
-            const uint32_t sV = sKV + e * Cfg::kKVBytes;
+            const uint64_t b0 = dV + (uint64_t)((e * Cfg::kKVBytes) >> 4);
+            const uint32_t d = tmem + h * 256 + 128, a = tmem + h * 256;
 #pragma unroll
             for (int kk = 0; kk < kPrefillTile / 16; ++kk)
-                tc_mma_ts(tmem + h * 256 + 128, tmem + h * 256 + kk * 8,
-                          smem_desc_sw128(sV + kk * 16 * 128, Cfg::kRegion, 1024), idesc_pv,
+                tc_mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
                           (!first || kk > 0) ? 1u : 0u);
             tc_commit(&o_done[h]);
         };
 
+        const int h = warp - 1;                // the half this warp issues for
+        // segment token: half 1 waits for half 0's segment (barrier 2); half 0
+        // waits for half 1's previous segment (barrier 3), except the first
+        bool first_segment = true;
+        auto token_wait = [&]() {
+            if (h == 1)
+                named_bar_sync(2, 64);
+            else if (!first_segment)
+                named_bar_sync(3, 64);
+            first_segment = false;
+        };
+        auto token_pass = [&]() { named_bar_arrive(h == 0 ? 2 : 3, 64); };
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
             if (((k - k_begin) & 31) == 0)
                 mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
             const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
             const int u = rec.tk.x;
-            const int H = G * rec.un.w > kPrefillHalfRows ? 2 : 1;
+            const bool mine_half = h == 0 || G * rec.un.w > kPrefillHalfRows;
             const int n = rec.tk.z - rec.tk.y;
             const int ctx_b = rec.ctx;
             wait(q_full, (uint32_t)(task_it & 1));
@@ -288,66 +323,78 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             {
                 const int eK = e_it;
                 wait(&kv_full[eK % E], (uint32_t)((eK / E) & 1));
+                token_wait();
                 if (lane == 0) {
                     tc_fence_after();
-                    for (int h = 0; h < H; ++h) issue_qk(h, eK % E);
+                    if (mine_half) issue_qk(h, eK % E);
                     tc_commit(&kv_empty[eK % E]);
                     if (n == 1) tc_commit(q_empty);
                 }
                 __syncwarp();
+                token_pass();
             }
             for (int j = 0; j < n; ++j) {
                 const int eV = e_it + 2 * j + 1, eKn = e_it + 2 * j + 2;
                 wait(&kv_full[eV % E], (uint32_t)((eV / E) & 1));
                 {
-                    // zero V rows of keys past the context (P is 0 there, 0 * NaN is not)
+                    // zero V rows of keys past the context (P is 0 there, 0 * NaN is
+                    // not): warp 1 writes, both MMA warps meet before their PV
                     const int kt = tile_of(u, rec.tk.y + j);
                     const int first_bad = ctx_b - kt * kPrefillTile;
                     if (first_bad < kPrefillTile) {
-                        uint8_t* sVp = smem + Cfg::kOffKV + (eV % E) * Cfg::kKVBytes;
-                        const int r0 = first_bad < 0 ? 0 : first_bad;
-                        for (int idx = lane; idx < (kPrefillTile - r0) * Cfg::kHalves * 8; idx += 32) {
-                            const int r = r0 + idx / (Cfg::kHalves * 8);
-                            const int rem = idx % (Cfg::kHalves * 8);
-                            *reinterpret_cast<uint4*>(sVp + (rem >> 3) * Cfg::kRegion +
-                                                      swz128(r, rem & 7)) = make_uint4(0u, 0u, 0u, 0u);
+                        if (h == 0) {
+                            uint8_t* sVp = smem + Cfg::kOffKV + (eV % E) * Cfg::kKVBytes;
+                            const int r0 = first_bad < 0 ? 0 : first_bad;
+                            for (int idx = lane; idx < (kPrefillTile - r0) * Cfg::kHalves * 8;
+                                 idx += 32) {
+                                const int r = r0 + idx / (Cfg::kHalves * 8);
+                                const int rem = idx % (Cfg::kHalves * 8);
+                                *reinterpret_cast<uint4*>(sVp + (rem >> 3) * Cfg::kRegion +
+                                                          swz128(r, rem & 7)) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            fence_proxy_async_smem();
                         }
-                        fence_proxy_async_smem();
+                        named_bar_sync(1, 64);
                     }
-                    __syncwarp();
                 }
-                for (int h = 0; h < H; ++h) {
+                if (j + 1 < n) wait(&kv_full[eKn % E], (uint32_t)((eKn / E) & 1));
+                if (mine_half) {
                     wait(&p_full[h], (uint32_t)(p_cnt[h] & 1));
                     ++p_cnt[h];
                     if (j == 0) {
                         wait(&o_free[h], (uint32_t)(of_cnt[h] & 1) ^ 1u);
                         ++of_cnt[h];
                     }
-                    if (j + 1 < n && h == 0) wait(&kv_full[eKn % E], (uint32_t)((eKn / E) & 1));
-                    if (lane == 0) {
+                }
+                token_wait();
+                if (lane == 0) {
+                    if (mine_half) {
                         tc_fence_after();
                         issue_pv(h, eV % E, j == 0);
                         if (j + 1 < n) issue_qk(h, eKn % E);
                     }
-                    __syncwarp();
-                }
-                if (lane == 0) {
                     tc_commit(&kv_empty[eV % E]);
                     if (j + 1 < n) tc_commit(&kv_empty[eKn % E]);
                     if (j + 1 == n - 1) tc_commit(q_empty);
                 }
                 __syncwarp();
+                token_pass();
             }
             e_it += 2 * n;
         }
+        // consume half 1's last token so every barrier arrival is matched
+        if (h == 0 && !first_segment) named_bar_sync(3, 64);
         if (lane == 0) {
             tc_commit(mma_done);
             mbar_wait(mma_done, 0, lim);
         }
         __syncwarp();
+      }
     } else {
+        regs_inc<Cfg::kRegsSoftmax>();
         // --------------------------------------------------- softmax (2 halves)
-        const int h = (warp - 2) >> 2;
+        const int h = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int row = wq * 32 + lane;              // row inside the half = TMEM lane
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -388,22 +435,23 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     continue;
                 }
                 const int limc = row_ok ? key_last - kt * kPrefillTile : -1;   // valid: c <= limc
-                // pass 1: row max over the tile, 64 columns at a time.  Fully
-                // visible chunks take the max of the raw scores (sm_scale >= 0).
+                // pass 1: row max of the raw scores (sm_scale >= 0 keeps the order),
+                // 32 columns at a time; the two softmax warps on each SM
+                // sub-partition hide each other's TMEM latency
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    float s[64];
-                    tmem_ld32(tS + hh * 64, s);
-                    tmem_ld32(tS + hh * 64 + 32, s + 32);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    float s[32];
+                    tmem_ld32(tS + c4 * 32, s);
                     tmem_wait_ld();
-                    const int lim = limc - hh * 64;
-                    if (lim >= 63) {
+                    reg_fence32(s);
+                    const int lim = limc - c4 * 32;
+                    if (lim >= 31) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
+                        for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
+                        for (int c = 0; c < 32; ++c)
                             mx4[c & 3] = fmaxf(mx4[c & 3], c <= lim ? s[c] : -INFINITY);
                     }
                 }
@@ -420,6 +468,40 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     m = mx;
                 }
                 const float mu = m == -INFINITY ? 0.f : m;
+                // pass 2: P = exp2(s * scale - m) in bf16, two exponentials per MUFU
+                // operation on full chunks (f16 holds x <= 8 to 2^-9 relative, below
+                // P's own bf16 rounding); keys [32c, 32c+32) go to S columns
+                // [16c, 16c+16), which every later chunk has already read
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    float s[32];
+                    tmem_ld32(tS + c4 * 32, s);
+                    tmem_wait_ld();
+                    reg_fence32(s);
+                    const int lim = limc - c4 * 32;
+                    uint32_t pk[16];
+                    if (lim >= 31) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const uint32_t e2 = ex2_h2(fmaf(s[c], scale_log2, -mu),
+                                                       fmaf(s[c + 1], scale_log2, -mu));
+                            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&e2));
+                            sum4[(c >> 1) & 3] += pf.x + pf.y;
+                            pk[c >> 1] = pack_bf16x2(pf.x, pf.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float p0 = c <= lim ? ex2(fmaf(s[c], scale_log2, -mu)) : 0.f;
+                            const float p1 =
+                                c + 1 <= lim ? ex2(fmaf(s[c + 1], scale_log2, -mu)) : 0.f;
+                            sum4[(c >> 1) & 3] += p0 + p1;
+                            pk[c >> 1] = pack_bf16x2(p0, p1);
+                        }
+                    }
+                    tmem_st16(tS + c4 * 16, pk);
+                }
                 if (j > 0) {
                     wait(&o_done[h], (uint32_t)(o_cnt & 1));   // PV of the previous tile
                     ++o_cnt;
@@ -432,40 +514,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         float o[32];
                         tmem_ld32(tO + c4 * 32, o);
                         tmem_wait_ld();
+                        reg_fence32(o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= f;
                         tmem_st32(tO + c4 * 32, o);
                     }
-                }
-                // pass 2: P = exp2(s * scale - m) in bf16, written over the S columns
-                // already read
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    float s[64];
-                    tmem_ld32(tS + hh * 64, s);
-                    tmem_ld32(tS + hh * 64 + 32, s + 32);
-                    tmem_wait_ld();
-                    const int lim = limc - hh * 64;
-                    uint32_t pk[32];
-                    if (lim >= 63) {
-#pragma unroll
-                        for (int c = 0; c < 64; c += 2) {
-                            const float p0 = ex2(fmaf(s[c], scale_log2, -mu));
-                            const float p1 = ex2(fmaf(s[c + 1], scale_log2, -mu));
-                            sum4[(c >> 1) & 3] += p0 + p1;
-                            pk[c >> 1] = pack_bf16x2(p0, p1);
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 64; c += 2) {
-                            const float p0 = c <= lim ? ex2(fmaf(s[c], scale_log2, -mu)) : 0.f;
-                            const float p1 = c + 1 <= lim ? ex2(fmaf(s[c + 1], scale_log2, -mu)) : 0.f;
-                            sum4[(c >> 1) & 3] += p0 + p1;
-                            pk[c >> 1] = pack_bf16x2(p0, p1);
-                        }
-                    }
-                    tmem_st32(tS + hh * 32, reinterpret_cast<const float*>(pk));
                 }
                 l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
                 tmem_wait_st();
@@ -486,6 +539,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 float o[32];
                 tmem_ld32(tO + c4 * 32, o);
                 tmem_wait_ld();
+                reg_fence32(o);
                 if (row_ok) {
                     if (rec.tk.w < 0) {
                         uint4* dst = reinterpret_cast<uint4*>(
@@ -531,7 +585,7 @@ int prefill_smem_bytes(int D, bool fp8) {
     return -1;
 }
 
-int prefill_threads() { return 320; }
+int prefill_threads() { return 384; }
 
 const void* prefill_kernel_ptr(int D, bool fp8) {
     if (fp8) return nullptr;
