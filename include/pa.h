@@ -29,7 +29,8 @@
  *   - Every pointer argument except those marked "host" is a DEVICE pointer.
  *     The caller owns every buffer; the library allocates no device memory
  *     and keeps no per-call state.  (It caches, per device, the SM count and
- *     per-kernel attributes.)
+ *     per-kernel attributes.  The one exception is pa_decode_noalloc, whose
+ *     fixed scratch array belongs to the library.)
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All calls
  *     are asynchronous on that stream except pa_read_task_map and
  *     pa_last_device_error, which synchronise it.
@@ -65,7 +66,8 @@ typedef enum pa_status {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1,  /* null pointer, bad dimension, misaligned buffer       */
     PA_ERR_UNSUPPORTED = 2,  /* valid but not built (head_dim, page_size, GQA ratio) */
-    PA_ERR_WORKSPACE = 3,    /* a workspace smaller than the *_workspace_size query */
+    PA_ERR_WORKSPACE = 3,    /* a workspace smaller than the *_workspace_size query, or a
+                                problem too large for the scratch of pa_decode_noalloc */
     PA_ERR_CUDA = 4,         /* a CUDA runtime call failed                           */
     PA_ERR_DEVICE_CHECK = 5, /* the device recorded a fault (pa_last_device_error)   */
     PA_ERR_TIMEOUT = 6       /* a bounded device wait ran out                        */
@@ -189,6 +191,54 @@ PA_API pa_status pa_decode_splitk(const pa_problem* problem, const void* q, cons
 PA_API pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
                      size_t assign_ws_bytes, const void* partial_ws, size_t partial_ws_bytes,
                      void* out, float* lse, void* stream);
+
+/* Size of the fixed device scratch array behind pa_decode_noalloc: 32 MiB. */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * Whole decode (Assign, Split-K compute, Combine: the same three passes and
+ * results as pa_assign + pa_decode_splitk + pa_combine in PA_MODE_DECODE)
+ * with every workspace taken from a fixed scratch array inside the library
+ * instead of caller buffers.  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.  The pages describe no such entry
+ * point; it is an addition of this library.
+ *
+ * Who it is for: callers that cannot hand the library device memory at call
+ * time -- a serving engine that gave all free HBM to its KV-cache page pool up
+ * front, or a plain C host with no device allocator of its own.  An
+ * allocation inside the call would also cost latency and can synchronise the
+ * device.
+ *
+ * The scratch is one file-scope device array of PA_NOALLOC_SCRATCH_BYTES
+ * bytes.  Every GPU that loads the library holds it, whether or not this
+ * entry point is called, until the process exits.
+ *
+ * Limit: the problem must fit, i.e. pa_assign_workspace_size (rounded up to
+ * 256) + pa_partial_workspace_size, both for PA_MODE_DECODE, must be at most
+ * PA_NOALLOC_SCRATCH_BYTES; otherwise the call returns PA_ERR_WORKSPACE and
+ * launches nothing (use the caller-workspace entry points for such problems).
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it.  Make that
+ * first call on every device before any stream capture starts.
+ *
+ * Sharing: all calls on one device use the same array.  Two calls that may
+ * run at the same time on one device (different streams without ordering,
+ * several host threads) race and corrupt each other's results; order them on
+ * one stream or synchronise between them.  Nothing needs clearing between
+ * calls: Assign rewrites every scratch word the later passes read, and its
+ * first kernel resets the device error word.
+ *
+ *   Arguments as pa_decode_splitk (out and lse receive the final result).
+ *   device_error: int32, DEVICE pointer or NULL.  When given, the device
+ *     error word of this call (PA_DEV_* bits) is copied there, on `stream`,
+ *     after Combine.
+ */
+PA_API pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_table,
+                                   const int32_t* context_lens, const int32_t* q_lens,
+                                   const float* k_scale, const float* v_scale, void* out,
+                                   float* lse, int32_t* device_error, void* stream);
 
 /*
  * Prefill / mixed-batch compute ("基于Triton-TLE…", 一.2 Prefill: tile

@@ -23,6 +23,7 @@ import torch
 from . import build as _build
 
 PA_OK = 0
+PA_ERR_WORKSPACE = 3
 PA_NHD, PA_HND = 0, 1
 PA_BF16, PA_FP8_E4M3 = 0, 1
 PA_MODE_DECODE, PA_MODE_PREFILL = 0, 1
@@ -31,8 +32,10 @@ PA_DEV_OK, PA_DEV_BAD_LENGTHS, PA_DEV_BAD_PAGE, PA_DEV_WAIT_TIMEOUT = 0, 1, 2, 4
 EXPORTED = (
     "pa_status_string", "pa_version", "pa_num_ctas", "pa_assign_workspace_size",
     "pa_partial_workspace_size", "pa_assign", "pa_decode_splitk", "pa_combine", "pa_prefill",
-    "pa_read_task_map", "pa_last_device_error",
+    "pa_read_task_map", "pa_last_device_error", "pa_decode_noalloc",
 )
+
+PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # size of the library's fixed scratch
 
 
 class PaError(RuntimeError):
@@ -101,6 +104,7 @@ def load(build_if_missing: bool = True):
                                  vp]),
             "pa_read_task_map": (i32, [PP, i32, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pa_last_device_error": (i32, [vp, ctypes.POINTER(ctypes.c_int32), vp]),
+            "pa_decode_noalloc": (i32, [PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -190,6 +194,19 @@ def pa_combine(problem, mode, assign_ws, partial_ws, out, lse, stream=None):
     _check(load().pa_combine(ctypes.byref(problem), mode, _p(assign_ws), _nbytes(assign_ws),
                              _p(partial_ws), _nbytes(partial_ws), _p(out), _p(lse),
                              _stream(stream)), "pa_combine")
+
+
+def pa_decode_noalloc(problem, q, k_cache, v_cache, block_table, context_lens, q_lens, k_scale,
+                      v_scale, out, lse, device_error=None, stream=None):
+    """Whole decode with the library's fixed scratch (no workspace arguments)."""
+    status = load().pa_decode_noalloc(
+        ctypes.byref(problem), _p(q), _p(k_cache), _p(v_cache), _p(block_table),
+        _p(context_lens), _p(q_lens), _p(k_scale), _p(v_scale), _p(out), _p(lse),
+        _p(device_error), _stream(stream))
+    if status == PA_ERR_WORKSPACE:
+        raise PaError(status, f"pa_decode_noalloc (the problem needs more than the "
+                              f"{PA_NOALLOC_SCRATCH_BYTES} bytes of fixed scratch)")
+    _check(status, "pa_decode_noalloc")
 
 
 def pa_prefill(problem, q, k_cache, v_cache, block_table, context_lens, q_lens, k_scale, v_scale,

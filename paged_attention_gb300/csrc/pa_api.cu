@@ -293,6 +293,36 @@ bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L)
     return true;
 }
 
+// ------------------------------------------- fixed scratch of pa_decode_noalloc
+// One array per device for the whole process: the task map at offset 0, the
+// split-K partials after it.  Being part of the module image, it exists on
+// every device that loads the library.  In host code the name below is only a
+// host-side stand-in that the CUDA runtime links to the device copy; the
+// device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch on the current device, looked up on the first
+// call for that device and cached.
+pa_status noalloc_scratch(char** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+            return PA_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = static_cast<char*>(g_noalloc_ptr[dev]);
+    return PA_OK;
+}
+
+}  // namespace
+
 }  // namespace pa
 
 using namespace pa;
@@ -399,6 +429,53 @@ pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
     if (grid > L.unit_cap) grid = L.unit_cap;
     if (grid < 1) grid = 1;
     cudaError_t e = launch_combine(L, assign_ws, partial_ws, out, lse, grid, (cudaStream_t)stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_table,
+                            const int32_t* context_lens, const int32_t* q_lens,
+                            const float* k_scale, const float* v_scale, void* out, float* lse,
+                            int32_t* device_error, void* stream) {
+    WsLayout L;
+    pa_status st = make_layout(problem, PA_MODE_DECODE, L);
+    if (st != PA_OK) return st;
+    const pa_problem& p = *problem;
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !out ||
+        !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(q_lens, 4) ||
+        !aligned(device_error, 4))
+        return PA_ERR_INVALID_ARG;
+    if (p.kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+    // task map first, partials from the next 256-byte boundary; both must fit
+    const int64_t part_off = align256(L.total_bytes);
+    if (part_off + L.partial_bytes > (int64_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+    CUtensorMap tq, tk, tv;
+    if (!encode_q_map(p, q, p.max_q_len > 0 ? p.max_q_len : 1, &tq)) return PA_ERR_INVALID_ARG;
+    bool one_box = encode_kv_map_one_box(p, k_cache, &tk) && encode_kv_map_one_box(p, v_cache, &tv);
+    if (!one_box && (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv)))
+        return PA_ERR_INVALID_ARG;
+    char* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != PA_OK) return st;
+    void* ws = scratch;
+    void* partial = scratch + part_off;
+    const cudaStream_t s = (cudaStream_t)stream;
+    // Assign resets the error word and rewrites every word read below
+    cudaError_t e = launch_assign(L, context_lens, q_lens, nullptr, ws, s);
+    if (e == cudaSuccess)
+        e = launch_decode_from_api(p, L, decode_row_tiles(p), tq, tk, tv, one_box, block_table,
+                                   context_lens, q_lens, k_scale, v_scale, ws, partial, out, lse,
+                                   s);
+    if (e == cudaSuccess) {
+        int grid = 2 * sm_count();
+        if (grid > L.unit_cap) grid = L.unit_cap;
+        if (grid < 1) grid = 1;
+        e = launch_combine(L, ws, partial, out, lse, grid, s);
+    }
+    if (e == cudaSuccess && device_error)
+        e = cudaMemcpyAsync(device_error, scratch + L.off_header + H_ERROR * 4, 4,
+                            cudaMemcpyDeviceToDevice, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

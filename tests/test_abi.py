@@ -84,3 +84,28 @@ def test_invalid_problems_rejected_on_host(lib):
     # null device pointers are refused before any CUDA call
     st = lib.pa_assign(ctypes.byref(p), 0, None, None, None, None, 0, None)
     assert st == 1
+
+
+def test_noalloc_host_checks(lib):
+    """pa_decode_noalloc refuses, before any CUDA call, null pointers and
+    problems whose task map + partials exceed the fixed scratch."""
+    w = W.decode_bf16(mtp=1, shrink=16)
+    p = B.problem_from(w, num_ctas=152)
+    fake = ctypes.c_void_p(1 << 20)           # aligned, never dereferenced
+    args = [fake] * 10
+    st = lib.pa_decode_noalloc(ctypes.byref(p), None, *args[:9], None, None)
+    assert st == 1
+    need = (-(-B.pa_assign_workspace_size(p, B.PA_MODE_DECODE) // 256) * 256
+            + B.pa_partial_workspace_size(p, B.PA_MODE_DECODE))
+    assert need <= B.PA_NOALLOC_SCRATCH_BYTES
+    big = B.PaProblem.from_buffer_copy(p)
+    big.num_seqs = 4096                       # (4096 * 8 + 152) slots x 16 rows x 129 x 4 B
+    big.num_ctas = 152
+    big_need = (-(-B.pa_assign_workspace_size(big, B.PA_MODE_DECODE) // 256) * 256
+                + B.pa_partial_workspace_size(big, B.PA_MODE_DECODE))
+    assert big_need > B.PA_NOALLOC_SCRATCH_BYTES
+    st = lib.pa_decode_noalloc(ctypes.byref(big), *args, None, None)
+    assert st == B.PA_ERR_WORKSPACE
+    assert B.PA_NOALLOC_SCRATCH_BYTES == 32 * 1024 * 1024
+    header = open(os.path.join(ROOT, "include", "pa.h")).read()
+    assert "#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)" in header
