@@ -352,7 +352,7 @@ def load_traffic(kernel, workload):
             d = json.load(f)
         from paged_attention_gb300 import build as build_mod
         entry = d.get(f"{kernel}:{workload}")
-        if not entry or entry.get("source_hash") != build_mod._fingerprint()[:16]:
+        if not entry or entry.get("source_hash") != build_mod.kernel_fingerprint(kernel):
             return None
         return entry.get("dram_bytes_per_launch")
     except Exception:

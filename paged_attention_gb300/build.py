@@ -80,6 +80,28 @@ def _fingerprint() -> str:
     return h.hexdigest()
 
 
+# Sources that decide what one kernel does on the device (its own file, the
+# shared device helpers, the launcher / tensor-map code and the ABI header).
+KERNEL_SOURCES = {
+    "pa_decode_splitk": ("pa_decode.cu",),
+    "pa_prefill": ("pa_prefill.cu",),
+}
+
+
+def kernel_fingerprint(kernel: str) -> str:
+    """Short hash of the sources of one entry point's kernel; stored beside
+    counters taken from that kernel so stale counters can be recognised."""
+    h = hashlib.sha256()
+    files = [os.path.join(CSRC, f) for f in KERNEL_SOURCES[kernel]] + [
+        os.path.join(CSRC, "pa_internal.cuh"), os.path.join(CSRC, "pa_api.cu"),
+        os.path.join(INCLUDE, "pa.h")]
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS[:4]).encode())
+    return h.hexdigest()[:16]
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     """Compile and link the library; returns its path.  Skips work when the
     sources are unchanged since the last build."""
