@@ -33,7 +33,8 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
 # must be launched with exactly this many registers per thread, or the
 # warpgroups' requests would not add up to what the block holds and
 # setmaxnreg.inc could wait forever.  Checked on every build from ptxas -v.
-REGISTER_BUDGETS = {"pa_prefill.cu": ("prefill_kernel", 168)}
+REGISTER_BUDGETS = {"pa_prefill.cu": ("prefill_kernel", 168),
+                    "pa_decode_fp8.cu": ("decode_fp8_kernel", 168)}
 
 
 def check_register_budget(src: str, ptxas_log: str) -> None:
@@ -83,7 +84,7 @@ def _fingerprint() -> str:
 # Sources that decide what one kernel does on the device (its own file, the
 # shared device helpers, the launcher / tensor-map code and the ABI header).
 KERNEL_SOURCES = {
-    "pa_decode_splitk": ("pa_decode.cu",),
+    "pa_decode_splitk": ("pa_decode.cu", "pa_decode_fp8.cu", "pa_decode_common.cuh"),
     "pa_prefill": ("pa_prefill.cu",),
 }
 

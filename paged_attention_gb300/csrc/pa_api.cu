@@ -16,10 +16,10 @@ cudaError_t launch_assign(const WsLayout& L, const int32_t* ctx, const int32_t* 
                           const uint8_t* mask, void* ws, cudaStream_t stream);
 cudaError_t launch_combine(const WsLayout& L, const void* ws, const void* partial, void* out,
                            float* lse, int grid, cudaStream_t stream);
-int decode_smem_bytes(int D, int RT, bool fp8);
-int decode_threads(int D, int RT, bool fp8);
-const void* decode_kernel_ptr(int D, int RT, bool fp8);
-cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L, int RT,
+int decode_smem_bytes(const pa_problem& p);
+int decode_threads(const pa_problem& p);
+const void* decode_kernel_ptr(const pa_problem& p);
+cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
                                    const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, bool kv_one_box,
                                    const int32_t* block_table,
@@ -122,10 +122,9 @@ int resolve_ctas(const pa_problem& p, int mode) {
     const void* k = nullptr;
     int smem = 0, threads = 0;
     if (mode == PA_MODE_DECODE) {
-        const int RT = decode_row_tiles(p);
-        k = decode_kernel_ptr(p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3);
-        smem = decode_smem_bytes(p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3);
-        threads = decode_threads(p.head_dim, RT, p.kv_dtype == PA_FP8_E4M3);
+        k = decode_kernel_ptr(p);
+        smem = decode_smem_bytes(p);
+        threads = decode_threads(p);
     } else {
         k = prefill_kernel_ptr(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
         smem = prefill_smem_bytes(p.head_dim, p.kv_dtype == PA_FP8_E4M3);
@@ -406,7 +405,7 @@ pa_status pa_decode_splitk(const pa_problem* problem, const void* q, const void*
     bool one_box = encode_kv_map_one_box(p, k_cache, &tk) && encode_kv_map_one_box(p, v_cache, &tv);
     if (!one_box && (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv)))
         return PA_ERR_INVALID_ARG;
-    cudaError_t e = launch_decode_from_api(p, L, decode_row_tiles(p), tq, tk, tv, one_box,
+    cudaError_t e = launch_decode_from_api(p, L, tq, tk, tv, one_box,
                                            block_table,
                                            context_lens, q_lens, k_scale, v_scale,
                                            const_cast<void*>(assign_ws), partial_ws, out, lse,
@@ -464,7 +463,7 @@ pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void
     // Assign resets the error word and rewrites every word read below
     cudaError_t e = launch_assign(L, context_lens, q_lens, nullptr, ws, s);
     if (e == cudaSuccess)
-        e = launch_decode_from_api(p, L, decode_row_tiles(p), tq, tk, tv, one_box, block_table,
+        e = launch_decode_from_api(p, L, tq, tk, tv, one_box, block_table,
                                    context_lens, q_lens, k_scale, v_scale, ws, partial, out, lse,
                                    s);
     if (e == cudaSuccess) {

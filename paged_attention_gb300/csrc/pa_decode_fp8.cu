@@ -1,0 +1,537 @@
+// pa_decode_fp8.cu -- persistent split-K decode compute for E4M3 K/V caches.
+//
+// "基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2 (Split-K Compute:
+// persistent CTAs follow the task map and emit a final or partial output with
+// its LSE), 三.1 (small-M geometry: the G*q_len query rows of one KV head
+// share every K/V tile), 三.2 (paged K/V through one tile descriptor for NHD
+// and HND); FP8 KV with fp32 scales per (page, KV head).
+//
+// GB300 design.  One CTA per SM, persistent over Assign's task map:
+//   warps 0..3   the shared TMA producer (pa_decode_common.cuh), tile
+//                it on warp it % 4: the unit's Q rows into one of two Q slots,
+//                64-token K and V tiles of E4M3 bytes into a kStages ring,
+//                each page's scales beside them.
+//   warps 4..11  consumers: 2 tile groups (one warpgroup each) x 4 token
+//                slices.  Group g takes the tiles with index % 2 == g; warp
+//                (g, ts) owns tokens [16ts, 16ts+16) of its tiles and all
+//                R = G*q_len <= 8*NT rows.
+// Launched with 168 registers a thread (three warps per SM sub-partition);
+// setmaxnreg moves them to 72 for the producer warpgroup and 216 for the
+// consumers, who hold the O^T accumulators (32*NT floats) in registers.
+// The decode is HBM-bound: at ~70 % of HBM an SM must retire a 16 KB tile
+// every ~1100 cycles, so the consumers may not spend a shared-memory round
+// trip and a barrier per tile on turning E4M3 into something the MMA takes.
+// Instead the bytes go from the ring straight into mma.sync fragments:
+//   - Scores are computed transposed, S^T = K Q^T (m16n8k16, M = 16 tokens,
+//     N = 8 rows per n-tile, K = head_dim).  The K operand is then the
+//     row-major E4M3 tile, and a thread's A-fragment pairs are consecutive
+//     bytes of one token's row once head_dim is visited in a permuted order:
+//     thread quad q reads bytes [32q, 32q+32) of a row, k-block kk uses the 4
+//     bytes at 32q + 4kk.  Each 16-bit pair converts with one exact
+//     cvt.rn.f16x2.e4m3x2.  Q is converted once per task to f16 in shared
+//     memory and read in the same order.
+//   - P^T leaves the score accumulators in the C-fragment layout; one
+//     movmatrix transpose per 8x8 block makes it the B operand of
+//     O^T = V^T P^T.  The V^T A-fragments pair two tokens' bytes at one
+//     head_dim position (prmt with sign replication), which turns into a bf16
+//     holding the E4M3 value times 2^-120 with a shift and a mask -- exact for
+//     every byte.  P carries v_scale * 2^64 in bf16 (fp32 range: no overflow
+//     for any scale), and the remaining 2^56 is applied with 1/l at the end.
+//   - A warp releases its ring stage as soon as its slice's 128 bytes of K
+//     and V are in registers; no converted copy is written and no barrier is
+//     taken per tile.
+// Per task the 4*NG partial (m, l, O) states of the unit merge through
+// shared memory (two rounds, fixed order: deterministic).
+#include "pa_decode_common.cuh"
+
+namespace pa {
+
+template <int NT, int STAGES>
+struct DecodeFp8Cfg {
+    static constexpr int D = 128;
+    // geometry the shared producer reads
+    static constexpr int kStages = STAGES;
+    static constexpr int kProducerWarps = 4;                 // the whole first warpgroup
+    static constexpr bool kFP8 = true;
+    static constexpr int kElem = 1;
+    static constexpr int kHalves = 1;                         // a K/V row is 128 bytes
+    static constexpr int kHalfBytes = kDecodeTile * 128;      // 64 rows x 128 B
+    static constexpr int kKBytes = kHalfBytes;
+    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kRows = 8 * NT;                      // unit rows covered
+    static constexpr int kQHalves = 2;                        // Q is bf16: two column blocks
+    static constexpr int kQHalfBytes = kRows * 128;
+    static constexpr int kQSlotBytes = kQHalves * kQHalfBytes;
+    // consumers
+    static constexpr int NG = 2;                              // tile groups
+    static constexpr int kConsumerWarps = 4 * NG;
+    static constexpr int kConsumerThreads = 32 * kConsumerWarps;
+    static constexpr int kThreads = 128 + kConsumerThreads;   // producer warpgroup + consumers
+    static constexpr int kRegsLaunch = 168;
+    static constexpr int kRegsProducer = 72;
+    static constexpr int kRegsConsumer = 216;
+    static_assert(128 * kRegsProducer + kConsumerThreads * kRegsConsumer <=
+                      kThreads * kRegsLaunch,
+                  "setmaxnreg split exceeds the registers the block is launched with");
+    static constexpr int kQhBytes = kRows * D * 2;            // f16 Q
+    static constexpr int kMergeStride = D + 4;                // floats per merge row
+    static constexpr int kMergeBufs = 4;
+    static constexpr int kMergeBytes = kMergeBufs * kRows * kMergeStride * 4;
+    static constexpr int kMLBytes = kConsumerWarps * kRows * 2 * 4;
+    static constexpr int kScaleBytes = STAGES * 2 * 4 * 4;
+    static constexpr int kOffQ = STAGES * kStageBytes;
+    static constexpr int kOffQh = kOffQ + 2 * kQSlotBytes;
+    static constexpr int kOffMerge = kOffQh + kQhBytes;
+    static constexpr int kOffML = kOffMerge + kMergeBytes;
+    static constexpr int kOffScale = kOffML + kMLBytes;
+    static constexpr int kOffBar = (kOffScale + kScaleBytes + 15) / 16 * 16;
+    static constexpr int kNumBars = 2 * STAGES + 4;
+    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+    static_assert(NT >= 1 && NT <= 4, "rows per unit");
+    // every ring stage is always consumed by the same group (a group that
+    // reused a stage after the other could wait two phases ahead)
+    static_assert(STAGES % NG == 0, "stages must be a multiple of the tile groups");
+    static_assert(kQHalfBytes % 1024 == 0, "Q slot alignment for the 128-byte swizzle");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+// 16-byte chunk c (head_dim [8c, 8c+8)) of f16 Q row r: chunks 8..15 are
+// XOR-ed with 2 and odd rows with 1, so that the eight lanes of each
+// 128-bit load phase (two rows, four thread quads) hit eight distinct bank
+// groups.
+__device__ __forceinline__ int qh_chunk(int c, int r) { return c ^ ((c >> 3) << 1) ^ (r & 1); }
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+    return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <int NT, int STAGES>
+__global__ void __launch_bounds__(384, 1)
+decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap tmq,
+                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    using Cfg = DecodeFp8Cfg<NT, STAGES>;
+    static_assert(Cfg::kThreads == 384, "launch bounds");
+    constexpr int NG = Cfg::NG;
+    constexpr int D = Cfg::D;
+    constexpr int kRows = Cfg::kRows;
+    constexpr int kCW = Cfg::kConsumerWarps;
+    constexpr int kCT = Cfg::kConsumerThreads;
+    constexpr int kBarConsumers = 1;           // named barrier of the consumer warps
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
+    uint64_t* empty = full + STAGES;
+    uint64_t* q_full = empty + STAGES;       // 2 slots
+    uint64_t* q_empty = q_full + 2;          // 2 slots
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
+    float* scales = reinterpret_cast<float*>(smem + Cfg::kOffScale);   // [stage][k|v][box]
+    const WsLayout& L = P.L;
+    int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t lim = P.wait_limit_ns;
+
+    if (header[H_CTAS] != (int)gridDim.x) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(header, PA_DEV_BAD_LENGTHS);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);          // the 4 slice warps of the stage's group
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], kCW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (*abort_flag) return;
+        if (!mbar_wait(bar, parity, lim)) {
+            *abort_flag = 1;
+            set_device_error(header, PA_DEV_WAIT_TIMEOUT);
+        }
+    };
+
+    const int32_t* cta_ptr = ws_ptr<int32_t>(P.ws, L.off_cta_ptr);
+    const int k_begin = cta_ptr[blockIdx.x], k_end = cta_ptr[blockIdx.x + 1];
+
+    if (warp < 4) {
+        regs_dec<Cfg::kRegsProducer>();
+        decode_produce<Cfg>(P, &tmq, &tmk, &tmv, smem, full, empty, q_full, q_empty, scales,
+                            abort_flag, header, k_begin, k_end, warp, lane, wait);
+    } else {
+        regs_inc<Cfg::kRegsConsumer>();
+        // ------------------------------------------------------- consumers
+        const int cw = warp - 4;
+        const int grp = cw >> 2, ts = cw & 3;
+        const int g = lane >> 2, q4 = lane & 3;
+        const int G = L.G, Hq = L.Hq;
+        const int4* tasks = ws_ptr<int4>(P.ws, L.off_tasks);
+        const int4* units = ws_ptr<int4>(P.ws, L.off_units);
+        const int32_t* cu_q = ws_ptr<int32_t>(P.ws, L.off_cu_q);
+        const float scale_log2 = P.sm_scale * kLog2e;
+        uint8_t* qh = smem + Cfg::kOffQh;
+        float* mbuf = reinterpret_cast<float*>(smem + Cfg::kOffMerge);
+        float* ml = reinterpret_cast<float*>(smem + Cfg::kOffML);
+        int it = 0, task_it = 0;
+        TaskRec mine;
+        for (int k = k_begin; k < k_end; ++k, ++task_it) {
+            if (((k - k_begin) & 31) == 0)
+                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            const int4 tk = rec.tk;
+            const int4 un = rec.un;
+            const int hk = un.y, q0 = un.z, nq = un.w;
+            const int R = G * nq;
+            const int ctx_b = rec.ctx, ql_b = rec.ql;
+            const int tok_base = rec.cuq + q0;
+            const int pbase = ctx_b - ql_b + q0;
+            // this thread's rows are 8nt + 2q4 + e; the last key each may see
+            // (-1 for padding rows)
+            int lastk[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 8 * nt + 2 * q4 + e;
+                    const int pr = pbase + r / G;
+                    lastk[nt][e] = r < R ? (pr < ctx_b - 1 ? pr : ctx_b - 1) : -1;
+                }
+
+            // ---- Q of the unit: bf16 slot -> f16 rows in head_dim order, then
+            // release the slot.  Every consumer warp has left the previous
+            // task's merge when it passes this barrier.
+            {
+                const int qs = task_it & 1;
+                wait(&q_full[qs], (uint32_t)((task_it >> 1) & 1));
+                const uint8_t* qslot = smem + Cfg::kOffQ + qs * Cfg::kQSlotBytes;
+                for (int idx = threadIdx.x - 128; idx < kRows * 16; idx += kCT) {
+                    const int r = idx >> 4, c = idx & 15;
+                    const uint4 v = lds128(qslot + (c >> 3) * Cfg::kQHalfBytes + swz(r, c & 7));
+                    const uint4 h = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                               bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+                    *reinterpret_cast<uint4*>(qh + r * (D * 2) + (qh_chunk(c, r) << 4)) = h;
+                }
+                named_bar_sync(kBarConsumers, kCT);
+                if (lane == 0) mbar_arrive(&q_empty[qs]);
+            }
+
+            float m[NT][2], l[NT][2];
+            float o[8][NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                m[nt][0] = m[nt][1] = -INFINITY;
+                l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb)
+                    o[mb][nt][0] = o[mb][nt][1] = o[mb][nt][2] = o[mb][nt][3] = 0.f;
+            }
+
+            for (int t = tk.y; t < tk.z; ++t, ++it) {
+                if (NG > 1 && (it % NG) != grp) continue;
+                const int s = it % STAGES;
+                wait(&full[s], (uint32_t)((it / STAGES) & 1));
+                const uint8_t* stK = smem + s * Cfg::kStageBytes;
+                const uint8_t* stV = stK + Cfg::kKBytes;
+                const int box = (16 * ts) / P.rows_per_box;
+                const float ksc = scales[(s * 2 + 0) * 4 + box];
+                const float vsc = scales[(s * 2 + 1) * 4 + box];
+                // this slice's K bytes: rows g and g+8, bytes [32q4, 32q4+32)
+                const int kr0 = 16 * ts + g, vr0 = 16 * ts + 2 * q4;
+                uint4 kw[2][2];
+                kw[0][0] = lds128(stK + swz(kr0, 2 * q4));
+                kw[0][1] = lds128(stK + swz(kr0, 2 * q4 + 1));
+                kw[1][0] = lds128(stK + swz(kr0 + 8, 2 * q4));
+                kw[1][1] = lds128(stK + swz(kr0 + 8, 2 * q4 + 1));
+
+                // ---- S^T = K Q^T over head_dim in the permuted order
+                float sacc[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {            // 16-byte chunk of each Q row
+                    uint4 qv[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int r = 8 * nt + g;
+                        qv[nt] = lds128(qh + r * (D * 2) + (qh_chunk(4 * q4 + i, r) << 4));
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {        // k-block kk = 2i + h
+                        const int kk = 2 * i + h;
+                        const uint32_t w0 = word_of(kw[0][kk >> 2], kk & 3);
+                        const uint32_t w1 = word_of(kw[1][kk >> 2], kk & 3);
+                        uint32_t a[4];
+                        a[0] = e4m3x2_to_f16x2((uint16_t)(w0 & 0xffffu));
+                        a[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xffffu));
+                        a[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
+                        a[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_f16_16816(sacc[nt], a, word_of(qv[nt], 2 * h),
+                                          word_of(qv[nt], 2 * h + 1));
+                    }
+                }
+
+                // this slice's V bytes: rows 2q4, 2q4+1, 2q4+8, 2q4+9, bytes
+                // [16g, 16g+16); then the stage goes back to the producer
+                uint4 vw[4];
+                vw[0] = lds128(stV + swz(vr0, g));
+                vw[1] = lds128(stV + swz(vr0 + 1, g));
+                vw[2] = lds128(stV + swz(vr0 + 8, g));
+                vw[3] = lds128(stV + swz(vr0 + 9, g));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);   // the stage's bytes are in registers
+
+                // ---- mask + online softmax (log2 domain, lazily moved max)
+                const int tok = t * kDecodeTile + 16 * ts + g;   // token of sacc[.][0..1]
+                const float cs = scale_log2 * ksc;
+                float sv[NT][4];
+                bool need = false;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        sv[nt][e] = tok <= lastk[nt][e] ? sacc[nt][e] * cs : -INFINITY;
+                        sv[nt][2 + e] = tok + 8 <= lastk[nt][e] ? sacc[nt][2 + e] * cs : -INFINITY;
+                        need |= fmaxf(sv[nt][e], sv[nt][2 + e]) > m[nt][e] + 8.f;
+                    }
+                if (__any_sync(0xffffffffu, need)) {
+                    // row max over the 8 lanes holding the row's tokens
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float mx = fmaxf(sv[nt][e], sv[nt][2 + e]);
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                            if (mx > m[nt][e] + 8.f) {
+                                const float al = ex2(m[nt][e] - mx);   // 0 while m = -inf
+                                m[nt][e] = mx;
+                                l[nt][e] *= al;
+#pragma unroll
+                                for (int mb = 0; mb < 8; ++mb) {
+                                    o[mb][nt][e] *= al;
+                                    o[mb][nt][2 + e] *= al;
+                                }
+                            }
+                        }
+                }
+                // P = 2^(s - m); the PV operand carries v_scale * 2^64 (bf16)
+                const float vs64 = vsc * 0x1p64f;
+                uint32_t pb[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float mu0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0];
+                    const float mu1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
+                    const float p0 = ex2(sv[nt][0] - mu0), p1 = ex2(sv[nt][1] - mu1);
+                    const float p2 = ex2(sv[nt][2] - mu0), p3 = ex2(sv[nt][3] - mu1);
+                    l[nt][0] += p0 + p2;
+                    l[nt][1] += p1 + p3;
+                    // [token][row] 8x8 blocks -> [row][token]: the B fragments
+                    pb[nt][0] = movmatrix_trans(pack_bf16x2(p0 * vs64, p1 * vs64));
+                    pb[nt][1] = movmatrix_trans(pack_bf16x2(p2 * vs64, p3 * vs64));
+                }
+
+                // ---- O^T += V^T P^T; A-fragment rows are head_dim in the order
+                // thread g <-> [16g, 16g+16), block mb <-> pair (16g+2mb, +1)
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) {
+                    const int wi = mb >> 1;
+                    const uint32_t v0 = word_of(vw[0], wi), v1 = word_of(vw[1], wi);
+                    const uint32_t v2 = word_of(vw[2], wi), v3 = word_of(vw[3], wi);
+                    uint32_t a[4];
+                    if (mb & 1) {
+                        a[0] = e4m3_pair_bf16_x2m120<2>(v0, v1);
+                        a[1] = e4m3_pair_bf16_x2m120<3>(v0, v1);
+                        a[2] = e4m3_pair_bf16_x2m120<2>(v2, v3);
+                        a[3] = e4m3_pair_bf16_x2m120<3>(v2, v3);
+                    } else {
+                        a[0] = e4m3_pair_bf16_x2m120<0>(v0, v1);
+                        a[1] = e4m3_pair_bf16_x2m120<1>(v0, v1);
+                        a[2] = e4m3_pair_bf16_x2m120<0>(v2, v3);
+                        a[3] = e4m3_pair_bf16_x2m120<1>(v2, v3);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[mb][nt], a, pb[nt][0], pb[nt][1]);
+                }
+            }
+
+            // ---- merge the 4*NG partial (m, l, O) states of this unit
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float v = l[nt][e];
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    l[nt][e] = v;
+                    if (g == 0) {
+                        const int r = 8 * nt + 2 * q4 + e;
+                        ml[(cw * kRows + r) * 2] = m[nt][e];
+                        ml[(cw * kRows + r) * 2 + 1] = v;
+                    }
+                }
+            named_bar_sync(kBarConsumers, kCT);
+            // weight 2^(m_w - M) of this warp's state, M = the rows' max over warps
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 8 * nt + 2 * q4 + e;
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < kCW; ++w) M = fmaxf(M, ml[(w * kRows + r) * 2]);
+                    const float wgt = m[nt][e] == -INFINITY ? 0.f : ex2(m[nt][e] - M);
+#pragma unroll
+                    for (int mb = 0; mb < 8; ++mb) {
+                        o[mb][nt][e] *= wgt;
+                        o[mb][nt][2 + e] *= wgt;
+                    }
+                }
+            // buffer ts holds the sum over the tile groups of slice ts, as
+            // [row][head_dim] fp32
+            float* sbuf = mbuf + ts * (kRows * Cfg::kMergeStride);
+            auto put = [&](bool add) {
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int r = 8 * nt + 2 * q4 + e;
+                            float2* dst = reinterpret_cast<float2*>(
+                                sbuf + r * Cfg::kMergeStride + 16 * g + 2 * mb);
+                            float2 v = make_float2(o[mb][nt][e], o[mb][nt][2 + e]);
+                            if (add) {
+                                const float2 old = *dst;
+                                v.x += old.x;
+                                v.y += old.y;
+                            }
+                            *dst = v;
+                        }
+            };
+            if (NG == 2) {
+                if (grp == 1) put(false);
+                named_bar_sync(kBarConsumers, kCT);
+                if (grp == 0) put(true);
+            } else {
+                put(false);
+            }
+            named_bar_sync(kBarConsumers, kCT);
+            // one warp per row, 4 head_dim values per lane
+            for (int r = cw; r < R; r += kCW) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kCW; ++w) M = fmaxf(M, ml[(w * kRows + r) * 2]);
+                float Lsum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kCW; ++w) {
+                    const float mw = ml[(w * kRows + r) * 2];
+                    if (mw != -INFINITY) Lsum += ex2(mw - M) * ml[(w * kRows + r) * 2 + 1];
+                }
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int b = 0; b < Cfg::kMergeBufs; ++b) {
+                    const float4 v = *reinterpret_cast<const float4*>(
+                        mbuf + (b * kRows + r) * Cfg::kMergeStride + 4 * lane);
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                // the PV operands carried 2^64 * 2^-120: undo the 2^-56 here
+                const float inv = Lsum > 0.f ? 0x1p56f / Lsum : 0.f;
+                const float lse_nat = Lsum > 0.f ? (M + lg2(Lsum)) * kLn2 : -INFINITY;
+                const int token = tok_base + r / G, head = hk * G + r % G;
+                if (tk.w < 0) {
+                    uint2 v;
+                    v.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                    v.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2*>(P.out + ((int64_t)token * Hq + head) * D + 4 * lane) = v;
+                    if (P.lse != nullptr && lane == 0) P.lse[(int64_t)token * Hq + head] = lse_nat;
+                } else {
+                    const int64_t prow = (int64_t)tk.w * L.rows_cap + r;
+                    *reinterpret_cast<float4*>(P.part_o + prow * D + 4 * lane) =
+                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    if (lane == 0) P.part_lse[prow] = lse_nat;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // the consumers stopped waiting: give copies already issued time to land
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000ull) {
+        }
+    }
+}
+
+// (8-row tiles, ring stages) built
+#define PA_DECODE_FP8_VARIANTS(X) \
+    X(1, 8)                       \
+    X(2, 8)                       \
+    X(3, 8)                       \
+    X(4, 8)
+
+int decode_fp8_row_tiles(int rows) { return (rows + 7) / 8; }
+
+int decode_fp8_smem_bytes(int nt) {
+#define X(n, st) \
+    if (nt == n) return DecodeFp8Cfg<n, st>::kSmemBytes;
+    PA_DECODE_FP8_VARIANTS(X)
+#undef X
+    return -1;
+}
+
+int decode_fp8_threads(int nt) {
+#define X(n, st) \
+    if (nt == n) return DecodeFp8Cfg<n, st>::kThreads;
+    PA_DECODE_FP8_VARIANTS(X)
+#undef X
+    return -1;
+}
+
+const void* decode_fp8_kernel_ptr(int nt) {
+#define X(n, st) \
+    if (nt == n) return (const void*)decode_fp8_kernel<n, st>;
+    PA_DECODE_FP8_VARIANTS(X)
+#undef X
+    return nullptr;
+}
+
+template <int NT, int STAGES>
+static cudaError_t launch_fp8_variant(const DecodeParams& P, const CUtensorMap& tq,
+                                      const CUtensorMap& tk, const CUtensorMap& tv,
+                                      cudaStream_t stream) {
+    using Cfg = DecodeFp8Cfg<NT, STAGES>;
+    auto kern = decode_fp8_kernel<NT, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<P.L.N, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(P, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_fp8(const DecodeParams& P, int nt, const CUtensorMap& tq,
+                              const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+#define X(n, st) \
+    if (nt == n) return launch_fp8_variant<n, st>(P, tq, tk, tv, stream);
+    PA_DECODE_FP8_VARIANTS(X)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

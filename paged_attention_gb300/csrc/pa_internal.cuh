@@ -221,14 +221,60 @@ __device__ __forceinline__ float lg2(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Two E4M3 bytes (low byte first) -> packed bf16x2 (exact: every E4M3 value
-// is representable in bf16).  E4M3 -> f16 is an exact hardware conversion.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+// D = A(16x16 f16, row) * B(16x8 f16, col) + D, fp32 accumulate
+__device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit values spread over the warp in the
+// mma fragment layout (lane l holds row l/4, columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Two E4M3 bytes (low byte first) -> packed f16x2, exact (hardware).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-    __half2 hh = *reinterpret_cast<__half2*>(&h2);
-    float2 f = __half22float2(hh);
-    return pack_bf16x2(f.x, f.y);
+    return h2;
+}
+
+// Packed bf16x2 -> f16x2, rounded to nearest; values beyond the f16 range
+// saturate to +-65504.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// E4M3 byte j of word a (low half) and byte j of word b (high half) -> a
+// packed bf16x2 holding each value times 2^-120, exactly, for every byte.
+// With the byte's sign replicated into the byte above it (prmt sign mode),
+// the 16-bit value is sext(s.eeee.mmm); shifted left by 4 and masked it is
+// s.0000.eeee.mmm.0000, i.e. a bf16 whose exponent field is the E4M3 one.  A
+// bf16 exponent field e encodes 2^(e-127), an E4M3 one 2^(e-7), and the
+// three mantissa bits sit at the top of the bf16 mantissa, so the bf16 is the
+// E4M3 value times 2^-120; E4M3 subnormals (e = 0) land on bf16 subnormals
+// with the same factor, zero stays zero, and the two NaN codes become finite.
+template <int J>
+__device__ __forceinline__ uint32_t e4m3_pair_bf16_x2m120(uint32_t a, uint32_t b) {
+    constexpr uint32_t sel = ((uint32_t)(4 + J) | 8u) << 12 | (uint32_t)(4 + J) << 8 |
+                             ((uint32_t)J | 8u) << 4 | (uint32_t)J;
+    return (prmt(a, b, sel) << 4) & 0x87f087f0u;
 }
 
 }  // namespace pa
