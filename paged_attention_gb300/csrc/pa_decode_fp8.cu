@@ -181,6 +181,13 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
         uint8_t* qh = smem + Cfg::kOffQh;
         float* mbuf = reinterpret_cast<float*>(smem + Cfg::kOffMerge);
         float* ml = reinterpret_cast<float*>(smem + Cfg::kOffML);
+        // scale box of this warp's token slice (a slice never spans two pages)
+        const int box = (16 * ts) / P.rows_per_box;
+        // byte offsets of this thread's four 16-byte Q chunks in n-tile 0
+        // (n-tile nt adds nt * 8 rows; 8 is even, so the swizzle is unchanged)
+        uint32_t qoff[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qoff[i] = g * (D * 2) + (qh_chunk(4 * q4 + i, g) << 4);
         int it = 0, task_it = 0;
         TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
@@ -241,29 +248,46 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                 wait(&full[s], (uint32_t)((it / STAGES) & 1));
                 const uint8_t* stK = smem + s * Cfg::kStageBytes;
                 const uint8_t* stV = stK + Cfg::kKBytes;
-                const int box = (16 * ts) / P.rows_per_box;
                 const float ksc = scales[(s * 2 + 0) * 4 + box];
                 const float vsc = scales[(s * 2 + 1) * 4 + box];
-                // this slice's K bytes: rows g and g+8, bytes [32q4, 32q4+32)
+                // this slice's bytes: K rows g and g+8 (bytes [32q4, 32q4+32)),
+                // V rows 2q4, 2q4+1, 2q4+8, 2q4+9 (bytes [16g, 16g+16)); then
+                // the stage goes back to the producer
                 const int kr0 = 16 * ts + g, vr0 = 16 * ts + 2 * q4;
-                uint4 kw[2][2];
+                uint4 kw[2][2], vw[4];
                 kw[0][0] = lds128(stK + swz(kr0, 2 * q4));
                 kw[0][1] = lds128(stK + swz(kr0, 2 * q4 + 1));
                 kw[1][0] = lds128(stK + swz(kr0 + 8, 2 * q4));
                 kw[1][1] = lds128(stK + swz(kr0 + 8, 2 * q4 + 1));
+                // V bytes: before the score product (their latency hides under
+                // it) unless the 32-row tile needs those registers
+                constexpr bool kEarlyV = NT <= 3;
+                auto load_v = [&]() {
+                    vw[0] = lds128(stV + swz(vr0, g));
+                    vw[1] = lds128(stV + swz(vr0 + 1, g));
+                    vw[2] = lds128(stV + swz(vr0 + 8, g));
+                    vw[3] = lds128(stV + swz(vr0 + 9, g));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);   // the stage's bytes are in registers
+                };
+                if (kEarlyV) load_v();
 
-                // ---- S^T = K Q^T over head_dim in the permuted order
-                float sacc[NT][4];
+                // ---- S^T = K Q^T over head_dim in the permuted order; with
+                // registers to spare, even and odd k-blocks accumulate in
+                // separate chains
+                constexpr int kChains = NT <= 3 ? 2 : 1;
+                float sacc[2][NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+                for (int h = 0; h < kChains; ++h)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        sacc[h][nt][0] = sacc[h][nt][1] = sacc[h][nt][2] = sacc[h][nt][3] = 0.f;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {            // 16-byte chunk of each Q row
                     uint4 qv[NT];
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const int r = 8 * nt + g;
-                        qv[nt] = lds128(qh + r * (D * 2) + (qh_chunk(4 * q4 + i, r) << 4));
+                        qv[nt] = lds128(qh + nt * 8 * (D * 2) + qoff[i]);
                     }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {        // k-block kk = 2i + h
@@ -277,20 +301,12 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                         a[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            mma_f16_16816(sacc[nt], a, word_of(qv[nt], 2 * h),
+                            mma_f16_16816(sacc[h % kChains][nt], a, word_of(qv[nt], 2 * h),
                                           word_of(qv[nt], 2 * h + 1));
                     }
                 }
 
-                // this slice's V bytes: rows 2q4, 2q4+1, 2q4+8, 2q4+9, bytes
-                // [16g, 16g+16); then the stage goes back to the producer
-                uint4 vw[4];
-                vw[0] = lds128(stV + swz(vr0, g));
-                vw[1] = lds128(stV + swz(vr0 + 1, g));
-                vw[2] = lds128(stV + swz(vr0 + 8, g));
-                vw[3] = lds128(stV + swz(vr0 + 9, g));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);   // the stage's bytes are in registers
+                if (!kEarlyV) load_v();
 
                 // ---- mask + online softmax (log2 domain, lazily moved max)
                 const int tok = t * kDecodeTile + 16 * ts + g;   // token of sacc[.][0..1]
@@ -301,8 +317,12 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        sv[nt][e] = tok <= lastk[nt][e] ? sacc[nt][e] * cs : -INFINITY;
-                        sv[nt][2 + e] = tok + 8 <= lastk[nt][e] ? sacc[nt][2 + e] * cs : -INFINITY;
+                        const float s0 = kChains == 2 ? sacc[0][nt][e] + sacc[1][nt][e]
+                                                      : sacc[0][nt][e];
+                        const float s2 = kChains == 2 ? sacc[0][nt][2 + e] + sacc[1][nt][2 + e]
+                                                      : sacc[0][nt][2 + e];
+                        sv[nt][e] = tok <= lastk[nt][e] ? s0 * cs : -INFINITY;
+                        sv[nt][2 + e] = tok + 8 <= lastk[nt][e] ? s2 * cs : -INFINITY;
                         need |= fmaxf(sv[nt][e], sv[nt][2 + e]) > m[nt][e] + 8.f;
                     }
                 if (__any_sync(0xffffffffu, need)) {
