@@ -33,10 +33,14 @@
 //   - P^T leaves the score accumulators in the C-fragment layout; one
 //     movmatrix transpose per 8x8 block makes it the B operand of
 //     O^T = V^T P^T.  The V^T A-fragments pair two tokens' bytes at one
-//     head_dim position (prmt with sign replication), which turns into a bf16
-//     holding the E4M3 value times 2^-120 with a shift and a mask -- exact for
-//     every byte.  P carries v_scale * 2^64 in bf16 (fp32 range: no overflow
-//     for any scale), and the remaining 2^56 is applied with 1/l at the end.
+//     head_dim position (one prmt for two fragment registers), again
+//     converted exactly by cvt.rn.f16x2.e4m3x2.  P is f16 and carries v_scale
+//     times a power of two that brings the warp's first v_scale of the task to
+//     [1, 2); the merge divides it out.  (P <= 2^8 after the lazy max, so
+//     pages whose v_scale is within 2^7 of that first one stay inside the f16
+//     range; the conversion saturates beyond.)  V bytes of tokens past the
+//     context are zeroed: the E4M3 NaN codes would otherwise turn 0 * V into
+//     NaN.
 //   - A warp releases its ring stage as soon as its slice's 128 bytes of K
 //     and V are in registers; no converted copy is written and no barrier is
 //     taken per tile.
@@ -188,6 +192,14 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
         uint32_t qoff[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) qoff[i] = g * (D * 2) + (qh_chunk(4 * q4 + i, g) << 4);
+        // byte offsets inside a stage of this thread's K pieces (token rows g
+        // and g+8 of the slice, bytes [32q4, 32q4+32)) and V pieces (token rows
+        // 2q4, 2q4+1, 2q4+8, 2q4+9, bytes [16g, 16g+16))
+        const int kr0 = 16 * ts + g, vr0 = 16 * ts + 2 * q4;
+        const uint32_t koff[4] = {swz(kr0, 2 * q4), swz(kr0, 2 * q4 + 1), swz(kr0 + 8, 2 * q4),
+                                  swz(kr0 + 8, 2 * q4 + 1)};
+        const uint32_t voff[4] = {swz(vr0, g), swz(vr0 + 1, g), swz(vr0 + 8, g),
+                                  swz(vr0 + 9, g)};
         int it = 0, task_it = 0;
         TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
@@ -233,6 +245,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
 
             float m[NT][2], l[NT][2];
             float o[8][NT][4];
+            float vpow = 0.f;   // set at this warp's first tile of the task
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 m[nt][0] = m[nt][1] = -INFINITY;
@@ -250,25 +263,33 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                 const uint8_t* stV = stK + Cfg::kKBytes;
                 const float ksc = scales[(s * 2 + 0) * 4 + box];
                 const float vsc = scales[(s * 2 + 1) * 4 + box];
-                // this slice's bytes: K rows g and g+8 (bytes [32q4, 32q4+32)),
-                // V rows 2q4, 2q4+1, 2q4+8, 2q4+9 (bytes [16g, 16g+16)); then
-                // the stage goes back to the producer
-                const int kr0 = 16 * ts + g, vr0 = 16 * ts + 2 * q4;
+                // this slice's K and V bytes; then the stage goes back to the
+                // producer
                 uint4 kw[2][2], vw[4];
-                kw[0][0] = lds128(stK + swz(kr0, 2 * q4));
-                kw[0][1] = lds128(stK + swz(kr0, 2 * q4 + 1));
-                kw[1][0] = lds128(stK + swz(kr0 + 8, 2 * q4));
-                kw[1][1] = lds128(stK + swz(kr0 + 8, 2 * q4 + 1));
+                kw[0][0] = lds128(stK + koff[0]);
+                kw[0][1] = lds128(stK + koff[1]);
+                kw[1][0] = lds128(stK + koff[2]);
+                kw[1][1] = lds128(stK + koff[3]);
                 // V bytes: before the score product (their latency hides under
                 // it) unless the 32-row tile needs those registers
                 constexpr bool kEarlyV = NT <= 3;
                 auto load_v = [&]() {
-                    vw[0] = lds128(stV + swz(vr0, g));
-                    vw[1] = lds128(stV + swz(vr0 + 1, g));
-                    vw[2] = lds128(stV + swz(vr0 + 8, g));
-                    vw[3] = lds128(stV + swz(vr0 + 9, g));
+                    vw[0] = lds128(stV + voff[0]);
+                    vw[1] = lds128(stV + voff[1]);
+                    vw[2] = lds128(stV + voff[2]);
+                    vw[3] = lds128(stV + voff[3]);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[s]);   // the stage's bytes are in registers
+                    // tokens past the context (slots after the last one of the
+                    // sequence, or pages not loaded): P is 0 there, but E4M3 NaN
+                    // codes would still poison the product
+                    const int tok_v = t * kDecodeTile + 16 * ts;
+                    if (tok_v + 15 >= ctx_b) {
+                        const int dt[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            if (tok_v + dt[x] >= ctx_b) vw[x] = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 };
                 if (kEarlyV) load_v();
 
@@ -313,6 +334,8 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                 const float cs = scale_log2 * ksc;
                 float sv[NT][4];
                 bool need = false;
+                // every row sees every token of the slice: no mask to apply
+                const bool open = R == kRows && t * kDecodeTile + 16 * ts + 15 <= pbase;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -321,8 +344,8 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                                                       : sacc[0][nt][e];
                         const float s2 = kChains == 2 ? sacc[0][nt][2 + e] + sacc[1][nt][2 + e]
                                                       : sacc[0][nt][2 + e];
-                        sv[nt][e] = tok <= lastk[nt][e] ? s0 * cs : -INFINITY;
-                        sv[nt][2 + e] = tok + 8 <= lastk[nt][e] ? s2 * cs : -INFINITY;
+                        sv[nt][e] = open || tok <= lastk[nt][e] ? s0 * cs : -INFINITY;
+                        sv[nt][2 + e] = open || tok + 8 <= lastk[nt][e] ? s2 * cs : -INFINITY;
                         need |= fmaxf(sv[nt][e], sv[nt][2 + e]) > m[nt][e] + 8.f;
                     }
                 if (__any_sync(0xffffffffu, need)) {
@@ -347,8 +370,16 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                             }
                         }
                 }
-                // P = 2^(s - m); the PV operand carries v_scale * 2^64 (bf16)
-                const float vs64 = vsc * 0x1p64f;
+                // P = 2^(s - m); the PV operand (f16) carries v_scale times the
+                // power of two that brought this warp's first v_scale of the
+                // task to [1, 2) -- P then stays far inside the f16 range for
+                // scales within 2^7 of that one, and saturates beyond
+                if (vpow == 0.f) {
+                    const uint32_t ex = (__float_as_uint(vsc) >> 23) & 0xffu;
+                    vpow = ex == 0u || ex == 255u ? 1.f
+                                                  : __uint_as_float((254u - (ex < 253u ? ex : 253u)) << 23);
+                }
+                const float vsw = vsc * vpow;
                 uint32_t pb[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -359,8 +390,8 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     l[nt][0] += p0 + p2;
                     l[nt][1] += p1 + p3;
                     // [token][row] 8x8 blocks -> [row][token]: the B fragments
-                    pb[nt][0] = movmatrix_trans(pack_bf16x2(p0 * vs64, p1 * vs64));
-                    pb[nt][1] = movmatrix_trans(pack_bf16x2(p2 * vs64, p3 * vs64));
+                    pb[nt][0] = movmatrix_trans(pack_f16x2_sat(p0 * vsw, p1 * vsw));
+                    pb[nt][1] = movmatrix_trans(pack_f16x2_sat(p2 * vsw, p3 * vsw));
                 }
 
                 // ---- O^T += V^T P^T; A-fragment rows are head_dim in the order
@@ -370,20 +401,18 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     const int wi = mb >> 1;
                     const uint32_t v0 = word_of(vw[0], wi), v1 = word_of(vw[1], wi);
                     const uint32_t v2 = word_of(vw[2], wi), v3 = word_of(vw[3], wi);
+                    // {t0.d, t1.d, t0.d+1, t1.d+1} -> the (d, d+1) fragment pair
+                    const uint32_t x01 = (mb & 1) ? interleave_bytes<2>(v0, v1)
+                                                  : interleave_bytes<0>(v0, v1);
+                    const uint32_t x23 = (mb & 1) ? interleave_bytes<2>(v2, v3)
+                                                  : interleave_bytes<0>(v2, v3);
                     uint32_t a[4];
-                    if (mb & 1) {
-                        a[0] = e4m3_pair_bf16_x2m120<2>(v0, v1);
-                        a[1] = e4m3_pair_bf16_x2m120<3>(v0, v1);
-                        a[2] = e4m3_pair_bf16_x2m120<2>(v2, v3);
-                        a[3] = e4m3_pair_bf16_x2m120<3>(v2, v3);
-                    } else {
-                        a[0] = e4m3_pair_bf16_x2m120<0>(v0, v1);
-                        a[1] = e4m3_pair_bf16_x2m120<1>(v0, v1);
-                        a[2] = e4m3_pair_bf16_x2m120<0>(v2, v3);
-                        a[3] = e4m3_pair_bf16_x2m120<1>(v2, v3);
-                    }
+                    a[0] = e4m3x2_to_f16x2((uint16_t)(x01 & 0xffffu));
+                    a[1] = e4m3x2_to_f16x2((uint16_t)(x01 >> 16));
+                    a[2] = e4m3x2_to_f16x2((uint16_t)(x23 & 0xffffu));
+                    a[3] = e4m3x2_to_f16x2((uint16_t)(x23 >> 16));
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[mb][nt], a, pb[nt][0], pb[nt][1]);
+                    for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[mb][nt], a, pb[nt][0], pb[nt][1]);
                 }
             }
 
@@ -413,7 +442,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     float M = -INFINITY;
 #pragma unroll
                     for (int w = 0; w < kCW; ++w) M = fmaxf(M, ml[(w * kRows + r) * 2]);
-                    const float wgt = m[nt][e] == -INFINITY ? 0.f : ex2(m[nt][e] - M);
+                    const float wgt = m[nt][e] == -INFINITY ? 0.f : ex2(m[nt][e] - M) / vpow;
 #pragma unroll
                     for (int mb = 0; mb < 8; ++mb) {
                         o[mb][nt][e] *= wgt;
@@ -471,8 +500,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     acc.z += v.z;
                     acc.w += v.w;
                 }
-                // the PV operands carried 2^64 * 2^-120: undo the 2^-56 here
-                const float inv = Lsum > 0.f ? 0x1p56f / Lsum : 0.f;
+                const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
                 const float lse_nat = Lsum > 0.f ? (M + lg2(Lsum)) * kLn2 : -INFINITY;
                 const int token = tok_base + r / G, head = hk * G + r % G;
                 if (tk.w < 0) {

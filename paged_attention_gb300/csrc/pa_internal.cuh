@@ -261,20 +261,21 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return d;
 }
 
-// E4M3 byte j of word a (low half) and byte j of word b (high half) -> a
-// packed bf16x2 holding each value times 2^-120, exactly, for every byte.
-// With the byte's sign replicated into the byte above it (prmt sign mode),
-// the 16-bit value is sext(s.eeee.mmm); shifted left by 4 and masked it is
-// s.0000.eeee.mmm.0000, i.e. a bf16 whose exponent field is the E4M3 one.  A
-// bf16 exponent field e encodes 2^(e-127), an E4M3 one 2^(e-7), and the
-// three mantissa bits sit at the top of the bf16 mantissa, so the bf16 is the
-// E4M3 value times 2^-120; E4M3 subnormals (e = 0) land on bf16 subnormals
-// with the same factor, zero stays zero, and the two NaN codes become finite.
+// f32 pair -> packed f16x2, rounded to nearest; beyond the f16 range the
+// values saturate to +-65504 instead of becoming infinite.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Bytes J and J+1 of two words, interleaved: {a.J, b.J, a.J+1, b.J+1} from
+// the lowest byte up (two 16-bit pairs, each holding one byte of a and one of b).
 template <int J>
-__device__ __forceinline__ uint32_t e4m3_pair_bf16_x2m120(uint32_t a, uint32_t b) {
-    constexpr uint32_t sel = ((uint32_t)(4 + J) | 8u) << 12 | (uint32_t)(4 + J) << 8 |
-                             ((uint32_t)J | 8u) << 4 | (uint32_t)J;
-    return (prmt(a, b, sel) << 4) & 0x87f087f0u;
+__device__ __forceinline__ uint32_t interleave_bytes(uint32_t a, uint32_t b) {
+    constexpr uint32_t sel = (uint32_t)(5 + J) << 12 | (uint32_t)(J + 1) << 8 |
+                             (uint32_t)(4 + J) << 4 | (uint32_t)J;
+    return prmt(a, b, sel);
 }
 
 }  // namespace pa

@@ -113,3 +113,16 @@ def test_bad_page_is_reported_not_faulted():
     bufs = B.run_decode(wd)
     torch.cuda.synchronize()
     assert B.pa_last_device_error(bufs.assign_ws) & B.PA_DEV_BAD_PAGE
+
+
+def test_decode_fp8_page_scales_spread():
+    """Per-page K/V scales that differ by up to 2^6 between the pages of one
+    sequence (P carries v_scale relative to the first page a warp sees)."""
+    w = W.make_workload("fp8s", [900, 3000, 130], [3, 3, 3], num_q_heads=64, num_kv_heads=8,
+                        head_dim=128, page_size=64, layout=W.HND, kv_dtype=W.FP8_E4M3, seed=41)
+    g = torch.Generator().manual_seed(41)
+    mult_k = torch.pow(2.0, -torch.randint(0, 7, w.k_scale.shape, generator=g).float())
+    mult_v = torch.pow(2.0, -torch.randint(0, 7, w.v_scale.shape, generator=g).float())
+    w.k_scale = (w.k_scale * mult_k).contiguous()
+    w.v_scale = (w.v_scale * mult_v).contiguous()
+    run_and_compare(w, num_ctas=17)
