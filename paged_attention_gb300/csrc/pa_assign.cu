@@ -7,13 +7,15 @@
 // compacted into an ascending active-KV-tile list with a warp ballot,
 // popcount and prefix rank).
 //
-// Three launches on the caller's stream:
+// Prefill mode: three launches on the caller's stream:
 //   1. assign_seq_kernel   (1 CTA)      validate lengths; cu_q and the first
 //                                       unit of every sequence (block scans)
 //   2. assign_units_kernel (warp/unit)  unit -> (b, hk, q0, nq), tile count,
 //                                       active-tile list (ballot + popc)
 //   3. assign_map_kernel   (1 CTA)      cost prefix, CTA ownership in closed
 //                                       form, tasks, split slots, cta_ptr
+// Decode mode: one launch (assign_decode_kernel, 1 CTA) does all three --
+// its units are (b, hk) in order, so nothing needs a search.
 // Closed form used in 3: with C the total cost and N CTAs, CTA c owns
 // [a_c, a_{c+1}), a_c = floor(c*C/N); the owner of cost x (0 <= x < C) is
 // floor(((x+1)*N - 1) / C).
@@ -184,8 +186,9 @@ __device__ __forceinline__ void for_each_owner(int64_t P, int n, int64_t w, int6
     }
 }
 
-__global__ void __launch_bounds__(kScanThreads) assign_map_kernel(WsLayout L, void* ws) {
-    __shared__ int64_t sm[32];
+// Cost prefix, ownership, tasks, split slots, combine fix list and cta_ptr,
+// for the U units already written (one CTA; sm: 32 int64 of shared memory).
+__device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm) {
     int32_t* header = ws_ptr<int32_t>(ws, L.off_header);
     const int4* units = ws_ptr<int4>(ws, L.off_units);
     const int32_t* ntiles = ws_ptr<int32_t>(ws, L.off_ntiles);
@@ -243,14 +246,17 @@ __global__ void __launch_bounds__(kScanThreads) assign_map_kernel(WsLayout L, vo
         if (S != 1 && units[u].w > 0) fix[f_run++] = u;
     }
     __syncthreads();
-    // cta_ptr[c] = number of tasks owned by CTAs < c (task_cta is sorted)
-    for (int c = tid; c <= N; c += blockDim.x) {
-        int lo = 0, hi = (int)T;
-        while (lo < hi) {
-            int mid = (lo + hi) >> 1;
-            if (task_cta[mid] < c) lo = mid + 1; else hi = mid;
-        }
-        cta_ptr[c] = lo;
+    // cta_ptr[c] = number of tasks owned by CTAs < c.  task_cta is sorted, so
+    // task k starts every CTA in (task_cta[k-1], task_cta[k]]; CTAs after the
+    // last task's start at T.
+    for (int k = tid; k < (int)T; k += blockDim.x) {
+        const int c = task_cta[k];
+        const int prev = k > 0 ? task_cta[k - 1] : -1;
+        for (int cc = prev + 1; cc <= c; ++cc) cta_ptr[cc] = k;
+    }
+    {
+        const int last = T > 0 ? task_cta[T - 1] : -1;
+        for (int c = last + 1 + tid; c <= N; c += blockDim.x) cta_ptr[c] = (int)T;
     }
     if (tid == 0) {
         header[H_TASKS] = (int32_t)T;
@@ -259,10 +265,74 @@ __global__ void __launch_bounds__(kScanThreads) assign_map_kernel(WsLayout L, vo
     }
 }
 
+__global__ void __launch_bounds__(kScanThreads) assign_map_kernel(WsLayout L, void* ws) {
+    __shared__ int64_t sm[32];
+    grid_launch_dependents();   // the compute kernel may become resident meanwhile
+    assign_map_body(L, ws, sm);
+}
+
+// Decode mode in one launch: units are (b, hk) in order, Hkv per sequence,
+// so the three passes need no search and fit one CTA.
+__global__ void __launch_bounds__(kScanThreads)
+assign_decode_kernel(WsLayout L, const int32_t* __restrict__ ctx, const int32_t* __restrict__ ql,
+                     void* ws) {
+    __shared__ int64_t sm[32];
+    grid_launch_dependents();   // the compute kernel may become resident meanwhile
+    int32_t* header = ws_ptr<int32_t>(ws, L.off_header);
+    int32_t* cu_q = ws_ptr<int32_t>(ws, L.off_cu_q);
+    int32_t* seq_u0 = ws_ptr<int32_t>(ws, L.off_seq_unit0);
+    int4* units = ws_ptr<int4>(ws, L.off_units);
+    int32_t* ntiles = ws_ptr<int32_t>(ws, L.off_ntiles);
+    const int tid = threadIdx.x;
+    // lengths: validate, cu_q
+    const int chunk = (L.B + kScanThreads - 1) / kScanThreads;
+    const int b0 = min(L.B, tid * chunk), b1 = min(L.B, b0 + chunk);
+    int64_t sq = 0;
+    int bad = 0;
+    for (int b = b0; b < b1; ++b) {
+        int q = ql[b], c = ctx[b];
+        if (q < 0 || c < q || c > L.max_ctx || q > L.max_q_len) bad = 1;
+        sq += max(0, min(q, L.max_q_len));
+    }
+    int64_t tq;
+    int64_t eq = block_exscan(sq, &tq, sm);
+    for (int b = b0; b < b1; ++b) {
+        cu_q[b] = (int32_t)eq;
+        seq_u0[b] = b * L.Hkv;
+        eq += max(0, min(ql[b], L.max_q_len));
+    }
+    const int64_t tu = (int64_t)L.B * L.Hkv;
+    bad = __syncthreads_or(bad) || tq != L.total_q || tu > L.unit_cap;
+    if (tid == 0) {
+        cu_q[L.B] = (int32_t)tq;
+        seq_u0[L.B] = (int32_t)tu;
+        for (int i = 0; i < kHeaderWords; ++i) header[i] = 0;
+        header[H_UNITS] = bad ? 0 : (int32_t)tu;
+        header[H_ERROR] = bad ? PA_DEV_BAD_LENGTHS : PA_DEV_OK;
+        header[H_CTAS] = L.N;
+        header[H_MODE] = L.mode;
+    }
+    // units (b, hk): all q_len[b] queries over all ctx[b] keys
+    const int U = bad ? 0 : (int)tu;
+    for (int u = tid; u < U; u += blockDim.x) {
+        const int b = u / L.Hkv, hk = u - b * L.Hkv;
+        const int nq = ql[b];
+        const int64_t keys = nq > 0 ? ctx[b] : 0;
+        units[u] = make_int4(b, hk, 0, nq);
+        ntiles[u] = (int)ceil_div64(keys, L.kv_tile);
+    }
+    __syncthreads();   // header, units and tiles visible to the whole CTA
+    assign_map_body(L, ws, sm);
+}
+
 }  // namespace
 
 cudaError_t launch_assign(const WsLayout& L, const int32_t* ctx, const int32_t* ql,
                           const uint8_t* mask, void* ws, cudaStream_t stream) {
+    if (L.mode == PA_MODE_DECODE) {
+        assign_decode_kernel<<<1, kScanThreads, 0, stream>>>(L, ctx, ql, ws);
+        return cudaGetLastError();
+    }
     assign_seq_kernel<<<1, kScanThreads, 0, stream>>>(L, ctx, ql, ws);
     const int warps = 8;
     const int grid = (L.unit_cap + warps - 1) / warps;

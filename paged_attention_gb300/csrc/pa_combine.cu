@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(128) combine_kernel(WsLayout L, const void* __
     const int32_t* slot0 = ws_ptr<int32_t>(ws, L.off_slot0);
     const int32_t* fix = ws_ptr<int32_t>(ws, L.off_fix);
     const int32_t* cu_q = ws_ptr<int32_t>(ws, L.off_cu_q);
+    grid_dependency_wait();   // the compute pass's partials are complete
     const int nfix = header[H_FIX];
     const int sub = threadIdx.x / TPR, d = (threadIdx.x % TPR) * 4;
     for (int f = blockIdx.x; f < nfix; f += gridDim.x) {
@@ -81,13 +82,16 @@ cudaError_t launch_combine(const WsLayout& L, const void* ws, const void* partia
     const float* po = reinterpret_cast<const float*>(partial);
     const float* pl = po + L.partial_slots * L.rows_cap * L.D;
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+    cudaError_t e;
     if (L.D == 128)
-        combine_kernel<128><<<grid, 128, 0, stream>>>(L, ws, po, pl, o, lse);
+        e = launch_dependent(combine_kernel<128>, dim3(grid), dim3(128), 0, stream, L, ws, po, pl,
+                             o, lse);
     else if (L.D == 64)
-        combine_kernel<64><<<grid, 128, 0, stream>>>(L, ws, po, pl, o, lse);
+        e = launch_dependent(combine_kernel<64>, dim3(grid), dim3(128), 0, stream, L, ws, po, pl,
+                             o, lse);
     else
         return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pa

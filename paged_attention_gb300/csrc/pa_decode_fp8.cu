@@ -138,6 +138,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t lim = P.wait_limit_ns;
 
+    grid_dependency_wait();   // Assign's task map is complete
     if (header[H_CTAS] != (int)gridDim.x) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(header, PA_DEV_BAD_LENGTHS);
         return;
@@ -518,6 +519,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
             }
         }
     }
+    grid_launch_dependents();   // Combine may become resident meanwhile
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
         // the consumers stopped waiting: give copies already issued time to land
@@ -569,8 +571,9 @@ static cudaError_t launch_fp8_variant(const DecodeParams& P, const CUtensorMap& 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<P.L.N, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(P, tq, tk, tv);
-    return cudaGetLastError();
+    e = launch_dependent(kern, dim3(P.L.N), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, P, tq,
+                         tk, tv);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_decode_fp8(const DecodeParams& P, int nt, const CUtensorMap& tq,

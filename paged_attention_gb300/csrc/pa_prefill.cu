@@ -117,6 +117,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t lim = P.wait_limit_ns;
 
+    grid_dependency_wait();   // Assign's task map is complete
     if (header[H_CTAS] != (int)gridDim.x) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(header, PA_DEV_BAD_LENGTHS);
         return;
@@ -626,10 +627,12 @@ cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (p.head_dim == 128)
-        prefill_kernel<128><<<L.N, PrefillCfg<128>::kThreads, smem, stream>>>(P, tq, tk, tv);
+        e = launch_dependent(prefill_kernel<128>, dim3(L.N), dim3(PrefillCfg<128>::kThreads), smem,
+                             stream, P, tq, tk, tv);
     else
-        prefill_kernel<64><<<L.N, PrefillCfg<64>::kThreads, smem, stream>>>(P, tq, tk, tv);
-    return cudaGetLastError();
+        e = launch_dependent(prefill_kernel<64>, dim3(L.N), dim3(PrefillCfg<64>::kThreads), smem,
+                             stream, P, tq, tk, tv);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pa
