@@ -255,40 +255,79 @@ def run_native(args, rank, world, dist):
     ms = t0.elapsed_time(t1) / args.steps
     kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
 
-    # end-to-end through the public API: per step, inputs copied from pinned
-    # host memory (Q, block table, lengths; the KV cache is resident state),
-    # Assign + compute + Combine, outputs (O, LSE) read back to pinned host
+    # end-to-end through the public API: every step copies its inputs from
+    # pinned host memory (Q, block table, lengths; the KV cache is resident
+    # state), runs Assign + compute + Combine, and reads its outputs (O, LSE)
+    # back to pinned host memory.  As in a serving loop, the copies run on
+    # their own streams with two sets of device buffers, so step k+1's upload
+    # and step k-1's read-back overlap step k's compute.
+    import copy
     hq = w_cpu.q.pin_memory()
     hbt = w_cpu.block_table.pin_memory()
     hctx = w_cpu.context_lens.pin_memory()
     hql = w_cpu.q_lens.pin_memory()
-    hout = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
-    hlse = torch.empty(bufs.lse.shape, dtype=bufs.lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hctx, hql))
-    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+    sets = []
+    for k in range(2):
+        wk = copy.copy(w)
+        if k == 1:
+            wk.q = torch.empty_like(w.q)
+            wk.block_table = torch.empty_like(w.block_table)
+            wk.context_lens = torch.empty_like(w.context_lens)
+            wk.q_lens = torch.empty_like(w.q_lens)
+        bk = bufs if k == 0 else B.make_buffers(w, mode)
+        hout = torch.empty(bk.out.shape, dtype=bk.out.dtype).pin_memory()
+        hlse = torch.empty(bk.lse.shape, dtype=bk.lse.dtype).pin_memory()
+        sets.append((wk, bk, hout, hlse))
+    d2h = sets[0][2].numel() * sets[0][2].element_size() + \
+        sets[0][3].numel() * sets[0][3].element_size()
+    up = torch.cuda.Stream(dev)
+    down = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        w.q.copy_(hq, non_blocking=True)
-        w.block_table.copy_(hbt, non_blocking=True)
-        w.context_lens.copy_(hctx, non_blocking=True)
-        w.q_lens.copy_(hql, non_blocking=True)
-        runner(w, bufs)
-        hout.copy_(bufs.out, non_blocking=True)
-        hlse.copy_(bufs.lse, non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        wk, bk, hout, hlse = sets[k]
+        with torch.cuda.stream(up):
+            up.wait_event(ev_done[k])          # step i-2 no longer reads this set
+            wk.q.copy_(hq, non_blocking=True)
+            wk.block_table.copy_(hbt, non_blocking=True)
+            wk.context_lens.copy_(hctx, non_blocking=True)
+            wk.q_lens.copy_(hql, non_blocking=True)
+            ev_in[k].record(up)
+        stream.wait_event(ev_in[k])
+        stream.wait_event(ev_out[k])           # step i-2's outputs have been read back
+        runner(wk, bk)
+        ev_done[k].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[k])
+            hout.copy_(bk.out, non_blocking=True)
+            hlse.copy_(bk.lse, non_blocking=True)
+            ev_out[k].record(down)
 
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
+    for i in range(max(3, args.warmup)):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_event(ev_out[0])
+    stream.wait_event(ev_out[1])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    for wk, bk, hout, hlse in sets:
+        if B.pa_last_device_error(bk.assign_ws) != 0:
+            raise SystemExit("device error during the end-to-end run")
+    for wk, bk, hout, hlse in sets:
+        if not torch.equal(hout, bufs.out.cpu()):
+            raise SystemExit("end-to-end outputs differ from the device-timed run")
     clk = clocks.stop()
     if dist is not None:
         from paged_attention_gb300.dist import max_over_ranks
@@ -328,7 +367,8 @@ def run_native(args, rank, world, dist):
                        l2="inputs larger than L2" if args.shrink == 1 else f"shrink {args.shrink}",
                        parallelism=f"independent batch per GPU x{world}"),
         "e2e": {"value": round(e2e_val, 2), "unit": unit, "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "overlap": "uploads and read-backs on their own streams, two buffer sets"},
         "roofline": roof,
         "gpu_launches": 5 * args.steps,
         "clocks": clk,
