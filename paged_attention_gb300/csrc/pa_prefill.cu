@@ -18,7 +18,8 @@
 // softmax warpgroups 200 each: 128*88 + 256*200 <= 384*168.
 //   warp 0      TMA producer: the unit's Q halves once per task, then for
 //               every active 128-token KV tile its K and its V, page by page,
-//               each into its own entry of a ring (128-byte swizzle).
+//               each into its own entry of a ring (128-byte swizzle); warp 0
+//               copies the even pages of an entry, warp 3 the odd ones.
 //   warps 1-2   warp 1 allocates the 512 TMEM columns; lane 0 of warp 1+h
 //               issues every MMA of half h:
 //               S_h = Q_h K^T (M=128, N=128, K=D, both operands K-major in
@@ -31,7 +32,7 @@
 //               softmax runs; MMAs of one thread execute in issue order,
 //               which keeps QK_h(j+1) from overwriting P_h(j) before PV_h(j)
 //               has read it.  Warp 1 also zeroes V rows past the context.
-//   warp 3      idle.
+//   warp 3      copies the odd pages of every K/V ring entry (see warp 0).
 //   warps 4-7   softmax for half 0, warps 8-11 for half 1: thread = query row
 //               = TMEM lane.  Reads its S row (tcgen05.ld), applies the
 //               causal / context mask, keeps the running max lazily (O is
@@ -126,7 +127,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         mbar_init(q_full, 1);
         mbar_init(q_empty, 2);                 // one commit from each MMA warp
         for (int e = 0; e < E; ++e) {
-            mbar_init(&kv_full[e], 1);
+            mbar_init(&kv_full[e], 2);            // the two producer warps
             mbar_init(&kv_empty[e], 2);
         }
         for (int h = 0; h < 2; ++h) {
@@ -171,8 +172,14 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
 
     if (warp < 4) {
       regs_dec<Cfg::kRegsProducer>();
-      if (warp == 0) {
-        // ---------------------------------------------------------- producer
+      if (warp == 0 || warp == 3) {
+        // --------------------------------------------------------- producers
+        // A tensor copy holds its issuing thread for hundreds of cycles, so
+        // the boxes of every ring entry are split by page between warp 0 (even
+        // pages) and warp 3 (odd pages).  Each arms the entry's barrier for
+        // its own bytes before its own copies, so neither waits for the
+        // other.  Warp 0 also loads Q.
+        const int pw = warp == 0 ? 0 : 1;
         if (lane == 0) {
             prefetch_tmap(&tmq);
             prefetch_tmap(&tmk);
@@ -191,8 +198,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             const int ctx_b = rec.ctx;
             const int npg = (ctx_b + ps - 1) / ps;
             const int32_t* bt_row = P.block_table + (int64_t)b * P.max_pages_per_seq;
-            wait(q_empty, (uint32_t)(task_it & 1) ^ 1u);
-            if (lane == 0) {
+            if (pw == 0) wait(q_empty, (uint32_t)(task_it & 1) ^ 1u);
+            if (pw == 0 && lane == 0) {
                 if (*abort_flag) {
                     mbar_arrive(q_full);
                 } else {
@@ -227,7 +234,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         page = -1;
                     }
                     pg[j] = page;
-                    if (page >= 0) bytes += box_bytes;
+                    if (page >= 0 && (j & 1) == pw) bytes += box_bytes;
                 }
                 // K first (QK needs it first), then V, each into its own ring entry
 #pragma unroll
@@ -238,11 +245,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         if (*abort_flag) {
                             mbar_arrive(&kv_full[e]);
                         } else {
-                            mbar_arrive_expect_tx(&kv_full[e], bytes);
+                            mbar_arrive_expect_tx(&kv_full[e], bytes);   // this warp's pages
                             uint8_t* dst = smem + Cfg::kOffKV + e * Cfg::kKVBytes;
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
-                                if (pg[j] < 0) continue;
+                                if (pg[j] < 0 || (j & 1) != pw) continue;
                                 const int slot0 = (kt * kPrefillTile + j * rpb) % ps;
 #pragma unroll
                                 for (int c = 0; c < Cfg::kHalves; ++c)
