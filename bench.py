@@ -370,7 +370,8 @@ def run_native(args, rank, world, dist):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "overlap": "uploads and read-backs on their own streams, two buffer sets"},
         "roofline": roof,
-        "gpu_launches": 5 * args.steps,
+        # Assign (1 launch in decode mode, 3 in prefill mode) + compute + Combine
+        "gpu_launches": (3 if mode == B.PA_MODE_DECODE else 5) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
