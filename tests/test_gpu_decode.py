@@ -126,3 +126,15 @@ def test_decode_fp8_page_scales_spread():
     w.k_scale = (w.k_scale * mult_k).contiguous()
     w.v_scale = (w.v_scale * mult_v).contiguous()
     run_and_compare(w, num_ctas=17)
+
+
+@pytest.mark.parametrize("ql,G,layout,ps", [(1, 8, W.HND, 64), (2, 8, W.NHD, 32), (1, 4, W.NHD, 16),
+                                            (3, 4, W.HND, 128)])
+def test_decode_fp8_row_tiles(ql, G, layout, ps):
+    """Every E4M3 row-tile variant (8, 16, 24 and 32 rows per unit hit NT = 1..4
+    across this and the other FP8 tests), both layouts, small and large pages."""
+    hkv = 4
+    w = W.make_workload(f"fp8r{ql}{G}", [37, 700, 1500, 64, 129], [ql] * 5, num_q_heads=G * hkv,
+                        num_kv_heads=hkv, head_dim=128, page_size=ps, layout=layout,
+                        kv_dtype=W.FP8_E4M3, seed=50 + ql * 10 + G)
+    run_and_compare(w, num_ctas=19)
