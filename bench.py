@@ -245,14 +245,20 @@ def run_native(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    # the step as a user runs it: nothing between the launches (events recorded
+    # between kernels would keep the dependent launches from overlapping)
     t0.record(stream)
     for i in range(args.steps):
-        step(kev[i])
+        step()
     t1.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
+    # the compute kernel alone, bracketed by events, for the roofline
+    for i in range(args.steps):
+        step(kev[i])
+    torch.cuda.synchronize()
     kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
 
     # end-to-end through the public API: every step copies its inputs from
@@ -328,6 +334,32 @@ def run_native(args, rank, world, dist):
     for wk, bk, hout, hlse in sets:
         if not torch.equal(hout, bufs.out.cpu()):
             raise SystemExit("end-to-end outputs differ from the device-timed run")
+    # the same device-resident step captured once in a CUDA graph and replayed
+    # (the launch chain without host launch overhead)
+    graph = None
+    try:
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            step()   # warm on the capture stream
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / args.steps
+        graph = {"ms_per_step": round(graph_ms, 4), "value": None}
+    except Exception as exc:   # report, do not fail the bench line
+        graph = {"unavailable": f"{type(exc).__name__}: {str(exc)[:120]}"}
     clk = clocks.stop()
     if dist is not None:
         from paged_attention_gb300.dist import max_over_ranks
@@ -353,6 +385,9 @@ def run_native(args, rank, world, dist):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
                 "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
                 "peak_source": peaks["source"]}
+    if graph is not None and "ms_per_step" in graph:
+        scale = 1e9 if kind == "bytes" else 1e12
+        graph["value"] = round(work * world / (graph["ms_per_step"] * 1e-3) / scale, 2)
     roof["kernel"] = "pa_decode_splitk" if mode == B.PA_MODE_DECODE else "pa_prefill"
     roof["kernel_ms"] = round(kern_ms, 4)
     roof["traffic"] = load_traffic(roof["kernel"], name)
@@ -373,6 +408,7 @@ def run_native(args, rank, world, dist):
         # Assign (1 launch in decode mode, 3 in prefill mode) + compute + Combine
         "gpu_launches": (3 if mode == B.PA_MODE_DECODE else 5) * args.steps,
         "clocks": clk,
+        "graph": graph,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, u, sample, cores, _ = oracle_sample_rate(w_cpu, name, args.cpu_seconds)

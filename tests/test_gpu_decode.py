@@ -138,3 +138,35 @@ def test_decode_fp8_row_tiles(ql, G, layout, ps):
                         num_kv_heads=hkv, head_dim=128, page_size=ps, layout=layout,
                         kv_dtype=W.FP8_E4M3, seed=50 + ql * 10 + G)
     run_and_compare(w, num_ctas=19)
+
+
+def test_decode_step_replays_from_a_cuda_graph():
+    """Assign + split-K + Combine captured once in a CUDA graph and replayed give
+    the eager result bit for bit, also after the inputs change in place."""
+    w = W.decode_bf16(mtp=2, shrink=16).to("cuda")
+    bufs = B.make_buffers(w, B.PA_MODE_DECODE)
+    B.run_decode(w, bufs)
+    torch.cuda.synchronize()
+    eager_o, eager_l = bufs.out.clone(), bufs.lse.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        B.run_decode(w, bufs)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.run_decode(w, bufs)
+    bufs.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(bufs.out, eager_o) and torch.equal(bufs.lse, eager_l)
+    # new query values in place: the replay reads them
+    w.q.mul_(-1.0)
+    B.run_decode(w, bufs)
+    torch.cuda.synchronize()
+    eager2 = bufs.out.clone()
+    bufs.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(bufs.out, eager2)
+    assert B.pa_last_device_error(bufs.assign_ws) == 0
