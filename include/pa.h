@@ -44,6 +44,10 @@
  *     call are then unspecified.  Read the code with pa_last_device_error.
  *   - Tensors are dense and row-major with the shapes given; every base
  *     pointer must be 16-byte aligned.
+ *   - With total_q_tokens == 0 there is no query row: pa_decode_splitk,
+ *     pa_decode_noalloc, pa_prefill and pa_combine return PA_OK without
+ *     launching anything, and their buffers may be NULL (pa_assign still
+ *     writes an empty task map).
  */
 #ifndef PA_H
 #define PA_H

@@ -391,6 +391,7 @@ pa_status pa_decode_splitk(const pa_problem* problem, const void* q, const void*
     pa_status st = make_layout(problem, PA_MODE_DECODE, L);
     if (st != PA_OK) return st;
     const pa_problem& p = *problem;
+    if (p.total_q_tokens == 0) return PA_OK;   // no query row: nothing to compute
     if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !assign_ws ||
         !out || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(out, 16) || !aligned(block_table, 4) || !aligned(assign_ws, 256))
@@ -419,6 +420,7 @@ pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
     WsLayout L;
     pa_status st = make_layout(problem, mode, L);
     if (st != PA_OK) return st;
+    if (problem->total_q_tokens == 0) return PA_OK;   // no query row: nothing to combine
     if (!assign_ws || !out || !aligned(out, 16) || !aligned(assign_ws, 256))
         return PA_ERR_INVALID_ARG;
     if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
@@ -440,6 +442,13 @@ pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void
     pa_status st = make_layout(problem, PA_MODE_DECODE, L);
     if (st != PA_OK) return st;
     const pa_problem& p = *problem;
+    if (p.total_q_tokens == 0) {   // no query row: nothing to compute, no error
+        if (device_error != nullptr && (!aligned(device_error, 4) ||
+                                        cudaMemsetAsync(device_error, 0, 4,
+                                                        (cudaStream_t)stream) != cudaSuccess))
+            return aligned(device_error, 4) ? PA_ERR_CUDA : PA_ERR_INVALID_ARG;
+        return PA_OK;
+    }
     if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !out ||
         !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(q_lens, 4) ||
@@ -489,6 +498,7 @@ pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cac
     pa_status st = make_layout(problem, PA_MODE_PREFILL, L);
     if (st != PA_OK) return st;
     const pa_problem& p = *problem;
+    if (p.total_q_tokens == 0) return PA_OK;   // no query row: nothing to compute
     if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !assign_ws ||
         !out || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(out, 16) || !aligned(block_table, 4) || !aligned(assign_ws, 256))
@@ -496,7 +506,6 @@ pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cac
     if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
     if (partial_ws_bytes < (size_t)L.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
         return PA_ERR_WORKSPACE;
-    if (p.total_q_tokens == 0) return PA_OK;
     CUtensorMap tq, tk, tv;
     if (!encode_q_map(p, q, kPrefillHalfRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
         !encode_kv_map(p, k_cache, &tk) ||

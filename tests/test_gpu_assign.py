@@ -72,3 +72,16 @@ def test_bad_lengths_flagged():
     assert B.pa_last_device_error(bufs.assign_ws) & B.PA_DEV_BAD_LENGTHS
     gpu = B.pa_read_task_map(bufs.problem, B.PA_MODE_DECODE, bufs.assign_ws)
     assert gpu["num_units"] == 0 and gpu["num_tasks"] == 0
+
+
+def test_decode_map_many_short_sequences():
+    """3000 sequences (24000 units, some with no query token, some one token
+    long): the one-launch decode Assign at scale."""
+    g = torch.Generator().manual_seed(77)
+    B_ = 3000
+    ctx = torch.randint(1, 300, (B_,), generator=g).tolist()
+    ql = [min(c, int(q)) for c, q in zip(ctx, torch.randint(0, 3, (B_,), generator=g).tolist())]
+    w = W.make_workload("many", ctx, ql, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        page_size=16, seed=77, mode="decode")
+    check(w, B.PA_MODE_DECODE)
+    check(w, B.PA_MODE_DECODE, num_ctas=7)

@@ -170,3 +170,27 @@ def test_decode_step_replays_from_a_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(bufs.out, eager2)
     assert B.pa_last_device_error(bufs.assign_ws) == 0
+
+
+def test_decode_many_short_sequences():
+    """3000 short sequences, a third of them without a query token."""
+    g = torch.Generator().manual_seed(78)
+    B_ = 3000
+    ctx = torch.randint(1, 300, (B_,), generator=g).tolist()
+    ql = [min(c, int(q)) for c, q in zip(ctx, torch.randint(0, 3, (B_,), generator=g).tolist())]
+    w = W.make_workload("many", ctx, ql, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        page_size=16, seed=78, mode="decode")
+    run_and_compare(w)
+
+
+def test_decode_and_prefill_without_query_tokens():
+    """A batch where no sequence has a new token: nothing to compute, no error."""
+    w = W.make_workload("noq", [5, 300, 64], [0, 0, 0], num_q_heads=8, num_kv_heads=2,
+                        head_dim=128, page_size=64, seed=79, mode="decode")
+    wd = w.to("cuda")
+    bufs = B.run_decode(wd)
+    torch.cuda.synchronize()
+    assert B.pa_last_device_error(bufs.assign_ws) == 0
+    bufs = B.run_prefill(wd)
+    torch.cuda.synchronize()
+    assert B.pa_last_device_error(bufs.assign_ws) == 0
