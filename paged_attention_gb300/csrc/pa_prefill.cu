@@ -241,22 +241,27 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 for (int kv = 0; kv < 2; ++kv, ++e_it) {
                     const int e = e_it % E;
                     wait(&kv_empty[e], (uint32_t)((e_it / E) & 1) ^ 1u);
+                    // lane 0 arms the entry for this warp's bytes; then each lane
+                    // issues one box (page j = pw + 2 (lane / kHalves), column block
+                    // lane % kHalves).  A tensor copy holds its issuing thread for
+                    // hundreds of cycles, so small pages need many issuing lanes.
+                    const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
                     if (lane == 0) {
-                        if (*abort_flag) {
-                            mbar_arrive(&kv_full[e]);
-                        } else {
-                            mbar_arrive_expect_tx(&kv_full[e], bytes);   // this warp's pages
-                            uint8_t* dst = smem + Cfg::kOffKV + e * Cfg::kKVBytes;
+                        if (go) mbar_arrive_expect_tx(&kv_full[e], bytes);   // this warp's pages
+                        else mbar_arrive(&kv_full[e]);
+                    }
+                    __syncwarp();
+                    if (go && lane < 4 * Cfg::kHalves) {
+                        const int j = pw + 2 * (lane / Cfg::kHalves), c = lane % Cfg::kHalves;
+                        int page = -1;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                if (pg[j] < 0 || (j & 1) != pw) continue;
-                                const int slot0 = (kt * kPrefillTile + j * rpb) % ps;
-#pragma unroll
-                                for (int c = 0; c < Cfg::kHalves; ++c)
-                                    tma_load_4d(dst + c * Cfg::kRegion + j * rpb * 128,
-                                                kv ? &tmv : &tmk, &kv_full[e], 64 * c, slot0, hk,
-                                                pg[j]);
-                            }
+                        for (int jj = 0; jj < 8; ++jj)
+                            if (jj == j) page = pg[jj];
+                        if (page >= 0) {
+                            const int slot0 = (kt * kPrefillTile + j * rpb) % ps;
+                            tma_load_4d(smem + Cfg::kOffKV + e * Cfg::kKVBytes + c * Cfg::kRegion +
+                                            j * rpb * 128,
+                                        kv ? &tmv : &tmk, &kv_full[e], 64 * c, slot0, hk, page);
                         }
                     }
                     __syncwarp();
