@@ -96,17 +96,18 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
         // Q rows of the unit into slot task_it & 1
         const int qs = task_it & 1;
         if (pw == 0) wait(&q_empty[qs], (uint32_t)((task_it >> 1) & 1) ^ 1u);
-        if (pw == 0 && lane == 0) {
-            if (*abort_flag) {
-                mbar_arrive(&q_full[qs]);
-            } else {
-                mbar_arrive_expect_tx(&q_full[qs], q_bytes);
-                uint8_t* qdst = smem + Cfg::kOffQ + qs * Cfg::kQSlotBytes;
-#pragma unroll
-                for (int h = 0; h < Cfg::kQHalves; ++h)
-                    tma_load_3d(qdst + h * Cfg::kQHalfBytes, tmq, &q_full[qs], 64 * h, hk * G,
-                                rec.cuq + un.z);
+        if (pw == 0) {
+            // lane 0 arms the slot, then lane h copies column block h (a tensor
+            // copy holds its issuing thread for hundreds of cycles)
+            const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+            if (lane == 0) {
+                if (go) mbar_arrive_expect_tx(&q_full[qs], q_bytes);
+                else mbar_arrive(&q_full[qs]);
             }
+            __syncwarp();
+            if (go && lane < Cfg::kQHalves)
+                tma_load_3d(smem + Cfg::kOffQ + qs * Cfg::kQSlotBytes + lane * Cfg::kQHalfBytes,
+                            tmq, &q_full[qs], 64 * lane, hk * G, rec.cuq + un.z);
         }
         __syncwarp();
         // block-table window: 32 page ids (and, for FP8, their K/V scales)
@@ -156,9 +157,10 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                 pg[j] = page;
                 if (page >= 0) bytes += 2u * box_bytes;
             }
+            uint8_t* stK = smem + s * Cfg::kStageBytes;
+            uint8_t* stV = stK + Cfg::kKBytes;
+            const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
             if (lane == 0) {
-                uint8_t* stK = smem + s * Cfg::kStageBytes;
-                uint8_t* stV = stK + Cfg::kKBytes;
                 if (Cfg::kFP8) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -166,30 +168,32 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                         scales[(s * 2 + 1) * 4 + j] = pg[j] >= 0 ? vsc[j] : 0.f;
                     }
                 }
-                if (*abort_flag) {
-                    mbar_arrive(&full[s]);
-                } else {
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    if (Cfg::kHalves == 2 && P.kv_one_box) {
-                        // pages of >= 64 tokens: one box = both column blocks
-                        const int slot0 = (kt * kDecodeTile) % ps;
-                        if (pg[0] >= 0) {
-                            tma_load_5d(stK, tmk, &full[s], 0, slot0, 0, hk, pg[0]);
-                            tma_load_5d(stV, tmv, &full[s], 0, slot0, 0, hk, pg[0]);
-                        }
-                    } else
+                if (go) mbar_arrive_expect_tx(&full[s], bytes);
+                else mbar_arrive(&full[s]);
+            }
+            __syncwarp();
+            // one box per lane: a tensor copy holds its issuing thread for
+            // hundreds of cycles, the SM takes a new one every ~90
+            if (go) {
+                if (Cfg::kHalves == 2 && P.kv_one_box) {
+                    // pages of >= 64 tokens: one box = both column blocks (lane 0 K, lane 1 V)
+                    const int slot0 = (kt * kDecodeTile) % ps;
+                    if (lane < 2 && pg[0] >= 0)
+                        tma_load_5d(lane ? stV : stK, lane ? tmv : tmk, &full[s], 0, slot0, 0, hk,
+                                    pg[0]);
+                } else if (lane < 8 * Cfg::kHalves) {
+                    // lane = (kv, page j, column block h)
+                    const int kv = lane / (4 * Cfg::kHalves);
+                    const int j = (lane / Cfg::kHalves) % 4, h = lane % Cfg::kHalves;
+                    int page = -1;
 #pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (pg[j] < 0) continue;
-                            const int slot0 = (kt * kDecodeTile + j * rpb) % ps;
-#pragma unroll
-                            for (int h = 0; h < Cfg::kHalves; ++h)
-                                tma_load_4d((kv ? stV : stK) + h * Cfg::kHalfBytes + j * rpb * 128,
-                                            kv ? tmv : tmk, &full[s], h * (128 / Cfg::kElem),
-                                            slot0, hk, pg[j]);
-                        }
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (jj == j) page = pg[jj];
+                    if (page >= 0) {
+                        const int slot0 = (kt * kDecodeTile + j * rpb) % ps;
+                        tma_load_4d((kv ? stV : stK) + h * Cfg::kHalfBytes + j * rpb * 128,
+                                    kv ? tmv : tmk, &full[s], h * (128 / Cfg::kElem), slot0, hk,
+                                    page);
                     }
                 }
             }
