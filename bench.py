@@ -190,6 +190,14 @@ def oracle_sample_rate(w, name, target_s):
 
 # ------------------------------------------------------------------ native
 
+def launches_per_step(w, mode):
+    from paged_attention_gb300 import binding as B
+    if mode == B.PA_MODE_DECODE:
+        return 3
+    G = w.num_q_heads // w.num_kv_heads
+    return 5 + (3 if w.block_mask is None and G <= 16 else 0)
+
+
 def run_native(args, rank, world, dist):
     import torch
     from paged_attention_gb300 import binding as B
@@ -405,8 +413,10 @@ def run_native(args, rank, world, dist):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "overlap": "uploads and read-backs on their own streams, two buffer sets"},
         "roofline": roof,
-        # Assign (1 launch in decode mode, 3 in prefill mode) + compute + Combine
-        "gpu_launches": (3 if mode == B.PA_MODE_DECODE else 5) * args.steps,
+        # decode mode: Assign, compute, Combine.  Prefill mode: Assign (3) +
+        # prefill kernel + Combine, and without a block mask (G <= 16) the
+        # decode part too: its Assign, the decode kernel and its Combine
+        "gpu_launches": launches_per_step(w_cpu, mode) * args.steps,
         "clocks": clk,
         "graph": graph,
     }

@@ -94,6 +94,9 @@ enum { PA_BF16 = 0, PA_FP8_E4M3 = 1 };
  *                    allowed.  Used by pa_prefill for prefill and mixed
  *                    batches. */
 enum { PA_MODE_DECODE = 0, PA_MODE_PREFILL = 1 };
+/* pa_read_task_map only: the decode-mode map that pa_assign(PA_MODE_PREFILL)
+ * builds for the decode-shaped sequences of a batch (see pa_prefill). */
+enum { PA_MAP_DECODE_PART = 2 };
 
 /* Device error codes written by the kernels (read with pa_last_device_error). */
 enum {
@@ -155,6 +158,10 @@ PA_API size_t pa_partial_workspace_size(const pa_problem* problem, int mode);
  * w_u = max(1, ceil(G*rows/balance_rows)); CTA c owns the cost interval
  * [floor(c*C/N), floor((c+1)*C/N)) of the total cost C; a task is a maximal
  * run of one unit's tiles inside one CTA; split units get partial slots.
+ * Prefill mode without a block mask builds two such maps: a decode-mode map
+ * (units (b, hk), 64-token tiles, the decode kernel's CTA count) over the
+ * sequences with 1 <= G*q_lens[b] <= 16, and the prefill-mode map over the
+ * others; each map treats the other part's sequences as having no query.
  */
 PA_API pa_status pa_assign(const pa_problem* problem, int mode, const int32_t* context_lens,
                     const int32_t* q_lens, const uint8_t* block_mask, void* assign_ws,
@@ -253,7 +260,11 @@ PA_API pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, con
  * pa_assign(PA_MODE_PREFILL) with 256-row GQA-packed q tiles and 128-token KV
  * tiles on the tcgen05 tensor cores (accumulators in tensor memory).
  * Arguments as pa_decode_splitk, plus block_mask (the one given to pa_assign,
- * or NULL).  Decode rows (q_len 1) of a mixed batch are ordinary units.
+ * or NULL).  In a batch without a block mask, the sequences with
+ * 1 <= G*q_lens[b] <= 16 (the decode steps of a mixed chunked-prefill + decode
+ * batch) run first, on the decode kernel of pa_decode_splitk over their own
+ * task map: such a unit would fill a few of the 128 rows of a tensor-core
+ * tile.  With a block mask every sequence takes the prefill path.
  */
 PA_API pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cache,
                      const void* v_cache, const int32_t* block_table,
@@ -270,7 +281,9 @@ PA_API pa_status pa_prefill(const pa_problem* problem, const void* q, const void
  * {b, hk, q0, nq}, unit_ntiles [units], unit_nsplit [units], unit_slot0
  * [units], active [units][max_kv_tiles] (only with a block mask; tile lists),
  * where max_kv_tiles = ceil(max_context_len / kv_tile), kv_tile 64 (decode) or
- * 128 (prefill).
+ * 128 (prefill).  mode PA_MAP_DECODE_PART reads the decode part of a
+ * pa_assign(PA_MODE_PREFILL) workspace (kv_tile 64; all counts 0 when the
+ * batch has a block mask or G > 16).
  */
 PA_API pa_status pa_read_task_map(const pa_problem* problem, int mode, const void* assign_ws,
                            size_t assign_ws_bytes, int32_t* counts, int32_t* cta_ptr,

@@ -240,3 +240,34 @@ def assign(mode, num_seqs, num_q_heads, num_kv_heads, num_ctas, kv_tile, balance
                    units=units[:U], unit_ntiles=ntiles[:U], active=active[:U],
                    cta_ptr=cta_ptr, tasks=tasks[:n_tasks], unit_nsplit=nsplit[:U],
                    unit_slot0=slot0[:U], max_kv_tiles=max_kv_tiles)
+
+
+# A prefill-mode batch without a block mask sends every sequence with
+# 1 <= G * q_len <= MIXED_DECODE_ROWS to a decode-mode map (the decode steps of a
+# mixed chunked-prefill + decode batch) and the others to the prefill-mode map.
+MIXED_DECODE_ROWS = 16
+
+
+def assign_prefill(num_seqs, num_q_heads, num_kv_heads, num_ctas, balance_rows,
+                   context_lens, q_lens, block_mask=None, decode_ctas=None):
+    """Prefill-mode Assign as pa_assign(PA_MODE_PREFILL) defines it.
+
+    Returns (prefill_map, decode_map).  Each map is the plain Assign over the
+    whole batch with the other part's q_lens taken as 0: such a sequence has no
+    prefill units, and its decode units hold no query and no tile.  decode_map
+    is None when the batch has a block mask or G > MIXED_DECODE_ROWS (every
+    sequence then stays in the prefill map).  decode_ctas: the decode map's CTA
+    count (default num_ctas)."""
+    G = num_q_heads // num_kv_heads
+    ql = [int(x) for x in q_lens]
+    if block_mask is not None or G > MIXED_DECODE_ROWS:
+        return assign(1, num_seqs, num_q_heads, num_kv_heads, num_ctas, 128, balance_rows,
+                      context_lens, ql, block_mask), None
+    small_q = MIXED_DECODE_ROWS // G
+    ql_pre = [q if q > small_q else 0 for q in ql]
+    ql_dec = [q if q <= small_q else 0 for q in ql]
+    pre = assign(1, num_seqs, num_q_heads, num_kv_heads, num_ctas, 128, balance_rows,
+                 context_lens, ql_pre)
+    dec = assign(0, num_seqs, num_q_heads, num_kv_heads, decode_ctas or num_ctas, 64,
+                 balance_rows, context_lens, ql_dec)
+    return pre, dec

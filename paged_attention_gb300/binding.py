@@ -27,6 +27,7 @@ PA_ERR_WORKSPACE = 3
 PA_NHD, PA_HND = 0, 1
 PA_BF16, PA_FP8_E4M3 = 0, 1
 PA_MODE_DECODE, PA_MODE_PREFILL = 0, 1
+PA_MAP_DECODE_PART = 2   # pa_read_task_map: decode part of a prefill-mode workspace
 PA_DEV_OK, PA_DEV_BAD_LENGTHS, PA_DEV_BAD_PAGE, PA_DEV_WAIT_TIMEOUT = 0, 1, 2, 4
 
 EXPORTED = (
@@ -227,7 +228,7 @@ def pa_read_task_map(problem, mode, assign_ws, stream=None) -> dict:
                                 c(counts), None, None, None, None, None, None, None,
                                 _stream(stream)), "pa_read_task_map")
     U, T, S, N = (int(x) for x in counts)
-    kv_tile = 64 if mode == PA_MODE_DECODE else 128
+    kv_tile = 64 if mode in (PA_MODE_DECODE, PA_MAP_DECODE_PART) else 128
     max_kv_tiles = max(1, -(-max(1, problem.max_context_len) // kv_tile))
     out = dict(num_units=U, num_tasks=T, num_slots=S, num_ctas=N,
                cta_ptr=np.zeros(N + 1, np.int32), tasks=np.zeros((T, 4), np.int32),

@@ -231,6 +231,68 @@ pa_status make_layout(const pa_problem* p, int mode, WsLayout& L) {
     return PA_OK;
 }
 
+// Prefill mode.  A batch without a block mask is split in two: the sequences
+// with 1 <= G * q_len <= kMixedDecodeRows (decode steps of a mixed batch) get
+// a decode-mode task map that the decode kernel runs (64-token tiles, one
+// unit per (sequence, KV head), balanced over its own persistent CTAs); the
+// others get the prefill map.  A decode unit fills a few of the 128 rows of a
+// tensor-core tile, so the prefill kernel would stream its K/V at a fraction
+// of the decode kernel's rate.  Both maps live in one workspace: the prefill
+// map first (its header, at offset 0, also takes the decode kernel's device
+// faults), the decode map from the next 256-byte boundary; the partials
+// likewise.
+struct PrefillLayout {
+    WsLayout L;          // the prefill map
+    WsLayout Ld;         // the decode map (split only)
+    pa_problem pd;       // the problem as the decode kernel sees it
+    bool split;
+    int64_t part_off;    // Ld's partials inside the partial workspace
+    int64_t total_bytes, partial_bytes;
+};
+
+pa_status make_prefill_layout(const pa_problem* p, PrefillLayout& M) {
+    pa_status st = make_layout(p, PA_MODE_PREFILL, M.L);
+    if (st != PA_OK) return st;
+    M.split = false;
+    M.part_off = 0;
+    M.total_bytes = M.L.total_bytes;
+    M.partial_bytes = M.L.partial_bytes;
+    const int G = p->num_q_heads / p->num_kv_heads;
+    if (p->mask_q_tiles > 0 || G > kMixedDecodeRows) return PA_OK;
+    const int small_q = kMixedDecodeRows / G;
+    M.pd = *p;
+    if (M.pd.max_q_len > small_q) M.pd.max_q_len = small_q;
+    if (check_problem(&M.pd, PA_MODE_DECODE) != PA_OK) return PA_OK;
+    const int Nd = resolve_ctas(M.pd, PA_MODE_DECODE);
+    if (Nd <= 0) return PA_ERR_CUDA;
+    WsLayout& Ld = M.Ld;
+    if (!layout_for(M.pd, PA_MODE_DECODE, Nd, rows_cap_for(M.pd, PA_MODE_DECODE), Ld))
+        return PA_ERR_INVALID_ARG;
+    const int64_t base = align256(M.L.total_bytes);
+    for (int64_t* o : {&Ld.off_header, &Ld.off_cta_ptr, &Ld.off_tasks, &Ld.off_task_cta,
+                       &Ld.off_units, &Ld.off_ntiles, &Ld.off_prefix, &Ld.off_nsplit,
+                       &Ld.off_slot0, &Ld.off_task0, &Ld.off_fix, &Ld.off_active, &Ld.off_cu_q,
+                       &Ld.off_seq_unit0})
+        *o += base;
+    Ld.off_err_header = M.L.off_header;
+    Ld.max_q_len = p->max_q_len;   // both Assigns check the caller's lengths
+    Ld.cls = 1;
+    Ld.small_q = small_q;
+    M.L.cls = 2;
+    M.L.small_q = small_q;
+    M.split = true;
+    M.total_bytes = base + Ld.total_bytes;
+    M.part_off = align256(M.L.partial_bytes);
+    M.partial_bytes = M.part_off + Ld.partial_bytes;
+    return PA_OK;
+}
+
+int combine_grid(const WsLayout& L) {
+    int grid = 2 * sm_count();
+    if (grid > L.unit_cap) grid = L.unit_cap;
+    return grid < 1 ? 1 : grid;
+}
+
 }  // namespace
 
 bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L) {
@@ -286,6 +348,7 @@ bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L)
     L.off_active = take(L.has_mask ? (int64_t)L.unit_cap * L.max_kv_tiles * 4 : 4);
     L.off_cu_q = take((int64_t)(p.num_seqs + 1) * 4);
     L.off_seq_unit0 = take((int64_t)(p.num_seqs + 1) * 4);
+    L.off_err_header = L.off_header;
     L.total_bytes = off;
     L.partial_slots = L.task_cap;
     L.partial_bytes = L.partial_slots * (int64_t)L.rows_cap * (L.D + 1) * 4;
@@ -354,12 +417,20 @@ pa_status pa_num_ctas(const pa_problem* problem, int mode, int32_t* num_ctas) {
 }
 
 size_t pa_assign_workspace_size(const pa_problem* problem, int mode) {
+    if (mode == PA_MODE_PREFILL) {
+        PrefillLayout M;
+        return make_prefill_layout(problem, M) == PA_OK ? (size_t)M.total_bytes : 0;
+    }
     WsLayout L;
     if (make_layout(problem, mode, L) != PA_OK) return 0;
     return (size_t)L.total_bytes;
 }
 
 size_t pa_partial_workspace_size(const pa_problem* problem, int mode) {
+    if (mode == PA_MODE_PREFILL) {
+        PrefillLayout M;
+        return make_prefill_layout(problem, M) == PA_OK ? (size_t)M.partial_bytes : 0;
+    }
     WsLayout L;
     if (make_layout(problem, mode, L) != PA_OK) return 0;
     return (size_t)L.partial_bytes;
@@ -368,16 +439,24 @@ size_t pa_partial_workspace_size(const pa_problem* problem, int mode) {
 pa_status pa_assign(const pa_problem* problem, int mode, const int32_t* context_lens,
                     const int32_t* q_lens, const uint8_t* block_mask, void* assign_ws,
                     size_t assign_ws_bytes, void* stream) {
-    WsLayout L;
-    pa_status st = make_layout(problem, mode, L);
+    PrefillLayout M;
+    pa_status st = mode == PA_MODE_PREFILL ? make_prefill_layout(problem, M)
+                                           : make_layout(problem, mode, M.L);
     if (st != PA_OK) return st;
+    if (mode != PA_MODE_PREFILL) {
+        M.split = false;
+        M.total_bytes = M.L.total_bytes;
+    }
+    const WsLayout& L = M.L;
     if (!context_lens || !q_lens || !assign_ws || !aligned(assign_ws, 256) ||
         !aligned(context_lens, 4) || !aligned(q_lens, 4))
         return PA_ERR_INVALID_ARG;
     if (L.has_mask && !block_mask) return PA_ERR_INVALID_ARG;
-    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
+    if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
     cudaError_t e = launch_assign(L, context_lens, q_lens, L.has_mask ? block_mask : nullptr,
                                   assign_ws, (cudaStream_t)stream);
+    if (e == cudaSuccess && M.split)
+        e = launch_assign(M.Ld, context_lens, q_lens, nullptr, assign_ws, (cudaStream_t)stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -417,19 +496,26 @@ pa_status pa_decode_splitk(const pa_problem* problem, const void* q, const void*
 pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
                      size_t assign_ws_bytes, const void* partial_ws, size_t partial_ws_bytes,
                      void* out, float* lse, void* stream) {
-    WsLayout L;
-    pa_status st = make_layout(problem, mode, L);
+    PrefillLayout M;
+    pa_status st = mode == PA_MODE_PREFILL ? make_prefill_layout(problem, M)
+                                           : make_layout(problem, mode, M.L);
     if (st != PA_OK) return st;
+    if (mode != PA_MODE_PREFILL) {
+        M.split = false;
+        M.total_bytes = M.L.total_bytes;
+        M.partial_bytes = M.L.partial_bytes;
+    }
     if (problem->total_q_tokens == 0) return PA_OK;   // no query row: nothing to combine
     if (!assign_ws || !out || !aligned(out, 16) || !aligned(assign_ws, 256))
         return PA_ERR_INVALID_ARG;
-    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
-    if (partial_ws_bytes < (size_t)L.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
+    if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
+    if (partial_ws_bytes < (size_t)M.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
         return PA_ERR_WORKSPACE;
-    int grid = 2 * sm_count();
-    if (grid > L.unit_cap) grid = L.unit_cap;
-    if (grid < 1) grid = 1;
-    cudaError_t e = launch_combine(L, assign_ws, partial_ws, out, lse, grid, (cudaStream_t)stream);
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_combine(M.L, assign_ws, partial_ws, out, lse, combine_grid(M.L), s);
+    if (e == cudaSuccess && M.split)
+        e = launch_combine(M.Ld, assign_ws, static_cast<const char*>(partial_ws) + M.part_off,
+                           out, lse, combine_grid(M.Ld), s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -475,12 +561,7 @@ pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void
         e = launch_decode_from_api(p, L, tq, tk, tv, one_box, block_table,
                                    context_lens, q_lens, k_scale, v_scale, ws, partial, out, lse,
                                    s);
-    if (e == cudaSuccess) {
-        int grid = 2 * sm_count();
-        if (grid > L.unit_cap) grid = L.unit_cap;
-        if (grid < 1) grid = 1;
-        e = launch_combine(L, ws, partial, out, lse, grid, s);
-    }
+    if (e == cudaSuccess) e = launch_combine(L, ws, partial, out, lse, combine_grid(L), s);
     if (e == cudaSuccess && device_error)
         e = cudaMemcpyAsync(device_error, scratch + L.off_header + H_ERROR * 4, 4,
                             cudaMemcpyDeviceToDevice, s);
@@ -494,26 +575,43 @@ pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cac
                      size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
                      void* out, float* lse, void* stream) {
     (void)block_mask;  // the active-tile lists in assign_ws already encode the mask
-    WsLayout L;
-    pa_status st = make_layout(problem, PA_MODE_PREFILL, L);
+    PrefillLayout M;
+    pa_status st = make_prefill_layout(problem, M);
     if (st != PA_OK) return st;
+    const WsLayout& L = M.L;
     const pa_problem& p = *problem;
     if (p.total_q_tokens == 0) return PA_OK;   // no query row: nothing to compute
     if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !assign_ws ||
         !out || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(out, 16) || !aligned(block_table, 4) || !aligned(assign_ws, 256))
         return PA_ERR_INVALID_ARG;
-    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
-    if (partial_ws_bytes < (size_t)L.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
+    if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
+    if (partial_ws_bytes < (size_t)M.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
         return PA_ERR_WORKSPACE;
     CUtensorMap tq, tk, tv;
     if (!encode_q_map(p, q, kPrefillHalfRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
         !encode_kv_map(p, k_cache, &tk) ||
         !encode_kv_map(p, v_cache, &tv))
         return PA_ERR_INVALID_ARG;
-    cudaError_t e = launch_prefill_from_api(p, L, q, tq, tk, tv, block_table, context_lens,
-                                            q_lens, k_scale, v_scale, const_cast<void*>(assign_ws),
-                                            partial_ws, out, lse, (cudaStream_t)stream);
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (M.split) {
+        // the decode-shaped sequences first, on the decode kernel; its 4-D
+        // K/V maps are the prefill kernel's
+        CUtensorMap tqd, tkd, tvd;
+        if (!encode_q_map(M.pd, q, M.pd.max_q_len > 0 ? M.pd.max_q_len : 1, &tqd))
+            return PA_ERR_INVALID_ARG;
+        const bool one_box = encode_kv_map_one_box(M.pd, k_cache, &tkd) &&
+                             encode_kv_map_one_box(M.pd, v_cache, &tvd);
+        e = launch_decode_from_api(M.pd, M.Ld, tqd, one_box ? tkd : tk, one_box ? tvd : tv,
+                                   one_box, block_table, context_lens, q_lens, k_scale, v_scale,
+                                   const_cast<void*>(assign_ws),
+                                   static_cast<char*>(partial_ws) + M.part_off, out, lse, s);
+    }
+    if (e == cudaSuccess)
+        e = launch_prefill_from_api(p, L, q, tq, tk, tv, block_table, context_lens, q_lens,
+                                    k_scale, v_scale, const_cast<void*>(assign_ws), partial_ws,
+                                    out, lse, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -522,11 +620,20 @@ pa_status pa_read_task_map(const pa_problem* problem, int mode, const void* assi
                            int32_t* tasks, int32_t* units, int32_t* unit_ntiles,
                            int32_t* unit_nsplit, int32_t* unit_slot0, int32_t* active,
                            void* stream) {
-    WsLayout L;
-    pa_status st = make_layout(problem, mode, L);
+    if (mode != PA_MODE_DECODE && mode != PA_MODE_PREFILL && mode != PA_MAP_DECODE_PART)
+        return PA_ERR_INVALID_ARG;
+    PrefillLayout M;
+    pa_status st = mode == PA_MODE_DECODE ? make_layout(problem, mode, M.L)
+                                          : make_prefill_layout(problem, M);
     if (st != PA_OK) return st;
+    if (mode == PA_MODE_DECODE) M.total_bytes = M.L.total_bytes;
     if (!assign_ws || !counts) return PA_ERR_INVALID_ARG;
-    if (assign_ws_bytes < (size_t)L.total_bytes) return PA_ERR_WORKSPACE;
+    if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
+    if (mode == PA_MAP_DECODE_PART && !M.split) {   // a masked batch has no decode part
+        for (int i = 0; i < 4; ++i) counts[i] = 0;
+        return PA_OK;
+    }
+    const WsLayout& L = mode == PA_MAP_DECODE_PART ? M.Ld : M.L;
     cudaStream_t s = (cudaStream_t)stream;
     int32_t hdr[kHeaderWords];
     const char* ws = reinterpret_cast<const char*>(assign_ws);

@@ -57,6 +57,13 @@ __device__ int64_t block_exscan(int64_t v, int64_t* total, int64_t* sm) {
 
 __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// query tokens of a sequence that this map covers (see WsLayout::cls)
+__device__ __forceinline__ int class_ql(const WsLayout& L, int q) {
+    if (L.cls == 1) return q <= L.small_q ? q : 0;
+    if (L.cls == 2) return q > L.small_q ? q : 0;
+    return q;
+}
+
 __device__ __forceinline__ int units_of_seq(const WsLayout& L, int ql) {
     if (L.mode == PA_MODE_DECODE) return L.Hkv;
     return L.Hkv * (int)ceil_div64(ql, L.qtok);
@@ -79,7 +86,7 @@ assign_seq_kernel(WsLayout L, const int32_t* __restrict__ ctx, const int32_t* __
         if (q < 0 || c < q || c > L.max_ctx || q > L.max_q_len) bad = 1;
         q = max(0, min(q, L.max_q_len));
         sq += q;
-        su += units_of_seq(L, q);
+        su += units_of_seq(L, class_ql(L, q));
     }
     int64_t tq, tu;
     int64_t eq = block_exscan(sq, &tq, sm);
@@ -89,7 +96,7 @@ assign_seq_kernel(WsLayout L, const int32_t* __restrict__ ctx, const int32_t* __
         cu_q[b] = (int32_t)eq;
         seq_u0[b] = (int32_t)eu;
         eq += q;
-        eu += units_of_seq(L, q);
+        eu += units_of_seq(L, class_ql(L, q));
     }
     bad = __syncthreads_or(bad);
     if (tid == 0) {
@@ -123,7 +130,7 @@ __global__ void assign_units_kernel(WsLayout L, const int32_t* __restrict__ ctx,
         if (seq_u0[mid] <= u) lo = mid; else hi = mid;
     }
     const int b = lo;
-    const int q_b = ql[b], c_b = ctx[b];
+    const int q_b = class_ql(L, max(0, min(ql[b], L.max_q_len))), c_b = ctx[b];
     const int nqt = L.mode == PA_MODE_DECODE ? 1 : (int)ceil_div64(q_b, L.qtok);
     const int local = u - seq_u0[b];
     const int hk = local / nqt, qt = local % nqt;
@@ -316,7 +323,7 @@ assign_decode_kernel(WsLayout L, const int32_t* __restrict__ ctx, const int32_t*
     const int U = bad ? 0 : (int)tu;
     for (int u = tid; u < U; u += blockDim.x) {
         const int b = u / L.Hkv, hk = u - b * L.Hkv;
-        const int nq = ql[b];
+        const int nq = class_ql(L, ql[b]);
         const int64_t keys = nq > 0 ? ctx[b] : 0;
         units[u] = make_int4(b, hk, 0, nq);
         ntiles[u] = (int)ceil_div64(keys, L.kv_tile);

@@ -88,12 +88,13 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
+    int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);   // device faults
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t lim = P.wait_limit_ns;
 
     grid_dependency_wait();   // Assign's task map is complete
     if (header[H_CTAS] != (int)gridDim.x) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(header, PA_DEV_BAD_LENGTHS);
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(err_hdr, PA_DEV_BAD_LENGTHS);
         return;
     }
     if (threadIdx.x == 0) {
@@ -114,7 +115,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         if (*abort_flag) return;
         if (!mbar_wait(bar, parity, lim)) {
             *abort_flag = 1;
-            set_device_error(header, PA_DEV_WAIT_TIMEOUT);
+            set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
         }
     };
 
@@ -127,7 +128,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
 
     if (warp < Cfg::kProducerWarps) {
         decode_produce<Cfg>(P, &tmq, &tmk, &tmv, smem, full, empty, q_full, q_empty, nullptr,
-                            abort_flag, header, k_begin, k_end, warp, lane, wait);
+                            abort_flag, err_hdr, k_begin, k_end, warp, lane, wait);
     } else {
         // ------------------------------------------------------- consumers
         const int cw = warp - Cfg::kProducerWarps;

@@ -64,7 +64,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                                                uint8_t* smem, uint64_t* full, uint64_t* empty,
                                                uint64_t* q_full, uint64_t* q_empty,
                                                float* scales, volatile int* abort_flag,
-                                               int32_t* header, int k_begin, int k_end,
+                                               int32_t* err_hdr, int k_begin, int k_end,
                                                int pw, int lane, Wait& wait) {
     static_assert(Cfg::kStages % Cfg::kProducerWarps == 0,
                   "every ring stage must stay with one producer warp");
@@ -151,7 +151,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                     vsc[j] = __shfl_sync(0xffffffffu, win_vs, lp - win_lo);
                 }
                 if (page < 0 || page >= P.num_pages) {
-                    if (lane == 0) set_device_error(header, PA_DEV_BAD_PAGE);
+                    if (lane == 0) set_device_error(err_hdr, PA_DEV_BAD_PAGE);
                     page = -1;
                 }
                 pg[j] = page;

@@ -135,12 +135,13 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     float* scales = reinterpret_cast<float*>(smem + Cfg::kOffScale);   // [stage][k|v][box]
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
+    int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);   // device faults
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t lim = P.wait_limit_ns;
 
     grid_dependency_wait();   // Assign's task map is complete
     if (header[H_CTAS] != (int)gridDim.x) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(header, PA_DEV_BAD_LENGTHS);
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(err_hdr, PA_DEV_BAD_LENGTHS);
         return;
     }
     if (threadIdx.x == 0) {
@@ -161,7 +162,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
         if (*abort_flag) return;
         if (!mbar_wait(bar, parity, lim)) {
             *abort_flag = 1;
-            set_device_error(header, PA_DEV_WAIT_TIMEOUT);
+            set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
         }
     };
 
@@ -171,7 +172,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     if (warp < 4) {
         regs_dec<Cfg::kRegsProducer>();
         decode_produce<Cfg>(P, &tmq, &tmk, &tmv, smem, full, empty, q_full, q_empty, scales,
-                            abort_flag, header, k_begin, k_end, warp, lane, wait);
+                            abort_flag, err_hdr, k_begin, k_end, warp, lane, wait);
     } else {
         regs_inc<Cfg::kRegsConsumer>();
         // ------------------------------------------------------- consumers

@@ -25,6 +25,10 @@ constexpr int kPrefillHalfRows = 128;  // rows of one tcgen05 M=128 tile
 constexpr int kPrefillRows = 256;    // rows (query token x head) per prefill unit (2 halves)
 constexpr int kMaskTile = 128;       // block-mask tile edge
 constexpr int kDefaultBalanceRows = 128;
+// A prefill-mode batch without a block mask sends every sequence with
+// 1 <= G * q_len <= kMixedDecodeRows (decode steps, short speculative runs)
+// to the decode kernel, through a second, decode-mode task map.
+constexpr int kMixedDecodeRows = 16;
 constexpr int kHeaderWords = 64;
 
 // header word indices inside the Assign workspace
@@ -56,6 +60,12 @@ struct WsLayout {
     int32_t total_q;
     int32_t max_q_len, max_ctx;
     int32_t mask_q_tiles, mask_kv_tiles;
+    // which sequences this map covers: 0 all; 1 those with 1 <= q_len <=
+    // small_q (the decode map of a mixed batch); 2 those with q_len > small_q
+    // (its prefill map).  The other sequences get no units, or (decode mode)
+    // units without query rows.
+    int32_t cls, small_q;
+    int64_t off_err_header;   // header whose error word device faults go to
     int64_t off_header, off_cta_ptr, off_tasks, off_task_cta, off_units, off_ntiles,
         off_prefix, off_nsplit, off_slot0, off_task0, off_fix, off_active, off_cu_q,
         off_seq_unit0;

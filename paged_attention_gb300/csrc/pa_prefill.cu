@@ -11,6 +11,10 @@
 // Deep Dive": Q blocks pack the G q heads of one KV head into one MMA tile;
 // the persistent grid is fixed at the SM count.
 //
+// In a batch without a block mask the sequences of at most 16 rows (G x
+// q_len: the decode steps of a mixed batch) never reach this kernel: they
+// run on the decode kernel over a task map of their own (pa_api.cu).
+//
 // GB300 design (one CTA per SM, 384 threads = 3 warpgroups).  A unit is up
 // to 256 query rows (G heads x 256/G tokens), computed as two 128-row halves
 // that share every K/V tile.  Registers: of the 168 per thread the block is
@@ -115,12 +119,13 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
+    int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);   // device faults
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t lim = P.wait_limit_ns;
 
     grid_dependency_wait();   // Assign's task map is complete
     if (header[H_CTAS] != (int)gridDim.x) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(header, PA_DEV_BAD_LENGTHS);
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(err_hdr, PA_DEV_BAD_LENGTHS);
         return;
     }
     if (threadIdx.x == 0) {
@@ -153,7 +158,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         if (*abort_flag) return;
         if (!mbar_wait(bar, parity, lim)) {
             *abort_flag = 1;
-            set_device_error(header, PA_DEV_WAIT_TIMEOUT);
+            set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
         }
     };
 
@@ -230,7 +235,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     }
                     int page = __shfl_sync(0xffffffffu, win_val, lp - win_lo);
                     if (page < 0 || page >= P.num_pages) {
-                        if (lane == 0) set_device_error(header, PA_DEV_BAD_PAGE);
+                        if (lane == 0) set_device_error(err_hdr, PA_DEV_BAD_PAGE);
                         page = -1;
                     }
                     pg[j] = page;

@@ -57,6 +57,15 @@ def test_workspace_sizes_host_only(lib):
     pp = B.problem_from(wp, num_ctas=152)
     assert B.pa_assign_workspace_size(pp, B.PA_MODE_PREFILL) > 0
     assert B.pa_partial_workspace_size(pp, B.PA_MODE_PREFILL) % (128 * 129 * 4) == 0
+    # without a mask, prefill mode adds a decode part: one 16-row slot per
+    # (sequence, KV head) and per CTA, after the prefill partials
+    wd = W.prefill_bf16(sparse=False, shrink=32)
+    pd = B.problem_from(wd, num_ctas=152)
+    extra = (wd.num_seqs * wd.num_kv_heads + 152) * 16 * (128 + 1) * 4
+    assert (B.pa_partial_workspace_size(pd, B.PA_MODE_PREFILL)
+            == B.pa_partial_workspace_size(pp, B.PA_MODE_PREFILL) + extra)
+    assert (B.pa_assign_workspace_size(pd, B.PA_MODE_PREFILL)
+            > B.pa_assign_workspace_size(pp, B.PA_MODE_PREFILL))
 
 
 def test_invalid_problems_rejected_on_host(lib):

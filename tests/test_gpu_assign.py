@@ -2,6 +2,8 @@
 
 "基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2 Assign (load-balanced task
 map) and 二.1 (active-KV-tile compaction of the block mask)."""
+import copy
+
 import numpy as np
 import pytest
 import torch
@@ -23,11 +25,27 @@ def check(w, mode, num_ctas=0, balance_rows=0):
                 wd.block_mask if mode == B.PA_MODE_PREFILL else None, bufs.assign_ws)
     gpu = B.pa_read_task_map(bufs.problem, mode, bufs.assign_ws)
     assert B.pa_last_device_error(bufs.assign_ws) == 0
-    tm = oracle.assign(mode, w.num_seqs, w.num_q_heads, w.num_kv_heads, N,
-                       64 if mode == B.PA_MODE_DECODE else 128,
-                       balance_rows or 128, w.context_lens, w.q_lens,
-                       w.block_mask if mode == B.PA_MODE_PREFILL else None)
-    task_map_equal(gpu, tm, with_active=(mode == B.PA_MODE_PREFILL and w.block_mask is not None))
+    if mode == B.PA_MODE_DECODE:
+        tm = oracle.assign(mode, w.num_seqs, w.num_q_heads, w.num_kv_heads, N, 64,
+                           balance_rows or 128, w.context_lens, w.q_lens)
+        task_map_equal(gpu, tm, with_active=False)
+        return gpu
+    # prefill mode: the prefill map and the decode part (its own CTA count: the
+    # decode kernel's, for at most MIXED_DECODE_ROWS rows per unit)
+    G = w.num_q_heads // w.num_kv_heads
+    pd = copy.copy(bufs.problem)
+    pd.max_q_len = min(pd.max_q_len, max(1, oracle.MIXED_DECODE_ROWS // G))
+    has_part = w.block_mask is None and G <= oracle.MIXED_DECODE_ROWS
+    Nd = B.pa_num_ctas(pd, B.PA_MODE_DECODE) if has_part else N
+    pre, dec = oracle.assign_prefill(w.num_seqs, w.num_q_heads, w.num_kv_heads, N,
+                                     balance_rows or 128, w.context_lens, w.q_lens,
+                                     w.block_mask, decode_ctas=Nd)
+    task_map_equal(gpu, pre, with_active=w.block_mask is not None)
+    gpu_d = B.pa_read_task_map(bufs.problem, B.PA_MAP_DECODE_PART, bufs.assign_ws)
+    if dec is None:
+        assert gpu_d["num_units"] == 0 and gpu_d["num_tasks"] == 0
+    else:
+        task_map_equal(gpu_d, dec, with_active=False)
     return gpu
 
 

@@ -176,3 +176,60 @@ def test_full_size_decode_map_is_balanced(oracle_mod):
         per_cta.append(sum(int(t[2] - t[1]) for t in tm.tasks[tm.cta_ptr[c]:tm.cta_ptr[c + 1]]))
     assert max(per_cta) - min(per_cta) <= 1
     assert tm.num_tasks <= 512 + 152
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_prefill_split_covers_every_query_row_once(oracle_mod, seed):
+    """Prefill-mode Assign without a block mask sends a sequence to the decode
+    part iff 1 <= G * q_len <= 16.  Independently of how the two maps are
+    built: together they hold every (sequence, KV head, query token) exactly
+    once, each unit reaches exactly the keys its rows may see (decode part:
+    all ctx keys in 64-token tiles; prefill part: up to its last query's
+    position in 128-token tiles), and each part is balanced like any map."""
+    rng = np.random.default_rng(1000 + seed)
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    Hq = G * Hkv
+    B = int(rng.integers(1, 9))
+    N = int(rng.integers(1, 20))
+    rbal = int(rng.choice([16, 128, 288]))
+    ctx, ql = [], []
+    for _ in range(B):
+        c = int(rng.integers(0, 900))
+        q = int(rng.integers(0, min(c, 4) + 1)) if rng.random() < 0.6 else \
+            int(rng.integers(0, min(c, 300) + 1))
+        ctx.append(c)
+        ql.append(q)
+    pre, dec = oracle_mod.assign_prefill(B, Hq, Hkv, N, rbal, np.array(ctx, np.int32),
+                                         np.array(ql, np.int32))
+    assert dec is not None
+    small = [1 <= G * q <= 16 for q in ql]
+    seen = {}
+    for (b, hk, q0, nq), n in zip(pre.units.tolist(), pre.unit_ntiles.tolist()):
+        assert not small[b] and nq >= 1
+        assert n == -(-(ctx[b] - ql[b] + q0 + nq) // 128)
+        for i in range(q0, q0 + nq):
+            seen[(b, hk, i)] = seen.get((b, hk, i), 0) + 1
+    assert dec.units.tolist() == [[b, hk, 0, ql[b] if small[b] else 0]
+                                  for b in range(B) for hk in range(Hkv)]
+    for (b, hk, q0, nq), n in zip(dec.units.tolist(), dec.unit_ntiles.tolist()):
+        assert n == (-(-ctx[b] // 64) if nq > 0 else 0)
+        for i in range(nq):
+            seen[(b, hk, i)] = seen.get((b, hk, i), 0) + 1
+    want = {(b, hk, i) for b in range(B) for hk in range(Hkv) for i in range(ql[b])}
+    assert set(seen) == want and all(v == 1 for v in seen.values())
+    for tm in (pre, dec):
+        for u, n in enumerate(tm.unit_ntiles):
+            runs = [t for t in tm.tasks.tolist() if t[0] == u]
+            assert sum(t1 - t0 for _, t0, t1, _ in runs) == n
+        assert tm.num_tasks <= tm.num_units + N
+
+
+def test_prefill_split_absent_with_mask_or_wide_groups(oracle_mod):
+    ctx = np.array([300, 40, 500], np.int32)
+    ql = np.array([1, 40, 2], np.int32)
+    mask = np.ones((3, 1, 4), np.uint8)
+    pre, dec = oracle_mod.assign_prefill(3, 8, 2, 5, 128, ctx, ql, block_mask=mask)
+    assert dec is None and sorted({int(u[0]) for u in pre.units}) == [0, 1, 2]
+    pre, dec = oracle_mod.assign_prefill(3, 32, 1, 5, 128, ctx, ql)   # G = 32 > 16
+    assert dec is None and sorted({int(u[0]) for u in pre.units}) == [0, 1, 2]
