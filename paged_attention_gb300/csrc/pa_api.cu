@@ -287,10 +287,13 @@ pa_status make_prefill_layout(const pa_problem* p, PrefillLayout& M) {
     return PA_OK;
 }
 
+// Combine walks (unit, 4-row chunk) items: up to 8 CTAs of 128 threads per
+// SM, never more than the items of the largest possible fix list
 int combine_grid(const WsLayout& L) {
-    int grid = 2 * sm_count();
-    if (grid > L.unit_cap) grid = L.unit_cap;
-    return grid < 1 ? 1 : grid;
+    int64_t grid = 8 * (int64_t)sm_count();
+    const int64_t items = (int64_t)L.unit_cap * ((L.rows_cap + 3) / 4);
+    if (grid > items) grid = items;
+    return grid < 1 ? 1 : (int)grid;
 }
 
 }  // namespace
