@@ -204,20 +204,26 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             const int npg = (ctx_b + ps - 1) / ps;
             const int32_t* bt_row = P.block_table + (int64_t)b * P.max_pages_per_seq;
             if (pw == 0) wait(q_empty, (uint32_t)(task_it & 1) ^ 1u);
-            if (pw == 0 && lane == 0) {
-                if (*abort_flag) {
-                    mbar_arrive(q_full);
-                } else {
-                    mbar_arrive_expect_tx(q_full, (uint32_t)H * Cfg::kQTileBytes);
-                    for (int h = 0; h < H; ++h)
-#pragma unroll
-                        for (int c = 0; c < Cfg::kHalves; ++c)
-                            tma_load_3d(smem + Cfg::kOffQ + h * Cfg::kQTileBytes + c * Cfg::kRegion,
-                                        &tmq, q_full, 64 * c, hk * G, rec.cuq + q0 + h * half_tokens);
+            if (pw == 0) {
+                // lane 0 arms the Q buffer, then lane h * kHalves + c copies half
+                // h's column block c (one tensor copy per lane)
+                const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+                if (lane == 0) {
+                    if (go) mbar_arrive_expect_tx(q_full, (uint32_t)H * Cfg::kQTileBytes);
+                    else mbar_arrive(q_full);
+                }
+                __syncwarp();
+                if (go && lane < H * Cfg::kHalves) {
+                    const int h = lane / Cfg::kHalves, c = lane % Cfg::kHalves;
+                    tma_load_3d(smem + Cfg::kOffQ + h * Cfg::kQTileBytes + c * Cfg::kRegion, &tmq,
+                                q_full, 64 * c, hk * G, rec.cuq + q0 + h * half_tokens);
                 }
             }
             __syncwarp();
+            // block-table window: 32 page ids read lane-parallel; the next
+            // window's ids are requested one window ahead
             int win_lo = -(1 << 30), win_val = -1;
+            int nxt_lo = -(1 << 30), nxt_val = -1;
             for (int t = rec.tk.y; t < rec.tk.z; ++t) {
                 const int kt = tile_of(u, t);
                 uint32_t bytes = 0;
@@ -230,8 +236,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     if (tok0 >= ctx_b) continue;
                     const int lp = tok0 / ps;
                     if (lp - win_lo < 0 || lp - win_lo >= 32) {
+                        win_val = (lp == nxt_lo) ? nxt_val
+                                                 : ((lp + lane < npg) ? __ldg(bt_row + lp + lane) : -1);
                         win_lo = lp;
-                        win_val = (lp + lane < npg) ? __ldg(bt_row + lp + lane) : -1;
+                        nxt_lo = lp + 32;
+                        nxt_val = (nxt_lo + lane < npg) ? __ldg(bt_row + nxt_lo + lane) : -1;
                     }
                     int page = __shfl_sync(0xffffffffu, win_val, lp - win_lo);
                     if (page < 0 || page >= P.num_pages) {
