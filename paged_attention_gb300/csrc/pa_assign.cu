@@ -55,6 +55,46 @@ __device__ int64_t block_exscan(int64_t v, int64_t* total, int64_t* sm) {
     return excl;
 }
 
+// The same for three values at once (one set of barriers); sm: 3 * 32 int64.
+__device__ void block_exscan3(const int64_t (&v)[3], int64_t (&excl)[3], int64_t (&total)[3],
+                              int64_t* sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int64_t x[3] = {v[0], v[1], v[2]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            int64_t y = __shfl_up_sync(0xffffffffu, x[i], o);
+            if (lane >= o) x[i] += y;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) sm[i * 32 + warp] = x[i];
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            int64_t w = lane < nwarps ? sm[i * 32 + lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            sm[i * 32 + lane] = w;  // inclusive per warp
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        excl[i] = (x[i] - v[i]) + (warp > 0 ? sm[i * 32 + warp - 1] : 0);
+        total[i] = sm[i * 32 + nwarps - 1];
+    }
+    __syncthreads();
+}
+
 __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // query tokens of a sequence that this map covers (see WsLayout::cls)
@@ -193,9 +233,18 @@ __device__ __forceinline__ void for_each_owner(int64_t P, int n, int64_t w, int6
     }
 }
 
+// Units whose tile count, weight and split count the map pass keeps in
+// shared memory (3 x 4 bytes each); larger maps read them from the workspace.
+constexpr int kMapCacheUnits = 12288;
+constexpr int kMapCacheBytes = kMapCacheUnits * 12;
+
 // Cost prefix, ownership, tasks, split slots, combine fix list and cta_ptr,
-// for the U units already written (one CTA; sm: 32 int64 of shared memory).
-__device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm) {
+// for the U units already written (one CTA; sm: 3 * 32 int64 of shared
+// memory; cache: kMapCacheBytes of shared memory or nullptr).  Each thread
+// owns a contiguous run of units; with the cache, the units' tile counts and
+// weights are staged once with coalesced loads, and a unit's prefix is
+// rebuilt from the thread's running sum instead of being read back.
+__device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm, int32_t* cache) {
     int32_t* header = ws_ptr<int32_t>(ws, L.off_header);
     const int4* units = ws_ptr<int4>(ws, L.off_units);
     const int32_t* ntiles = ws_ptr<int32_t>(ws, L.off_ntiles);
@@ -212,45 +261,67 @@ __device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm) {
     const int chunk = (U + kScanThreads - 1) / kScanThreads;
     const int u0 = min(U, tid * chunk), u1 = min(U, u0 + chunk);
 
+    const bool cached = cache != nullptr && U <= kMapCacheUnits;
+    int32_t* c_n = cache;                                   // [U] tiles
+    int32_t* c_w = cache + (cached ? U : 0);                // [U] weight
+    int32_t* c_s = cache + (cached ? 2 * U : 0);            // [U] tasks (splits)
+    if (cached) {
+        for (int u = tid; u < U; u += blockDim.x) {
+            c_n[u] = ntiles[u];
+            c_w[u] = (int32_t)unit_weight(L, units[u].w);
+        }
+        __syncthreads();
+    }
+    auto n_of = [&](int u) -> int { return cached ? c_n[u] : ntiles[u]; };
+    auto w_of = [&](int u) -> int64_t { return cached ? (int64_t)c_w[u] : unit_weight(L, units[u].w); };
+    auto nq_of = [&](int u) -> int { return units[u].w; };
+
     // cost prefix
     int64_t cost = 0;
-    for (int u = u0; u < u1; ++u) cost += (int64_t)ntiles[u] * unit_weight(L, units[u].w);
+    for (int u = u0; u < u1; ++u) cost += (int64_t)n_of(u) * w_of(u);
     int64_t C;
-    int64_t run = block_exscan(cost, &C, sm);
-    for (int u = u0; u < u1; ++u) {
-        prefix[u] = run;
-        run += (int64_t)ntiles[u] * unit_weight(L, units[u].w);
-    }
+    const int64_t run0 = block_exscan(cost, &C, sm);
 
     // tasks per unit, split slots, units the combine pass must finish
-    int64_t nt = 0, ns = 0, nf = 0;
-    for (int u = u0; u < u1; ++u) {
-        int S = 0;
-        for_each_owner(prefix[u], ntiles[u], unit_weight(L, units[u].w), C, N,
-                       [&](int, int, int) { ++S; });
-        nsplit[u] = S;
-        nt += S;
-        ns += S > 1 ? S : 0;
-        nf += (S != 1 && units[u].w > 0) ? 1 : 0;
+    int64_t cnt[3] = {0, 0, 0};   // tasks, split slots, fix-list entries
+    {
+        int64_t run = run0;
+        for (int u = u0; u < u1; ++u) {
+            const int n = n_of(u);
+            const int64_t w = w_of(u);
+            prefix[u] = run;
+            int S = 0;
+            for_each_owner(run, n, w, C, N, [&](int, int, int) { ++S; });
+            run += (int64_t)n * w;
+            nsplit[u] = S;
+            if (cached) c_s[u] = S;
+            cnt[0] += S;
+            cnt[1] += S > 1 ? S : 0;
+            cnt[2] += (S != 1 && nq_of(u) > 0) ? 1 : 0;
+        }
     }
-    int64_t T, Sl, F;
-    int64_t t_run = block_exscan(nt, &T, sm);
-    int64_t s_run = block_exscan(ns, &Sl, sm);
-    int64_t f_run = block_exscan(nf, &F, sm);
-    for (int u = u0; u < u1; ++u) {
-        const int S = nsplit[u];
-        const int s0 = S > 1 ? (int)s_run : -1;
-        slot0[u] = s0;
-        int k = 0;
-        for_each_owner(prefix[u], ntiles[u], unit_weight(L, units[u].w), C, N,
-                       [&](int c, int tlo, int thi) {
-                           tasks[t_run + k] = make_int4(u, tlo, thi, S > 1 ? s0 + k : -1);
-                           task_cta[t_run + k] = c;
-                           ++k;
-                       });
-        t_run += S;
-        s_run += S > 1 ? S : 0;
-        if (S != 1 && units[u].w > 0) fix[f_run++] = u;
+    int64_t base[3], tot[3];
+    block_exscan3(cnt, base, tot, sm);
+    const int64_t T = tot[0], Sl = tot[1], F = tot[2];
+    {
+        int64_t run = run0, t_run = base[0], s_run = base[1], f_run = base[2];
+        for (int u = u0; u < u1; ++u) {
+            const int n = n_of(u);
+            const int64_t w = w_of(u);
+            const int S = cached ? c_s[u] : nsplit[u];
+            const int s0 = S > 1 ? (int)s_run : -1;
+            slot0[u] = s0;
+            int k = 0;
+            for_each_owner(run, n, w, C, N, [&](int c, int tlo, int thi) {
+                tasks[t_run + k] = make_int4(u, tlo, thi, S > 1 ? s0 + k : -1);
+                task_cta[t_run + k] = c;
+                ++k;
+            });
+            run += (int64_t)n * w;
+            t_run += S;
+            s_run += S > 1 ? S : 0;
+            if (S != 1 && nq_of(u) > 0) fix[f_run++] = u;
+        }
     }
     __syncthreads();
     // cta_ptr[c] = number of tasks owned by CTAs < c.  task_cta is sorted, so
@@ -273,9 +344,10 @@ __device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm) {
 }
 
 __global__ void __launch_bounds__(kScanThreads) assign_map_kernel(WsLayout L, void* ws) {
-    __shared__ int64_t sm[32];
+    __shared__ int64_t sm[3 * 32];
+    extern __shared__ int32_t map_cache[];   // kMapCacheBytes
     grid_launch_dependents();   // the compute kernel may become resident meanwhile
-    assign_map_body(L, ws, sm);
+    assign_map_body(L, ws, sm, map_cache);
 }
 
 // Decode mode in one launch: units are (b, hk) in order, Hkv per sequence,
@@ -283,7 +355,7 @@ __global__ void __launch_bounds__(kScanThreads) assign_map_kernel(WsLayout L, vo
 __global__ void __launch_bounds__(kScanThreads)
 assign_decode_kernel(WsLayout L, const int32_t* __restrict__ ctx, const int32_t* __restrict__ ql,
                      void* ws) {
-    __shared__ int64_t sm[32];
+    __shared__ int64_t sm[3 * 32];
     grid_launch_dependents();   // the compute kernel may become resident meanwhile
     int32_t* header = ws_ptr<int32_t>(ws, L.off_header);
     int32_t* cu_q = ws_ptr<int32_t>(ws, L.off_cu_q);
@@ -329,7 +401,7 @@ assign_decode_kernel(WsLayout L, const int32_t* __restrict__ ctx, const int32_t*
         ntiles[u] = (int)ceil_div64(keys, L.kv_tile);
     }
     __syncthreads();   // header, units and tiles visible to the whole CTA
-    assign_map_body(L, ws, sm);
+    assign_map_body(L, ws, sm, nullptr);
 }
 
 }  // namespace
@@ -344,7 +416,18 @@ cudaError_t launch_assign(const WsLayout& L, const int32_t* ctx, const int32_t* 
     const int warps = 8;
     const int grid = (L.unit_cap + warps - 1) / warps;
     assign_units_kernel<<<grid > 0 ? grid : 1, warps * 32, 0, stream>>>(L, ctx, ql, mask, ws);
-    assign_map_kernel<<<1, kScanThreads, 0, stream>>>(L, ws);
+    // the shared-memory opt-in, once per device
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(assign_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMapCacheBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    assign_map_kernel<<<1, kScanThreads, kMapCacheBytes, stream>>>(L, ws);
     return cudaGetLastError();
 }
 

@@ -103,3 +103,15 @@ def test_decode_map_many_short_sequences():
                         page_size=16, seed=77, mode="decode")
     check(w, B.PA_MODE_DECODE)
     check(w, B.PA_MODE_DECODE, num_ctas=7)
+
+
+def test_prefill_map_beyond_the_shared_memory_cache():
+    """24,000 prefill units: more than the map pass keeps in shared memory, so
+    it reads unit data from the workspace (the other path of the same pass)."""
+    g = torch.Generator().manual_seed(78)
+    B_ = 3000
+    ctx = torch.randint(40, 200, (B_,), generator=g).tolist()
+    ql = [min(c, 5 + int(q)) for c, q in zip(ctx, torch.randint(0, 20, (B_,), generator=g).tolist())]
+    w = W.make_workload("manyp", ctx, ql, num_q_heads=32, num_kv_heads=8, head_dim=64,
+                        page_size=16, seed=78, mode="prefill")
+    check(w, B.PA_MODE_PREFILL)
