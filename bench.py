@@ -45,16 +45,18 @@ def load_peaks():
             "source": "fallback"}
 
 
-def make_workload(name: str, rank: int, shrink: int = 1):
+def make_workload(name: str, rank: int, shrink: int = 1, mtp: int = 0):
     """The workload's batch for `rank`: every rank draws its own independent
     batch of the same shape (weak scaling).  shrink > 1 divides batch and
-    lengths (small profiling cases only; bench lines use shrink = 1)."""
+    lengths (small profiling cases only; bench lines use shrink = 1).  mtp
+    (decode workloads) sets q_len = 1 + mtp; 0 keeps the default (1 for bf16,
+    2 for E4M3)."""
     from paged_attention_gb300 import workloads as W
     from paged_attention_gb300.dist import rank_seed
     if name == "decode_bf16":
-        return W.decode_bf16(mtp=1, seed=rank_seed(1002, rank), shrink=shrink)
+        return W.decode_bf16(mtp=mtp or 1, seed=rank_seed(1002, rank), shrink=shrink)
     if name == "decode_fp8":
-        return W.decode_fp8(seed=rank_seed(1003, rank), shrink=shrink)
+        return W.decode_fp8(seed=rank_seed(1003, rank), shrink=shrink, mtp=mtp or 2)
     if name == "prefill_dense":
         return W.prefill_bf16(sparse=False, seed=rank_seed(1004, rank), shrink=shrink)
     if name == "prefill_sparse":
@@ -206,7 +208,7 @@ def run_native(args, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     name = args.workload
-    w_cpu = make_workload(name, rank, args.shrink)
+    w_cpu = make_workload(name, rank, args.shrink, args.mtp)
     w = w_cpu.to(dev)
     work, kind = work_of(w_cpu, name)
     mode = B.PA_MODE_DECODE if is_decode(name) else B.PA_MODE_PREFILL
@@ -452,7 +454,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     name = args.workload
-    w = make_workload(name, 0)
+    w = make_workload(name, 0, 1, args.mtp)
     per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     vals = []
     sample = ""
@@ -489,6 +491,8 @@ def main():
                              "hybrid"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mtp", type=int, default=0,
+                    help="decode workloads: q_len = 1 + MTP (default: 1 for bf16, 2 for E4M3)")
     ap.add_argument("--shrink", type=int, default=1,
                     help="divide batch and lengths (profiling of small cases only)")
     args = ap.parse_args()

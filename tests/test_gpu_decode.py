@@ -97,6 +97,16 @@ def test_decode_fp8_full_size_sampled():
     run_and_compare(w, rows=rows)
 
 
+def test_decode_fp8_q_len_4_full_size_sampled():
+    """The E4M3 workload with four query tokens per sequence (MTP 3 here;
+    the pages' "MTP4" row counts the tokens): 32 rows per unit, the
+    four-tile variant, sampled rows at full size."""
+    w = W.decode_fp8(mtp=3)
+    rng = np.random.default_rng(4)
+    rows = np.sort(rng.choice(w.total_q * w.num_q_heads, size=4096, replace=False))
+    run_and_compare(w, rows=rows)
+
+
 def test_decode_is_deterministic():
     w = W.decode_bf16(mtp=3, shrink=8).to("cuda")
     a = B.run_decode(w)
