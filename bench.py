@@ -156,13 +156,13 @@ def oracle_sample_rate(w, name, target_s):
     ql = [int(x) for x in w.q_lens]
     cu = np.concatenate([[0], np.cumsum(ql)])
     done_rows = 0
-    seqs = 0
+    runs = 0          # sequence runs; the batch is walked again when it runs out
     t_total = 0.0
     work = 0
-    order = list(range(w.num_seqs))
+    n = w.num_seqs
     decode_like = is_decode(name) or name == "hybrid"
-    while seqs < len(order) and t_total < target_s:
-        b = order[seqs]
+    while runs < 100 * n and (runs == 0 or t_total < target_s):
+        b = runs % n
         rows = np.arange(cu[b] * Hq, cu[b + 1] * Hq, dtype=np.int64)
         if not decode_like and len(rows) > 4096:
             rows = rows[:: max(1, len(rows) // 4096)]
@@ -178,15 +178,18 @@ def oracle_sample_rate(w, name, target_s):
             frac = len(rows) / (ql[b] * Hq)
             pairs = ql[b] * (c - ql[b]) + ql[b] * (ql[b] + 1) // 2
             work += int(4 * w.head_dim * Hq * pairs * frac)
-        seqs += 1
+        runs += 1
     if decode_like:
         value = work / t_total / 1e9
         unit = "GB/s"
     else:
         value = work / t_total / 1e12
         unit = "TFLOP/s"
-    sample = (f"oracle on sequences 0..{seqs - 1} of the workload ({done_rows} query rows, "
-              f"{t_total:.1f} s)")
+    if runs <= n:
+        what = f"sequences 0..{runs - 1} of the workload"
+    else:
+        what = f"the whole batch ({n} sequences) {runs / n:.1f} times over"
+    sample = f"oracle on {what} ({done_rows} query rows, {t_total:.1f} s)"
     return value, unit, sample, cores, t_total
 
 
