@@ -442,7 +442,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             const int p_row = ctx_b - rec.ql + q0 + r / G;   // last key this row sees
             const int key_last = p_row < ctx_b - 1 ? p_row : ctx_b - 1;
             const int n = rec.tk.z - rec.tk.y;
-            // a warp whose 32 rows are all padding (decode units fill a few rows)
+            // a warp whose 32 rows are all padding (units of a few rows: short
+            // sequences of a masked batch, or the last q tile of a sequence)
             // keeps the barrier protocol but skips the math: MMA rows are
             // independent and padding rows are never written
             const bool warp_live = __any_sync(0xffffffffu, row_ok);

@@ -1,5 +1,6 @@
-"""GPU prefill / mixed batch (Assign + tcgen05 prefill + Combine) against the
-fp64 oracle.
+"""GPU prefill / mixed batch (Assign + tcgen05 prefill + Combine; the
+decode-shaped sequences of an unmasked batch run on the decode kernel) against
+the fp64 oracle.
 
 "基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2 Prefill (causal,
 block-sparse over paged KV) and 二.1 (only kept tiles are computed); the
