@@ -90,16 +90,40 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments or blank-line and trailing-space noise."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] in "\"'":
+            q, j = text[i], i + 1
+            while j < n and text[j] != q:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_fingerprint(kernel: str) -> str:
-    """Short hash of the sources of one entry point's kernel; stored beside
-    counters taken from that kernel so stale counters can be recognised."""
+    """Short hash of the code (comments stripped) of one entry point's kernel
+    sources; stored beside counters taken from that kernel so stale counters
+    can be recognised, while a comment edit keeps them valid."""
     h = hashlib.sha256()
     files = [os.path.join(CSRC, f) for f in KERNEL_SOURCES[kernel]] + [
         os.path.join(CSRC, "pa_internal.cuh"), os.path.join(CSRC, "pa_api.cu"),
         os.path.join(INCLUDE, "pa.h")]
     for f in files:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(os.path.basename(f).encode() + _code_only(fh.read()).encode())
     h.update(" ".join(ARCH + NVCC_FLAGS[:4]).encode())
     return h.hexdigest()[:16]
 
