@@ -51,6 +51,7 @@ class OracleProblem(ctypes.Structure):
         ("mask_kv_tiles", ctypes.c_int32),
         ("mask_tile", ctypes.c_int32),
         ("sm_scale", ctypes.c_double),
+        ("window", ctypes.c_int32),
     ]
 
 
@@ -167,7 +168,7 @@ def attention(w, rows=None, key_lo=0, key_hi=INT64_MAX, mask=True, num_threads=0
         max_pages_per_seq=bt.shape[1], layout=w.layout, kv_dtype=w.kv_dtype,
         mask_q_tiles=(bm.shape[1] if bm is not None else 0),
         mask_kv_tiles=(bm.shape[2] if bm is not None else 0),
-        mask_tile=w.mask_tile, sm_scale=float(w.sm_scale))
+        mask_tile=w.mask_tile, sm_scale=float(w.sm_scale), window=int(getattr(w, "window", 0)))
     out = np.zeros((n_rows, w.head_dim), dtype=np.float64)
     lse = np.zeros((n_rows,), dtype=np.float64)
     rc = lib.oracle_attention(ctypes.byref(prob), _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks),

@@ -55,6 +55,9 @@ typedef struct {
     int32_t mask_kv_tiles;
     int32_t mask_tile;         /* tokens per mask tile edge (128)            */
     double sm_scale;
+    int32_t window;            /* 0: none; else sliding window: query p sees keys
+                                  p - window < j <= p ("HiLS-Attention", 二.1
+                                  local branch; the bounds are our reading) */
 } oracle_problem;
 
 /* ---------------------------------------------------------------- decoding */
@@ -118,12 +121,15 @@ static double kv_value(const oracle_problem* P, const void* cache, const float* 
 }
 
 /* Visibility of key j to local query i of sequence b: inside the context,
- * not after the query's own position (causal), inside [key_lo, key_hi) and,
- * when a block mask is given, inside a kept tile. */
+ * not after the query's own position (causal), inside the sliding window when
+ * one is set, inside [key_lo, key_hi) and, when a block mask is given, inside a
+ * kept tile. */
 static int visible(const oracle_problem* P, const uint8_t* mask, int b, int i, int64_t p, int j,
                    int64_t key_lo, int64_t key_hi)
 {
     if (j > p || j < key_lo || j >= key_hi)
+        return 0;
+    if (P->window > 0 && (int64_t)j <= p - P->window)
         return 0;
     if (mask && P->mask_q_tiles > 0) {
         int qt = i / P->mask_tile, kt = j / P->mask_tile;

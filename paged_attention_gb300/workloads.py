@@ -70,6 +70,7 @@ class Workload:
     block_mask: Optional[torch.Tensor] = None   # uint8 [B, mask_q_tiles, mask_kv_tiles]
     mask_tile: int = 128
     mode: str = "decode"                  # which Assign mode the workload is run with
+    window: int = 0                       # sliding window (0 = none); oracle only so far
     meta: dict = field(default_factory=dict)
 
     @property

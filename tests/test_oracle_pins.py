@@ -54,6 +54,8 @@ def visibility(w, b):
     i = torch.arange(ql)[:, None]
     j = torch.arange(ctx)[None, :]
     vis = j <= (ctx - ql + i)
+    if w.window > 0:                         # sliding window: p - window < j <= p
+        vis = vis & (j > (ctx - ql + i) - w.window)
     if w.block_mask is not None:
         m = w.block_mask[b].bool()
         qt = (i // w.mask_tile).expand(ql, ctx)
@@ -406,3 +408,71 @@ def test_block_mask_skip_ratio_matches_pages():
     assert 0.70 < 1.0 - kept < 0.78
     assert bool(m[:, torch.eye(t, dtype=torch.bool)].all())
     assert not bool(m[:, torch.triu(torch.ones(t, t, dtype=torch.bool), 1)].any())
+
+
+# ------------------------------------------------ sliding window (local branch)
+# "HiLS-Attention" page, 二.1 (the local sliding-window branch): query p sees
+# the keys p - window < j <= p.  The bounds are our reading (the page gives
+# none); the kernels do not take a window yet.
+
+def _windowed(w, window):
+    w.window = window
+    return w
+
+
+@pytest.mark.parametrize("which,window", [("decode", 100), ("prefill", 300), ("hybrid", 64),
+                                          ("tiny", 7)])
+def test_window_matches_torch_sdpa(oracle_mod, which, window):
+    w = {"decode": lambda: W.decode_bf16(mtp=3, shrink=32),
+         "prefill": lambda: W.prefill_bf16(sparse=False, shrink=32),
+         "hybrid": lambda: W.hybrid_bf16(shrink=32),
+         "tiny": W.tiny_mixed}[which]()
+    _windowed(w, window)
+    out, lse = oracle_mod.attention(w)
+    ref_o, ref_l = library_reference(w)
+    np.testing.assert_allclose(out, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l, rtol=0, atol=1e-12)
+
+
+def test_window_as_long_as_the_context_changes_nothing(oracle_mod):
+    w = W.hybrid_bf16(shrink=32)
+    out, lse = oracle_mod.attention(w)
+    _windowed(w, int(w.context_lens.max()))
+    o2, l2 = oracle_mod.attention(w)
+    assert np.array_equal(out, o2) and np.array_equal(lse, l2)
+
+
+def test_window_of_one_selects_the_own_key(oracle_mod):
+    """Only key p is visible: O = v_p and LSE = sm_scale * q . k_p."""
+    w = _windowed(_decode_ws([40, 9], [3, 9]), 1)
+    out, lse = oracle_mod.attention(w)
+    G = w.num_q_heads // w.num_kv_heads
+    cu = 0
+    for b in range(2):
+        ctx, ql = int(w.context_lens[b]), int(w.q_lens[b])
+        for hk in range(w.num_kv_heads):
+            K, V = dense_kv(w, b, hk, "k"), dense_kv(w, b, hk, "v")
+            for i in range(ql):
+                p = ctx - ql + i
+                for g in range(G):
+                    h = hk * G + g
+                    r = (cu + i) * w.num_q_heads + h
+                    q = w.q[cu + i, h].double()
+                    np.testing.assert_allclose(out[r], V[p].numpy(), rtol=0, atol=1e-12)
+                    assert abs(lse[r] - float(w.sm_scale * (q @ K[p]))) <= 1e-12
+        cu += ql
+
+
+def test_keys_before_the_window_are_never_read(oracle_mod):
+    """NaN in every key at or before p - window leaves a decode row unchanged."""
+    w = _windowed(_decode_ws([70], [1]), 10)
+    out, lse = oracle_mod.attention(w)
+    p = 69
+    pages = w.block_table[0, :(70 + 15) // 16]
+    for j in range(0, p - 10 + 1):
+        pg, sl = int(pages[j // 16]), j % 16
+        w.k_cache[pg, sl] = float("nan")
+        w.v_cache[pg, sl] = float("inf")
+    o2, l2 = oracle_mod.attention(w)
+    assert np.isfinite(o2).all()
+    assert np.array_equal(o2, out) and np.array_equal(l2, lse)
