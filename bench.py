@@ -74,6 +74,8 @@ def workload_config(w, name):
            "total_q_tokens": w.total_q, "total_kv_tokens": int(w.context_lens.sum())}
     if "mtp" in w.meta:
         cfg["mtp"] = w.meta["mtp"]
+    if w.window:
+        cfg["window"] = w.window
     return cfg
 
 
@@ -212,6 +214,10 @@ def run_native(args, rank, world, dist):
     torch.cuda.set_device(dev)
     name = args.workload
     w_cpu = make_workload(name, rank, args.shrink, args.mtp)
+    if args.window:
+        if not is_decode(name) or w_cpu.kv_dtype != 0:
+            raise SystemExit("--window: bf16 decode workloads only")
+        w_cpu.window = args.window
     w = w_cpu.to(dev)
     work, kind = work_of(w_cpu, name)
     mode = B.PA_MODE_DECODE if is_decode(name) else B.PA_MODE_PREFILL
@@ -458,6 +464,8 @@ def run_reference(args, rank, world):
         return
     name = args.workload
     w = make_workload(name, 0, 1, args.mtp)
+    if args.window:
+        w.window = args.window
     per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     vals = []
     sample = ""
@@ -494,6 +502,8 @@ def main():
                              "hybrid"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window (bf16 decode workloads): keys p - window < j <= p")
     ap.add_argument("--mtp", type=int, default=0,
                     help="decode workloads: q_len = 1 + MTP (default: 1 for bf16, 2 for E4M3)")
     ap.add_argument("--shrink", type=int, default=1,

@@ -126,6 +126,11 @@ typedef struct pa_problem {
     int32_t num_ctas;          /* persistent CTAs; 0 = the library's choice          */
     int32_t balance_rows;      /* Assign weight divisor; 0 = 128                     */
     float sm_scale;            /* softmax scale applied to q.k; finite and >= 0      */
+    int32_t window;            /* sliding window ("HiLS-Attention", 二.1 local
+                                  branch): 0 = none, else the query at position p
+                                  sees only the keys p - window < j <= p.  Decode
+                                  mode with bf16 K/V only so far; elsewhere
+                                  PA_ERR_UNSUPPORTED.  Negative: invalid.       */
 } pa_problem;
 
 /* Human-readable name of a pa_status or PA_DEV_* code set. */

@@ -85,7 +85,7 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int64, vp, vp, vp,
-                ctypes.c_int64]
+                ctypes.c_int64, ctypes.c_int]
             lib.oracle_combine.restype = None
             lib.oracle_combine.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]
             lib.oracle_e4m3_to_double.restype = ctypes.c_double
@@ -200,10 +200,11 @@ class TaskMap:
 
 
 def assign(mode, num_seqs, num_q_heads, num_kv_heads, num_ctas, kv_tile, balance_rows,
-           context_lens, q_lens, block_mask=None, mask_tile=128):
+           context_lens, q_lens, block_mask=None, mask_tile=128, window=0):
     """Oracle Assign (the tile-by-tile procedure written in pa_oracle.c).
 
     mode 0 = decode units (b, hk); mode 1 = prefill / mixed units (b, hk, q tile).
+    window > 0: a unit's tiles start at the first one its first query can see.
     """
     lib = _load()
     ctx = _arr(context_lens, np.int32)
@@ -233,7 +234,7 @@ def assign(mode, num_seqs, num_q_heads, num_kv_heads, num_ctas, kv_tile, balance
         (bm.shape[1] if bm is not None else 0), (bm.shape[2] if bm is not None else 0),
         int(mask_tile), _ptr(units), _ptr(ntiles), _ptr(active), int(max_kv_tiles),
         _ptr(cta_ptr), _ptr(tasks), int(task_cap), _ptr(nsplit), _ptr(slot0), _ptr(counts),
-        int(unit_cap))
+        int(unit_cap), int(window))
     if rc != 0:
         raise ValueError(f"oracle_assign failed with status {rc}")
     U, n_tasks, n_slots = (int(x) for x in counts)

@@ -369,7 +369,7 @@ int oracle_assign(int mode, int B, int Hq, int Hkv, int N, int kv_tile, int bala
                   int mask_kv_tiles, int mask_tile, int32_t* units, int32_t* unit_ntiles,
                   int32_t* active, int max_kv_tiles, int32_t* cta_ptr, int32_t* tasks,
                   int64_t task_cap, int32_t* unit_nsplit, int32_t* unit_slot0, int32_t* counts,
-                  int64_t unit_cap)
+                  int64_t unit_cap, int window)
 {
     int G, qtok, b, hk, c;
     int64_t U = 0, u, C, n_tasks = 0, slots = 0;
@@ -408,7 +408,16 @@ int oracle_assign(int mode, int B, int Hq, int Hkv, int N, int kv_tile, int bala
                 units[U * 4 + 1] = hk;
                 units[U * 4 + 2] = q0;
                 units[U * 4 + 3] = nq;
-                for (t = 0; (int64_t)t * kv_tile < L; ++t) {
+                /* sliding window: the unit's first query (position ctx - ql + q0)
+                 * sees no key before p0 - window + 1; tiles wholly before it are
+                 * not the unit's */
+                t = 0;
+                if (window > 0) {
+                    int64_t lo = (int64_t)ctx[b] - ql[b] + q0 - window + 1;
+                    if (lo > 0)
+                        t = (int)(lo / kv_tile);
+                }
+                for (; (int64_t)t * kv_tile < L; ++t) {
                     int keep = 1;
                     if (mask) {
                         int mq = q0 / mask_tile;

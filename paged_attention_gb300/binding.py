@@ -66,6 +66,7 @@ class PaProblem(ctypes.Structure):
         ("num_ctas", ctypes.c_int32),
         ("balance_rows", ctypes.c_int32),
         ("sm_scale", ctypes.c_float),
+        ("window", ctypes.c_int32),
     ]
 
 
@@ -153,7 +154,8 @@ def problem_from(w, num_ctas: int = 0, balance_rows: int = 0) -> PaProblem:
         layout=w.layout, kv_dtype=w.kv_dtype,
         mask_q_tiles=(bm.shape[1] if bm is not None else 0),
         mask_kv_tiles=(bm.shape[2] if bm is not None else 0),
-        num_ctas=num_ctas, balance_rows=balance_rows, sm_scale=float(w.sm_scale))
+        num_ctas=num_ctas, balance_rows=balance_rows, sm_scale=float(w.sm_scale),
+        window=int(getattr(w, "window", 0)))
 
 
 # ------------------------------------------------------------ entry points

@@ -91,8 +91,11 @@ pa_status check_problem(const pa_problem* pp, int mode) {
         p.num_q_heads % p.num_kv_heads != 0 || p.num_pages < 1 || p.max_pages_per_seq < 1 ||
         p.total_q_tokens < 0 || p.max_q_len < 0 || p.max_context_len < p.max_q_len ||
         p.mask_q_tiles < 0 || p.mask_kv_tiles < 0 || p.num_ctas < 0 || p.balance_rows < 0 ||
-        !std::isfinite(p.sm_scale) || p.sm_scale < 0.f)
+        !std::isfinite(p.sm_scale) || p.sm_scale < 0.f || p.window < 0)
         return PA_ERR_INVALID_ARG;
+    // sliding window: the bf16 decode kernel only, so far
+    if (p.window > 0 && (mode != PA_MODE_DECODE || p.kv_dtype != PA_BF16))
+        return PA_ERR_UNSUPPORTED;
     if (p.layout != PA_NHD && p.layout != PA_HND) return PA_ERR_INVALID_ARG;
     if (p.kv_dtype != PA_BF16 && p.kv_dtype != PA_FP8_E4M3) return PA_ERR_INVALID_ARG;
     if ((p.mask_q_tiles > 0) != (p.mask_kv_tiles > 0)) return PA_ERR_INVALID_ARG;
@@ -331,6 +334,7 @@ bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L)
     L.max_ctx = p.max_context_len;
     L.mask_q_tiles = p.mask_q_tiles;
     L.mask_kv_tiles = p.mask_kv_tiles;
+    L.window = p.window;
     int64_t off = 0;
     auto take = [&](int64_t bytes) {
         int64_t o = off;

@@ -398,7 +398,10 @@ assign_decode_kernel(WsLayout L, const int32_t* __restrict__ ctx, const int32_t*
         const int nq = class_ql(L, ql[b]);
         const int64_t keys = nq > 0 ? ctx[b] : 0;
         units[u] = make_int4(b, hk, 0, nq);
-        ntiles[u] = (int)ceil_div64(keys, L.kv_tile);
+        // with a sliding window the unit's tiles start at the first one its
+        // first query (position ctx - nq) can see
+        const int first = nq > 0 ? window_first_tile(L.window, ctx[b] - nq, L.kv_tile) : 0;
+        ntiles[u] = (int)ceil_div64(keys, L.kv_tile) - first;
     }
     __syncthreads();   // header, units and tiles visible to the whole CTA
     assign_map_body(L, ws, sm, nullptr);

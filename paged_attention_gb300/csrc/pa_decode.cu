@@ -153,6 +153,11 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
             const int r_lo = 16 * rt + g, r_hi = r_lo + 8;
             const bool v_lo = r_lo < R, v_hi = r_hi < R;
             const int p_lo = pbase + r_lo / G, p_hi = pbase + r_hi / G;
+            // sliding window: keys > p - window (no bound without a window), and
+            // task positions count from the unit's first visible tile
+            const int w_lo = L.window > 0 ? p_lo - L.window : -1;
+            const int w_hi = L.window > 0 ? p_hi - L.window : -1;
+            const int first = window_first_tile(L.window, pbase, kDecodeTile);
 
             // Q fragments (A operand, rows x D) from the TMA-filled slot
             uint32_t qf[D / 16][4];
@@ -180,7 +185,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                 if (NG > 1 && (it % NG) != grp) continue;
                 const int s = it % STAGES;
                 wait(&full[s], (uint32_t)((it / STAGES) & 1));
-                const int kt = t;
+                const int kt = t + first;
                 const int tok_s0 = kt * kDecodeTile + 16 * ts;
                 uint8_t* stK = smem + s * Cfg::kStageBytes;
                 uint8_t* stV = stK + Cfg::kKBytes;
@@ -230,8 +235,8 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int tok = tok_s0 + 8 * j + 2 * q4 + e;
-                        const bool okl = v_lo && tok < ctx_b && tok <= p_lo;
-                        const bool okh = v_hi && tok < ctx_b && tok <= p_hi;
+                        const bool okl = v_lo && tok < ctx_b && tok <= p_lo && tok > w_lo;
+                        const bool okh = v_hi && tok < ctx_b && tok <= p_hi && tok > w_hi;
                         sv[j][e] = okl ? (sa[j][e] + sb[j][e]) * cs : -INFINITY;
                         sv[j][2 + e] = okh ? (sa[j][2 + e] + sb[j][2 + e]) * cs : -INFINITY;
                     }

@@ -116,11 +116,13 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
         int win_lo = -(1 << 30), win_val = -1;
         int nxt_lo = -(1 << 30), nxt_val = -1;
         float win_ks = 0.f, win_vs = 0.f;
+        // sliding window: task positions count from the unit's first visible tile
+        const int first = window_first_tile(L.window, ctx_b - rec.ql + un.z, kDecodeTile);
         for (int t = tk.y; t < tk.z; ++t, ++it) {
             if (Cfg::kProducerWarps > 1 && it % Cfg::kProducerWarps != pw) continue;
             const int s = it % Cfg::kStages;
             wait(&empty[s], (uint32_t)((it / Cfg::kStages) & 1) ^ 1u);
-            const int kt = t;
+            const int kt = t + first;
             int pg[4];
             float ksc[4], vsc[4];
             uint32_t bytes = 0;

@@ -42,6 +42,14 @@ enum HeaderWord {
     H_MODE = 6,
 };
 
+// First KV tile (of `tile` tokens) any row of a unit can see under a sliding
+// window: its first query sits at position p0 and sees keys > p0 - window.
+__host__ __device__ inline int window_first_tile(int window, int p0, int tile) {
+    if (window <= 0) return 0;
+    const int lo = p0 - window + 1;
+    return lo > 0 ? lo / tile : 0;
+}
+
 // Byte offsets of every array inside the Assign workspace.  Computed on the
 // host from the problem (layout_for) and passed to every kernel by value.
 struct WsLayout {
@@ -65,6 +73,7 @@ struct WsLayout {
     // (its prefill map).  The other sequences get no units, or (decode mode)
     // units without query rows.
     int32_t cls, small_q;
+    int32_t window;   // sliding window (0 = none): the query at p sees keys p - window < j <= p
     int64_t off_err_header;   // header whose error word device faults go to
     int64_t off_header, off_cta_ptr, off_tasks, off_task_cta, off_units, off_ntiles,
         off_prefix, off_nsplit, off_slot0, off_task0, off_fix, off_active, off_cu_q,

@@ -70,7 +70,7 @@ class Workload:
     block_mask: Optional[torch.Tensor] = None   # uint8 [B, mask_q_tiles, mask_kv_tiles]
     mask_tile: int = 128
     mode: str = "decode"                  # which Assign mode the workload is run with
-    window: int = 0                       # sliding window (0 = none); oracle only so far
+    window: int = 0                       # sliding window (0 = none): keys p - window < j <= p
     meta: dict = field(default_factory=dict)
 
     @property
@@ -288,9 +288,12 @@ def decode_algorithmic_bytes(w: Workload) -> int:
     once, the FP8 scales of the pages touched, Q in, O out (bf16) and LSE out
     (fp32), and the block-table entries used."""
     ctx = [int(x) for x in w.context_lens]
+    ql = [int(x) for x in w.q_lens]
     e = 2 if w.kv_dtype == BF16 else 1
-    kv = sum(ctx) * w.num_kv_heads * w.head_dim * 2 * e
-    pages = sum((c + w.page_size - 1) // w.page_size for c in ctx)
+    # first key any query of the sequence sees (a sliding window starts it late)
+    lo = [max(0, c - q - w.window + 1) if w.window > 0 else 0 for c, q in zip(ctx, ql)]
+    kv = sum(c - a for c, a in zip(ctx, lo)) * w.num_kv_heads * w.head_dim * 2 * e
+    pages = sum((c + w.page_size - 1) // w.page_size - a // w.page_size for c, a in zip(ctx, lo))
     scales = pages * w.num_kv_heads * 2 * 4 if w.kv_dtype == FP8_E4M3 else 0
     rows = w.total_q * w.num_q_heads
     qo = rows * w.head_dim * 2 * 2 + rows * 4

@@ -84,6 +84,15 @@ def test_invalid_problems_rejected_on_host(lib):
     ok = B.PaProblem.from_buffer_copy(p)
     ok.max_q_len = 8                          # 32 rows: built
     assert B.pa_assign_workspace_size(ok, B.PA_MODE_DECODE) > 0
+    win = B.PaProblem.from_buffer_copy(p)
+    win.window = 100                          # sliding window: bf16 decode is built
+    assert B.pa_assign_workspace_size(win, B.PA_MODE_DECODE) > 0
+    assert B.pa_assign_workspace_size(win, B.PA_MODE_PREFILL) == 0   # not yet
+    win.kv_dtype = 1                          # E4M3 decode with a window: not yet
+    assert B.pa_assign_workspace_size(win, B.PA_MODE_DECODE) == 0
+    bad = B.PaProblem.from_buffer_copy(p)
+    bad.window = -1
+    assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0
     bad = B.PaProblem.from_buffer_copy(p)
     bad.mask_q_tiles, bad.mask_kv_tiles = 1, 1  # masks are prefill-only
     assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0

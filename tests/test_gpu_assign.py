@@ -27,7 +27,8 @@ def check(w, mode, num_ctas=0, balance_rows=0):
     assert B.pa_last_device_error(bufs.assign_ws) == 0
     if mode == B.PA_MODE_DECODE:
         tm = oracle.assign(mode, w.num_seqs, w.num_q_heads, w.num_kv_heads, N, 64,
-                           balance_rows or 128, w.context_lens, w.q_lens)
+                           balance_rows or 128, w.context_lens, w.q_lens,
+                           window=int(getattr(w, "window", 0)))
         task_map_equal(gpu, tm, with_active=False)
         return gpu
     # prefill mode: the prefill map and the decode part (its own CTA count: the
@@ -79,6 +80,13 @@ def test_weighted_map(rbal):
 
 def test_tiny_mixed_map():
     check(W.tiny_mixed(), B.PA_MODE_PREFILL, num_ctas=5)
+
+
+@pytest.mark.parametrize("window", [1, 100, 4096])
+def test_decode_map_with_sliding_window(window):
+    w = W.decode_bf16(mtp=2)
+    w.window = window
+    check(w, B.PA_MODE_DECODE)
 
 
 def test_bad_lengths_flagged():

@@ -107,6 +107,21 @@ def test_decode_fp8_q_len_4_full_size_sampled():
     run_and_compare(w, rows=rows)
 
 
+@pytest.mark.parametrize("window,ps,ql,D", [(1, 64, 1, 128), (64, 64, 2, 128), (100, 16, 3, 128),
+                                             (1000, 32, 4, 128), (5000, 64, 2, 128),
+                                             (300, 16, 2, 64)])
+def test_decode_sliding_window(window, ps, ql, D):
+    """Sliding window ("HiLS-Attention", 二.1 local branch): each query sees
+    the keys p - window < j <= p.  Windows shorter than a tile, a tile long,
+    across page boundaries, past some contexts; MTP rows whose windows start
+    at different keys; split units (19 CTAs)."""
+    ctx = [37, 700, 1500, 4096, 129, 9000]
+    w = W.make_workload(f"win{window}", ctx, [ql] * 6, num_q_heads=32, num_kv_heads=8,
+                        head_dim=D, page_size=ps, seed=window + ps + ql)
+    w.window = window
+    run_and_compare(w, num_ctas=19)
+
+
 def test_decode_is_deterministic():
     w = W.decode_bf16(mtp=3, shrink=8).to("cuda")
     a = B.run_decode(w)

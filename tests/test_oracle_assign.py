@@ -54,7 +54,7 @@ def test_worked_examples(oracle_mod, ex):
 
 # ------------------------------------------------------- brute force
 
-def brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask=None, mask_tile=128):
+def brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask=None, mask_tile=128, window=0):
     G = Hq // Hkv
     units = []
     for b in range(B):
@@ -70,6 +70,11 @@ def brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask=None, mask_tile=128)
     lists = []
     for (b, hk, q0, nq, L) in units:
         reach = list(range(-(-L // T)))
+        if window > 0:
+            # the unit's first query sits at ctx - ql + q0 and sees keys after
+            # p - window: keep the tiles whose last key reaches that far
+            first_key = ctx[b] - ql[b] + q0 - window + 1
+            reach = [t for t in reach if (t + 1) * T - 1 >= first_key]
         if mask is not None:
             reach = [t for t in reach if t < mask.shape[2] and mask[b, q0 // mask_tile, t]]
         lists.append(reach)
@@ -233,3 +238,36 @@ def test_prefill_split_absent_with_mask_or_wide_groups(oracle_mod):
     assert dec is None and sorted({int(u[0]) for u in pre.units}) == [0, 1, 2]
     pre, dec = oracle_mod.assign_prefill(3, 32, 1, 5, 128, ctx, ql)   # G = 32 > 16
     assert dec is None and sorted({int(u[0]) for u in pre.units}) == [0, 1, 2]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_window_maps_match_brute_force(oracle_mod, seed):
+    """Sliding window ("HiLS-Attention", 二.1 local branch; keys p - window < j
+    <= p): a unit's tiles start at the first one its first query can see."""
+    rng = np.random.default_rng(500 + seed)
+    mode = int(rng.integers(0, 2))
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    B = int(rng.integers(1, 7))
+    N = int(rng.integers(1, 20))
+    T = 64 if mode == 0 else 128
+    window = int(rng.choice([1, 17, 64, 100, 300, 5000]))
+    ctx, ql = [], []
+    for _ in range(B):
+        c = int(rng.integers(0, 900))
+        q = int(rng.integers(0, min(c, 4 if mode == 0 else 300) + 1))
+        ctx.append(c)
+        ql.append(q)
+    tm = oracle_mod.assign(mode, B, G * Hkv, Hkv, N, T, 128, np.array(ctx, np.int32),
+                           np.array(ql, np.int32), window=window)
+    bf = brute_force(mode, B, G * Hkv, Hkv, N, T, 128, ctx, ql, window=window)
+    assert tm.unit_ntiles.tolist() == [len(x) for x in bf["lists"]]
+    assert tm.tasks.tolist() == bf["tasks"]
+    assert tm.cta_ptr.tolist() == bf["cta_ptr"]
+    assert tm.unit_slot0.tolist() == bf["slot0"]
+    # a window as long as every context changes nothing
+    full = oracle_mod.assign(mode, B, G * Hkv, Hkv, N, T, 128, np.array(ctx, np.int32),
+                             np.array(ql, np.int32), window=max(ctx + [1]) + 1)
+    plain = oracle_mod.assign(mode, B, G * Hkv, Hkv, N, T, 128, np.array(ctx, np.int32),
+                              np.array(ql, np.int32))
+    assert full.tasks.tolist() == plain.tasks.tolist()
