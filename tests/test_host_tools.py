@@ -40,3 +40,20 @@ def test_launches_per_step():
     # decode part's Assign, kernel and Combine
     assert bench.launches_per_step(W.hybrid_bf16(shrink=16), B.PA_MODE_PREFILL) == 8
     assert bench.launches_per_step(W.prefill_bf16(sparse=True, shrink=32), B.PA_MODE_PREFILL) == 5
+
+
+def test_windowed_algorithmic_bytes():
+    """A window as long as every context changes nothing; a window of one
+    reads exactly each sequence's q_len newest keys (the queries' own)."""
+    w = W.decode_bf16(mtp=2, shrink=16)
+    full = W.decode_algorithmic_bytes(w)
+    w.window = int(w.context_lens.max()) + 5
+    assert W.decode_algorithmic_bytes(w) == full
+    w.window = 1
+    ql = [int(x) for x in w.q_lens]
+    ctx = [int(x) for x in w.context_lens]
+    kv = sum(ql) * w.num_kv_heads * w.head_dim * 2 * 2
+    pages = sum((c + w.page_size - 1) // w.page_size - (c - q) // w.page_size
+                for c, q in zip(ctx, ql))
+    rows = sum(ql) * w.num_q_heads
+    assert W.decode_algorithmic_bytes(w) == kv + rows * w.head_dim * 4 + rows * 4 + pages * 4
