@@ -140,15 +140,19 @@ PA_API const char* pa_status_string(int status);
 PA_API const char* pa_version(void);
 
 /* Persistent CTA count that pa_assign and the compute pass of `mode` use for
- * this problem on the current device (problem->num_ctas if non-zero).
- * *num_ctas: host out. */
+ * this problem on the current device (problem->num_ctas if non-zero).  In
+ * prefill mode this is the prefill kernel's; the decode part of a mixed batch
+ * uses pa_num_ctas(PA_MODE_DECODE) of the problem with max_q_len capped at
+ * 16 / G.  *num_ctas: host out. */
 PA_API pa_status pa_num_ctas(const pa_problem* problem, int mode, int32_t* num_ctas);
 
 /* Bytes of the Assign workspace for (problem, mode).  Its content (task map,
- * unit table, active-tile lists, error word) is private to the library. */
+ * unit table, active-tile lists, error word; in prefill mode without a block
+ * mask also the decode part's map) is private to the library. */
 PA_API size_t pa_assign_workspace_size(const pa_problem* problem, int mode);
 
-/* Bytes of the split-K partial workspace (fp32 O and LSE per split slot). */
+/* Bytes of the split-K partial workspace (fp32 O and LSE per split slot; in
+ * prefill mode without a block mask also the decode part's slots). */
 PA_API size_t pa_partial_workspace_size(const pa_problem* problem, int mode);
 
 /*
@@ -202,6 +206,7 @@ PA_API pa_status pa_decode_splitk(const pa_problem* problem, const void* q, cons
  * tasks: m = max_k lse_k, O = sum_k e^(lse_k - m) O_k / sum_k e^(lse_k - m),
  * lse = m + ln sum_k e^(lse_k - m).  Units with no visible key get O = 0,
  * lse = -inf.  Units written directly by the compute pass are not touched.
+ * In prefill mode both task maps of the workspace are finished.
  *   mode: the mode assign_ws was built with.
  */
 PA_API pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
