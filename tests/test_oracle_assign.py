@@ -271,3 +271,22 @@ def test_window_maps_match_brute_force(oracle_mod, seed):
     plain = oracle_mod.assign(mode, B, G * Hkv, Hkv, N, T, 128, np.array(ctx, np.int32),
                               np.array(ql, np.int32))
     assert full.tasks.tolist() == plain.tasks.tolist()
+
+
+def test_prefill_split_worked_example(oracle_mod):
+    """The two maps of a small mixed batch, worked by hand
+    (tests/golden/assign_prefill_split_example.json)."""
+    with open(os.path.join(GOLDEN, "assign_prefill_split_example.json")) as f:
+        ex = json.load(f)["example"]
+    pre, dec = oracle_mod.assign_prefill(ex["num_seqs"], ex["num_q_heads"], ex["num_kv_heads"],
+                                         ex["num_ctas"], ex["balance_rows"],
+                                         np.array(ex["context_lens"], np.int32),
+                                         np.array(ex["q_lens"], np.int32))
+    for tm, e in ((pre, ex["expect_prefill"]), (dec, ex["expect_decode"])):
+        assert tm.units.tolist() == e["units"]
+        assert tm.unit_ntiles.tolist() == e["unit_ntiles"]
+        assert tm.cta_ptr.tolist() == e["cta_ptr"]
+        assert tm.tasks.tolist() == e["tasks"]
+        assert tm.unit_nsplit.tolist() == e["unit_nsplit"]
+        assert tm.unit_slot0.tolist() == e["unit_slot0"]
+        assert tm.num_slots == e["num_slots"]
