@@ -29,7 +29,8 @@ def run_oracle(oracle_mod, ex):
     return oracle_mod.assign(ex["mode"], ex["num_seqs"], ex["num_q_heads"], ex["num_kv_heads"],
                              ex["num_ctas"], ex["kv_tile"], ex["balance_rows"],
                              np.array(ex["context_lens"], np.int32),
-                             np.array(ex["q_lens"], np.int32), bm)
+                             np.array(ex["q_lens"], np.int32), bm,
+                             window=ex.get("window", 0))
 
 
 def load_examples():
