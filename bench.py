@@ -1,13 +1,24 @@
 """Benchmark: paged-KV attention forward on GB300.
 
-Default workload: the dynamic bf16 decode batch (B=64, Hq=32, Hkv=8, D=128,
+Headline workload: the dynamic bf16 decode batch (B=64, Hq=32, Hkv=8, D=128,
 64-token pages, NHD, KV lengths log-uniform in [128, 32768], q_len = 1+MTP
 with MTP=1).  One step = Assign + split-K decode + Combine over the whole
 batch.  Metric: achieved HBM GB/s = algorithmic bytes (every visible K/V
-element once, Q in, O and LSE out, block-table entries) / step time.
+element once, Q in, O and LSE out, block-table entries) / step time; for the
+prefill workloads TFLOP/s = algorithmic FLOPs (4 * D * Hq per visible
+query-key pair) / step time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                  [--workload decode_bf16|decode_fp8|prefill_dense|prefill_sparse|hybrid]
+                  [--workload decode_bf16|decode_fp8|prefill_dense|prefill_sparse|hybrid|
+                              tiny_mixed]
+                  [--configs all|none]
+
+With no --workload (N = 1), the one JSON line also carries a "configs" object:
+every other workload of the metric (tiny mixed batch, bf16 decode with q_len
+3 and 4, E4M3 decode with q_len 3 and 4, dense and block-sparse prefill, the
+hybrid batch), each timed on the same contract (W warm-up steps, K timed
+steps, CUDA events on the launching stream) with its own roofline, clocks, CPU
+baseline and a parity check of sampled rows against the oracle leg's output.
 
 Under torchrun each rank processes its own independent batch (seed + rank)
 on its own GPU with no data-path collective (weak scaling); the barrier and
@@ -31,6 +42,20 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode attn achieved HBM GB/s; prefill attn TFLOP/s; both as % of GB300 roofline"
+WORKLOADS = ["decode_bf16", "decode_fp8", "prefill_dense", "prefill_sparse", "hybrid",
+             "tiny_mixed"]
+# the "configs" object of the default line: (key, workload, mtp)
+CONFIG_SET = [
+    ("tiny_mixed", "tiny_mixed", 0),
+    ("decode_bf16_mtp2", "decode_bf16", 2),
+    ("decode_bf16_mtp3", "decode_bf16", 3),
+    ("decode_fp8_mtp2", "decode_fp8", 2),
+    ("decode_fp8_mtp3", "decode_fp8", 3),
+    ("prefill_dense", "prefill_dense", 0),
+    ("prefill_sparse", "prefill_sparse", 0),
+    ("hybrid", "hybrid", 0),
+]
+PARALLELISM = "independent batch per GPU x{world}"
 
 
 def load_peaks():
@@ -63,17 +88,23 @@ def make_workload(name: str, rank: int, shrink: int = 1, mtp: int = 0):
         return W.prefill_bf16(sparse=True, seed=rank_seed(1004, rank), shrink=shrink)
     if name == "hybrid":
         return W.hybrid_bf16(seed=rank_seed(1005, rank), shrink=shrink)
+    if name == "tiny_mixed":
+        return W.tiny_mixed(seed=rank_seed(1001, rank))
     raise SystemExit(f"unknown workload {name}")
 
 
-def workload_config(w, name):
+def workload_config(w, name, world):
     cfg = {"workload": name, "batch": w.num_seqs, "num_q_heads": w.num_q_heads,
            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
            "layout": "NHD" if w.layout == 0 else "HND",
            "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
-           "total_q_tokens": w.total_q, "total_kv_tokens": int(w.context_lens.sum())}
+           "total_q_tokens": w.total_q, "total_kv_tokens": int(w.context_lens.sum()),
+           "l2": "inputs larger than L2" if w.meta.get("shrink", 1) == 1 and
+           name != "tiny_mixed" else "inputs smaller than L2 (launch-bound case)",
+           "parallelism": PARALLELISM.format(world=world)}
     if "mtp" in w.meta:
         cfg["mtp"] = w.meta["mtp"]
+        cfg["q_len"] = 1 + w.meta["mtp"]
     if w.window:
         cfg["window"] = w.window
     return cfg
@@ -83,9 +114,14 @@ def is_decode(name):
     return name.startswith("decode")
 
 
+def bytes_metric(name):
+    """Decode-shaped workloads report HBM GB/s, prefill ones TFLOP/s."""
+    return is_decode(name) or name in ("hybrid", "tiny_mixed")
+
+
 def work_of(w, name):
     from paged_attention_gb300 import workloads as W
-    if is_decode(name) or name == "hybrid":
+    if bytes_metric(name):
         return W.decode_algorithmic_bytes(w), "bytes"
     return W.prefill_algorithmic_flops(w), "flops"
 
@@ -97,14 +133,18 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, uuid=None):
+    def __init__(self, uuid=None, path=None):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.keep = path is not None
+        if path is None:
+            import tempfile
+            fd, path = tempfile.mkstemp(prefix="pa_clocks_", suffix=".csv")
+            os.close(fd)
+        self.path = path
         self.uuid = uuid
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
                    "-lms", "50"]
             if self.uuid:
@@ -123,6 +163,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
+        self.proc = None
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
@@ -138,6 +179,11 @@ class ClockSampler:
                 for n, v in zip(names, parts[5:9]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
@@ -146,53 +192,81 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_sample_rate(w, name, target_s):
-    """Time the fp64 oracle on the first sequences of the workload (all heads,
-    all new tokens) until about target_s seconds of work; returns
-    (value in the metric's unit, sample description, cores)."""
+def visible_keys_per_row(w, b, toks):
+    """Visible keys of query tokens `toks` (local indices) of sequence b, per
+    q head: causal (bottom-right), sliding window, block mask."""
+    c, q = int(w.context_lens[b]), int(w.q_lens[b])
+    toks = np.asarray(toks, dtype=np.int64)
+    p = c - q + toks                                   # absolute positions
+    hi = np.minimum(p, c - 1)
+    lo = np.maximum(0, p - w.window + 1) if w.window > 0 else np.zeros_like(p)
+    if w.block_mask is None:
+        return np.clip(hi - lo + 1, 0, None)
+    T = w.mask_tile
+    m = w.block_mask[b].numpy().astype(np.int64)
+    mq = toks // T
+    out = np.zeros_like(p)
+    for kt in range(min(m.shape[1], c // T + 1)):
+        a = np.maximum(lo, kt * T)
+        e = np.minimum(hi, kt * T + T - 1)
+        keep = np.where(mq < m.shape[0], m[np.minimum(mq, m.shape[0] - 1), kt], 0)
+        out += np.clip(e - a + 1, 0, None) * keep
+    return out
+
+
+def oracle_sample(w, name, target_s, keep_first=True):
+    """Time the fp64 oracle, as it stands, on the workload's sequences in order
+    (every row of a decode sequence; at most 4096 evenly spaced rows of a long
+    prefill chunk), walking the batch again if it runs out, until about
+    target_s seconds of work.  Returns a dict with the value in the metric's
+    unit, the sample description, the threads used, and (keep_first) the rows
+    and oracle outputs of the first walk over the batch, for a parity check."""
     import oracle
-    from paged_attention_gb300 import workloads as W
     oracle.build()
     cores = oracle.max_threads()
-    Hq = w.num_q_heads
+    Hq, D = w.num_q_heads, w.head_dim
     ql = [int(x) for x in w.q_lens]
-    cu = np.concatenate([[0], np.cumsum(ql)])
-    done_rows = 0
-    runs = 0          # sequence runs; the batch is walked again when it runs out
-    t_total = 0.0
-    work = 0
-    n = w.num_seqs
-    decode_like = is_decode(name) or name == "hybrid"
+    cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int64)
+    kind = "bytes" if bytes_metric(name) else "flops"
+    e = 2 if w.kv_dtype == 0 else 1
+    done_rows, runs, t_total, work, n = 0, 0, 0.0, 0.0, w.num_seqs
+    first = []
     while runs < 100 * n and (runs == 0 or t_total < target_s):
         b = runs % n
-        rows = np.arange(cu[b] * Hq, cu[b + 1] * Hq, dtype=np.int64)
-        if not decode_like and len(rows) > 4096:
-            rows = rows[:: max(1, len(rows) // 4096)]
-        t0 = time.perf_counter()
-        oracle.attention(w, rows=rows)
-        t_total += time.perf_counter() - t0
-        done_rows += len(rows)
-        c = int(w.context_lens[b])
-        if decode_like:
-            e = 2 if w.kv_dtype == 0 else 1
-            work += c * w.num_kv_heads * w.head_dim * 2 * e + ql[b] * Hq * (w.head_dim * 4 + 4)
-        else:
-            frac = len(rows) / (ql[b] * Hq)
-            pairs = ql[b] * (c - ql[b]) + ql[b] * (ql[b] + 1) // 2
-            work += int(4 * w.head_dim * Hq * pairs * frac)
         runs += 1
-    if decode_like:
-        value = work / t_total / 1e9
-        unit = "GB/s"
-    else:
-        value = work / t_total / 1e12
-        unit = "TFLOP/s"
-    if runs <= n:
-        what = f"sequences 0..{runs - 1} of the workload"
-    else:
-        what = f"the whole batch ({n} sequences) {runs / n:.1f} times over"
-    sample = f"oracle on {what} ({done_rows} query rows, {t_total:.1f} s)"
-    return value, unit, sample, cores, t_total
+        if ql[b] == 0:
+            continue
+        toks = np.arange(ql[b], dtype=np.int64)
+        nrows = ql[b] * Hq
+        if nrows > 4096:
+            toks = toks[:: max(1, nrows // 4096)]
+        rows = ((cu[b] + toks)[:, None] * Hq + np.arange(Hq)[None, :]).reshape(-1)
+        t0 = time.perf_counter()
+        ref_o, ref_l = oracle.attention(w, rows=rows)
+        t_total += time.perf_counter() - t0
+        if keep_first and runs <= n:
+            first.append((rows, ref_o, ref_l))
+        done_rows += len(rows)
+        vis = visible_keys_per_row(w, b, toks)
+        if kind == "bytes":
+            # the sequence's algorithmic bytes, scaled by the fraction of its rows computed
+            lo = max(0, int(w.context_lens[b]) - ql[b] - w.window + 1) if w.window > 0 else 0
+            c = int(w.context_lens[b])
+            pages = (c + w.page_size - 1) // w.page_size - lo // w.page_size
+            seq = ((c - lo) * w.num_kv_heads * D * 2 * e + ql[b] * Hq * (D * 4 + 4) + pages * 4
+                   + (pages * w.num_kv_heads * 8 if w.kv_dtype == 1 else 0))
+            work += seq * len(rows) / nrows
+        else:
+            work += 4.0 * D * Hq * float(vis.sum())
+    value = work / max(t_total, 1e-9) / (1e9 if kind == "bytes" else 1e12)
+    unit = "GB/s" if kind == "bytes" else "TFLOP/s"
+    what = (f"sequences 0..{runs - 1} of the workload" if runs <= n else
+            f"the whole batch ({n} sequences) {runs / n:.1f} times over")
+    if first:
+        first = tuple(np.concatenate([f[i] for f in first]) for i in range(3))
+    return {"value": value, "unit": unit, "cores": cores, "seconds": t_total,
+            "sample": f"oracle on {what} ({done_rows} query rows, {t_total:.1f} s)",
+            "first": first or None}
 
 
 # ------------------------------------------------------------------ native
@@ -205,32 +279,36 @@ def launches_per_step(w, mode):
     return 5 + (3 if w.block_mask is None and G <= 16 else 0)
 
 
-def run_native(args, rank, world, dist):
-    import torch
-    from paged_attention_gb300 import binding as B
-    from paged_attention_gb300 import build as build_mod
-    build_mod.build()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    name = args.workload
-    w_cpu = make_workload(name, rank, args.shrink, args.mtp)
-    if args.window:
-        if not is_decode(name) or w_cpu.kv_dtype != 0:
-            raise SystemExit("--window: bf16 decode workloads only")
-        w_cpu.window = args.window
-    w = w_cpu.to(dev)
-    work, kind = work_of(w_cpu, name)
-    mode = B.PA_MODE_DECODE if is_decode(name) else B.PA_MODE_PREFILL
-    bufs = B.make_buffers(w, mode)
-    stream = torch.cuda.current_stream()
-    runner = B.run_decode if mode == B.PA_MODE_DECODE else B.run_prefill
+class Case:
+    """One workload on the device: its buffers, one step of the hot path
+    (Assign + compute + Combine), and the timed loops."""
 
-    def step(ev=None):
-        p = bufs.problem
+    def __init__(self, name, mtp, rank, shrink, window, dev):
+        import torch
+        from paged_attention_gb300 import binding as B
+        self.B = B
+        self.name = name
+        self.w_cpu = make_workload(name, rank, shrink, mtp)
+        if window:
+            if not is_decode(name):
+                raise SystemExit("--window: decode workloads only")
+            self.w_cpu.window = window
+        self.w = self.w_cpu.to(dev)
+        self.work, self.kind = work_of(self.w_cpu, name)
+        self.mode = B.PA_MODE_DECODE if is_decode(name) else B.PA_MODE_PREFILL
+        self.bufs = B.make_buffers(self.w, self.mode)
+        self.stream = torch.cuda.current_stream()
+        self.runner = B.run_decode if self.mode == B.PA_MODE_DECODE else B.run_prefill
+
+    def step(self, ev=None, w=None, bufs=None):
+        B = self.B
+        w = w or self.w
+        bufs = bufs or self.bufs
+        p, mode = bufs.problem, self.mode
         B.pa_assign(p, mode, w.context_lens, w.q_lens,
                     w.block_mask if mode == B.PA_MODE_PREFILL else None, bufs.assign_ws)
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(self.stream)
         if mode == B.PA_MODE_DECODE:
             B.pa_decode_splitk(p, w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens,
                                w.q_lens, w.k_scale, w.v_scale, bufs.assign_ws, bufs.partial_ws,
@@ -240,53 +318,119 @@ def run_native(args, rank, world, dist):
                          w.k_scale, w.v_scale, w.block_mask, bufs.assign_ws, bufs.partial_ws,
                          bufs.out, bufs.lse)
         if ev is not None:
-            ev[1].record(stream)
+            ev[1].record(self.stream)
         B.pa_combine(p, mode, bufs.assign_ws, bufs.partial_ws, bufs.out, bufs.lse)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if B.pa_last_device_error(bufs.assign_ws) != 0:
-        raise SystemExit("device error during warm-up")
+    def device_error(self):
+        return self.B.pa_last_device_error(self.bufs.assign_ws)
 
-    uuid = None
+    def timed(self, args, dist, uuid):
+        """W warm-up steps, then exactly K steps bracketed by a barrier and a
+        synchronize (the step as a user runs it: nothing recorded between its
+        launches), then K steps with events around the compute call (the
+        kernel's own time, for the roofline).  Clocks are sampled from an
+        untimed soak of about 0.3 s before the timed region to its end."""
+        import torch
+        for _ in range(args.warmup):
+            self.step()
+        torch.cuda.synchronize()
+        if self.device_error() != 0:
+            raise SystemExit(f"{self.name}: device error during warm-up")
+        clocks = ClockSampler(uuid)
+        clocks.start()
+        t_end = time.perf_counter() + 0.3
+        while time.perf_counter() < t_end:
+            self.step()
+            torch.cuda.synchronize()
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0.record(self.stream)
+        for _ in range(args.steps):
+            self.step()
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        ms = t0.elapsed_time(t1) / args.steps
+        for i in range(args.steps):
+            self.step(kev[i])
+        torch.cuda.synchronize()
+        kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+        clk = clocks.stop()
+        if self.device_error() != 0:
+            raise SystemExit(f"{self.name}: device error during the timed region")
+        return ms, kern_ms, clk
+
+    def rate(self, ms, world=1):
+        scale = 1e9 if self.kind == "bytes" else 1e12
+        return self.work * world / (ms * 1e-3) / scale
+
+    def unit(self):
+        return "GB/s" if self.kind == "bytes" else "TFLOP/s"
+
+    def roofline(self, kern_ms, peaks):
+        achieved = self.rate(kern_ms)
+        if self.kind == "bytes":
+            roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+        else:
+            pk = peaks["bf16_tflops"]
+            roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
+                    "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
+                    "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+        roof["peak_source"] = peaks["source"]
+        roof["kernel"] = "pa_decode_splitk" if self.mode == self.B.PA_MODE_DECODE else "pa_prefill"
+        roof["kernel_ms"] = round(kern_ms, 4)
+        roof["algorithmic_" + self.kind + "_per_launch"] = int(self.work)
+        roof["traffic"] = load_traffic(roof["kernel"], self.name,
+                                       self.w_cpu.meta.get("mtp"))
+        return roof
+
+    def parity(self, first):
+        """Sampled rows of the last timed step's output against the oracle
+        leg's output for the same rows."""
+        import torch
+        if first is None:
+            return None
+        rows, ref_o, ref_l = first
+        idx = torch.as_tensor(rows, device=self.bufs.out.device)
+        o = self.bufs.out.reshape(-1, self.w.head_dim).index_select(0, idx).float().cpu().numpy()
+        lg = self.bufs.lse.reshape(-1).index_select(0, idx).cpu().numpy().astype(np.float64)
+        fin = np.isfinite(ref_l)
+        tol = 6e-2 if self.w.kv_dtype == 1 else 2e-2
+        err_o = float(np.abs(o - ref_o).max()) if o.size else 0.0
+        err_l = float(np.abs(lg[fin] - ref_l[fin]).max()) if fin.any() else 0.0
+        ok = bool(np.isfinite(o).all() and np.array_equal(np.isfinite(lg), fin)
+                  and err_o <= tol and err_l <= 1e-3)
+        return {"rows": int(len(rows)), "max_abs_out": round(err_o, 6),
+                "max_abs_lse": round(err_l, 7), "tol_out": tol, "tol_lse": 1e-3, "ok": ok}
+
+
+def gpu_uuid(dev):
+    import torch
     try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
-        uuid = None
-    clocks = ClockSampler(uuid)
-    clocks.start()
-    time.sleep(0.3)
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    # the step as a user runs it: nothing between the launches (events recorded
-    # between kernels would keep the dependent launches from overlapping)
-    t0.record(stream)
-    for i in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    ms = t0.elapsed_time(t1) / args.steps
-    # the compute kernel alone, bracketed by events, for the roofline
-    for i in range(args.steps):
-        step(kev[i])
-    torch.cuda.synchronize()
-    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+        return None
 
-    # end-to-end through the public API: every step copies its inputs from
-    # pinned host memory (Q, block table, lengths; the KV cache is resident
-    # state), runs Assign + compute + Combine, and reads its outputs (O, LSE)
-    # back to pinned host memory.  As in a serving loop, the copies run on
-    # their own streams with two sets of device buffers, so step k+1's upload
-    # and step k-1's read-back overlap step k's compute.
+
+def e2e_measure(case, args, dist, dev):
+    """The same metric through the public C-ABI calls, with each step's
+    inputs copied from pinned host memory (Q, block table, lengths; the K/V
+    cache is resident state) and its outputs (O, LSE) read back to pinned host
+    memory.  As in a serving loop, uploads and read-backs run on their own
+    streams with two sets of device buffers, so step k+1's upload and step
+    k-1's read-back overlap step k's compute.  Also the serial latency of one
+    step with its copies (upload, compute, read-back, synchronize)."""
     import copy
+    import torch
+    B = case.B
+    w, w_cpu, stream = case.w, case.w_cpu, case.stream
     hq = w_cpu.q.pin_memory()
     hbt = w_cpu.block_table.pin_memory()
     hctx = w_cpu.context_lens.pin_memory()
@@ -300,7 +444,7 @@ def run_native(args, rank, world, dist):
             wk.block_table = torch.empty_like(w.block_table)
             wk.context_lens = torch.empty_like(w.context_lens)
             wk.q_lens = torch.empty_like(w.q_lens)
-        bk = bufs if k == 0 else B.make_buffers(w, mode)
+        bk = case.bufs if k == 0 else B.make_buffers(w, case.mode)
         hout = torch.empty(bk.out.shape, dtype=bk.out.dtype).pin_memory()
         hlse = torch.empty(bk.lse.shape, dtype=bk.lse.dtype).pin_memory()
         sets.append((wk, bk, hout, hlse))
@@ -324,7 +468,7 @@ def run_native(args, rank, world, dist):
             ev_in[k].record(up)
         stream.wait_event(ev_in[k])
         stream.wait_event(ev_out[k])           # step i-2's outputs have been read back
-        runner(wk, bk)
+        case.runner(wk, bk)
         ev_done[k].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(ev_done[k])
@@ -350,96 +494,138 @@ def run_native(args, rank, world, dist):
     for wk, bk, hout, hlse in sets:
         if B.pa_last_device_error(bk.assign_ws) != 0:
             raise SystemExit("device error during the end-to-end run")
+    ref = case.bufs.out.cpu()
     for wk, bk, hout, hlse in sets:
-        if not torch.equal(hout, bufs.out.cpu()):
+        if not torch.equal(hout, ref):
             raise SystemExit("end-to-end outputs differ from the device-timed run")
-    # the same device-resident step captured once in a CUDA graph and replayed
-    # (the launch chain without host launch overhead)
-    graph = None
+    # serial: one step at a time, copies not overlapped with anything
+    wk, bk, hout, hlse = sets[1]
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(args.steps):
+        wk.q.copy_(hq, non_blocking=True)
+        wk.block_table.copy_(hbt, non_blocking=True)
+        wk.context_lens.copy_(hctx, non_blocking=True)
+        wk.q_lens.copy_(hql, non_blocking=True)
+        case.runner(wk, bk)
+        hout.copy_(bk.out, non_blocking=True)
+        hlse.copy_(bk.lse, non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = s0.elapsed_time(s1) / args.steps
+    return e2e_ms, serial_ms, h2d, d2h
+
+
+def graph_measure(case, args, dev):
+    """The device-resident step captured once in a CUDA graph and replayed."""
+    import torch
     try:
         gs = torch.cuda.Stream(dev)
-        gs.wait_stream(stream)
+        gs.wait_stream(case.stream)
         with torch.cuda.stream(gs):
-            step()   # warm on the capture stream
+            case.step()   # warm on the capture stream
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=gs):
-            step()
+            case.step()
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
+        g0.record(case.stream)
         for _ in range(args.steps):
             g.replay()
-        g1.record(stream)
+        g1.record(case.stream)
         torch.cuda.synchronize()
         graph_ms = g0.elapsed_time(g1) / args.steps
-        graph = {"ms_per_step": round(graph_ms, 4), "value": None}
+        return {"ms_per_step": round(graph_ms, 4), "value": round(case.rate(graph_ms), 2)}
     except Exception as exc:   # report, do not fail the bench line
-        graph = {"unavailable": f"{type(exc).__name__}: {str(exc)[:120]}"}
-    clk = clocks.stop()
+        return {"unavailable": f"{type(exc).__name__}: {str(exc)[:120]}"}
+
+
+def config_entry(key, name, mtp, args, dev, peaks, uuid):
+    """One entry of the "configs" object (N = 1 only)."""
+    import torch
+    case = Case(name, mtp, 0, 1, 0, dev)
+    ms, kern_ms, clk = case.timed(args, None, uuid)
+    entry = {"workload": name, "value": round(case.rate(ms), 2), "unit": case.unit(),
+             "ms_per_step": round(ms, 4), "kernel_ms": round(kern_ms, 4),
+             "roofline": case.roofline(kern_ms, peaks), "clocks": clk,
+             "gpu_launches": launches_per_step(case.w_cpu, case.mode) * args.steps,
+             "config": workload_config(case.w_cpu, name, 1)}
+    if name == "tiny_mixed":
+        entry["note"] = "launch-bound: parity workload, time reported only"
+    if not args.no_cpu_baseline:
+        s = oracle_sample(case.w_cpu, name, args.config_cpu_seconds)
+        entry["cpu_baseline"] = {"value": round(s["value"], 4), "unit": s["unit"],
+                                 "cores": s["cores"], "kind": "oracle", "sample": s["sample"]}
+        entry["parity"] = case.parity(s["first"])
+    del case
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_native(args, rank, world, dist):
+    import torch
+    from paged_attention_gb300 import build as build_mod
+    build_mod.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    uuid = gpu_uuid(dev)
+    peaks = load_peaks()
+    name = args.workload or "decode_bf16"
+    case = Case(name, args.mtp, rank, args.shrink, args.window, dev)
+    ms, kern_ms, clk = case.timed(args, dist, uuid)
+    e2e_ms, serial_ms, h2d, d2h = e2e_measure(case, args, dist, dev)
+    graph = graph_measure(case, args, dev)
     if dist is not None:
         from paged_attention_gb300.dist import max_over_ranks
-        ms, e2e_ms, kern_ms = max_over_ranks([ms, e2e_ms, kern_ms])
-    if B.pa_last_device_error(bufs.assign_ws) != 0:
-        raise SystemExit("device error during the timed region")
-
-    peaks = load_peaks()
-    if kind == "bytes":
-        value = work * world / (ms * 1e-3) / 1e9
-        unit = "GB/s"
-        e2e_val = work * world / (e2e_ms * 1e-3) / 1e9
-        achieved = work / (kern_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "peak_source": peaks["source"]}
-    else:
-        value = work * world / (ms * 1e-3) / 1e12
-        unit = "TFLOP/s"
-        e2e_val = work * world / (e2e_ms * 1e-3) / 1e12
-        achieved = work / (kern_ms * 1e-3) / 1e12
-        pk = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
-                "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
-                "peak_source": peaks["source"]}
-    if graph is not None and "ms_per_step" in graph:
-        scale = 1e9 if kind == "bytes" else 1e12
-        graph["value"] = round(work * world / (graph["ms_per_step"] * 1e-3) / scale, 2)
-    roof["kernel"] = "pa_decode_splitk" if mode == B.PA_MODE_DECODE else "pa_prefill"
-    roof["kernel_ms"] = round(kern_ms, 4)
-    roof["traffic"] = load_traffic(roof["kernel"], name)
-
+        ms, e2e_ms, kern_ms, serial_ms = max_over_ranks([ms, e2e_ms, kern_ms, serial_ms])
+    unit = case.unit()
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.kv_dtype == 0 else "e4m3-kv/bf16",
+        "metric": METRIC, "value": round(case.rate(ms, world), 2), "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if case.w.kv_dtype == 0 else "e4m3-kv/bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, paged, NaN decoy pages)",
-        "config": dict(workload_config(w_cpu, name),
-                       l2="inputs larger than L2" if args.shrink == 1 else f"shrink {args.shrink}",
-                       parallelism=f"independent batch per GPU x{world}"),
-        "e2e": {"value": round(e2e_val, 2), "unit": unit, "ms_per_step": round(e2e_ms, 4),
+        "config": workload_config(case.w_cpu, name, world),
+        "e2e": {"value": round(case.rate(e2e_ms, world), 2), "unit": unit,
+                "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "overlap": "uploads and read-backs on their own streams, two buffer sets"},
-        "roofline": roof,
+                "overlap": "uploads and read-backs on their own streams, two buffer sets",
+                "serial_ms_per_step": round(serial_ms, 4),
+                "serial_value": round(case.rate(serial_ms, world), 2)},
+        "roofline": case.roofline(kern_ms, peaks),
         # decode mode: Assign, compute, Combine.  Prefill mode: Assign (3) +
         # prefill kernel + Combine, and without a block mask (G <= 16) the
         # decode part too: its Assign, the decode kernel and its Combine
-        "gpu_launches": launches_per_step(w_cpu, mode) * args.steps,
+        "gpu_launches": launches_per_step(case.w_cpu, case.mode) * args.steps,
         "clocks": clk,
         "graph": graph,
     }
+    first = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, u, sample, cores, _ = oracle_sample_rate(w_cpu, name, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": u, "cores": cores,
-                                "kind": "oracle", "sample": sample}
+        s = oracle_sample(case.w_cpu, name, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(s["value"], 4), "unit": s["unit"],
+                                "cores": s["cores"], "kind": "oracle", "sample": s["sample"]}
+        first = s["first"]
+        line["parity"] = case.parity(first)
+    del case
+    torch.cuda.empty_cache()
+    want_configs = args.configs == "all" or (args.configs is None and args.workload is None)
+    if world == 1 and want_configs:
+        configs = {}
+        for key, wname, mtp in CONFIG_SET:
+            configs[key] = config_entry(key, wname, mtp, args, dev, peaks, uuid)
+        line["configs"] = configs
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def load_traffic(kernel, workload):
+def load_traffic(kernel, workload, mtp=None):
     """DRAM bytes per launch from the committed ncu summary, if it matches the
     current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -449,7 +635,12 @@ def load_traffic(kernel, workload):
         with open(path) as f:
             d = json.load(f)
         from paged_attention_gb300 import build as build_mod
-        entry = d.get(f"{kernel}:{workload}")
+        entry = d.get(f"{kernel}:{workload}" + (f":mtp{mtp}" if mtp is not None else ""))
+        if entry is None:
+            entry = d.get(f"{kernel}:{workload}")
+            # an entry without a q_len is the workload's default q_len only
+            if entry is not None and mtp is not None and entry.get("mtp", mtp) != mtp:
+                entry = None
         if not entry or entry.get("source_hash") != build_mod.kernel_fingerprint(kernel):
             return None
         return entry.get("dram_bytes_per_launch")
@@ -462,30 +653,27 @@ def load_traffic(kernel, workload):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    name = args.workload
+    name = args.workload or "decode_bf16"
     w = make_workload(name, 0, 1, args.mtp)
     if args.window:
         w.window = args.window
     per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     vals = []
-    sample = ""
-    cores = 1
-    unit = "GB/s"
+    s = None
     for i in range(args.warmup + args.steps):
-        v, unit, sample, cores, t = oracle_sample_rate(w, name, per_step)
+        s = oracle_sample(w, name, per_step, keep_first=False)
         if i >= args.warmup:
-            vals.append(v)
+            vals.append(s["value"])
     value = statistics.median(vals)
     line = {
-        "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 4), "unit": s["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": dict(workload_config(w, name), l2="inputs larger than L2",
-                       parallelism="host cores"),
-        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": cores,
-                         "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,
+        "config": workload_config(w, name, world),
+        "cpu_baseline": {"value": round(value, 4), "unit": s["unit"], "cores": s["cores"],
+                         "kind": "oracle", "sample": s["sample"]},
+        "e2e": {"value": round(value, 4), "unit": s["unit"], "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -497,10 +685,14 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="decode_bf16",
-                    choices=["decode_bf16", "decode_fp8", "prefill_dense", "prefill_sparse",
-                             "hybrid"])
+    ap.add_argument("--workload", default=None, choices=WORKLOADS,
+                    help="headline workload (default decode_bf16); giving one skips the "
+                         "configs object unless --configs all")
+    ap.add_argument("--configs", default=None, choices=["all", "none"],
+                    help="time every other workload into a configs object (default: all "
+                         "when no --workload is given; N = 1 only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--config-cpu-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window (bf16 decode workloads): keys p - window < j <= p")

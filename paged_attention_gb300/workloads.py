@@ -95,15 +95,36 @@ class Workload:
         return Workload(**kw)
 
 
-def _randn_bf16(shape, g: torch.Generator, chunk: int = 1 << 26) -> torch.Tensor:
-    """N(0,1) rounded to bf16, drawn in chunks to bound host memory."""
+_RANDN_CHUNK = 1 << 24
+
+
+def _randn_bf16(shape, g: torch.Generator, chunk: int = _RANDN_CHUNK) -> torch.Tensor:
+    """N(0,1) rounded to bf16.  One 63-bit base seed is drawn from ``g``; chunk
+    c of the flat tensor comes from its own generator seeded with
+    base + c, so the chunks can be drawn on several host threads and the bytes
+    depend only on (g's state, shape), not on the thread count."""
     n = 1
     for s in shape:
         n *= int(s)
     out = torch.empty(n, dtype=torch.bfloat16)
-    for s in range(0, n, chunk):
+    base = int(torch.randint(0, 1 << 62, (1,), generator=g, dtype=torch.int64))
+    starts = list(range(0, n, chunk))
+
+    def fill(ci):
+        s = starts[ci]
         e = min(n, s + chunk)
-        out[s:e] = torch.randn(e - s, generator=g, dtype=torch.float32).to(torch.bfloat16)
+        gc = torch.Generator().manual_seed(base + ci)
+        out[s:e] = torch.randn(e - s, generator=gc, dtype=torch.float32).to(torch.bfloat16)
+
+    if len(starts) <= 1:
+        for ci in range(len(starts)):
+            fill(ci)
+    else:
+        import concurrent.futures as cf
+        import os
+        workers = max(1, min(len(starts), os.cpu_count() or 1, 32))
+        with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(fill, range(len(starts))))
     return out.view(*shape)
 
 
@@ -147,7 +168,7 @@ def make_workload(name: str, context_lens: List[int], q_lens: List[int], *, num_
         k_cache = _randn_bf16(shape, g)
         v_cache = _randn_bf16(shape, g)
     else:
-        def quant(x: torch.Tensor):
+        def quant_block(x: torch.Tensor):
             # per (page, kv head) scale: amax / 448, then round-to-nearest E4M3
             xf = x.float()
             if layout == NHD:
@@ -159,7 +180,27 @@ def make_workload(name: str, context_lens: List[int], q_lens: List[int], *, num_
                 sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
                 y = xf / sc[:, :, None, None]
             y = y.clamp(-E4M3_MAX, E4M3_MAX)
-            return y.to(torch.float8_e4m3fn).view(torch.uint8), sc.float().contiguous()
+            return y.to(torch.float8_e4m3fn).view(torch.uint8), sc.float()
+
+        def quant(x: torch.Tensor):
+            # pages are independent: quantise blocks of pages on host threads
+            import concurrent.futures as cf
+            import os
+            q8 = torch.empty(x.shape, dtype=torch.uint8)
+            sc = torch.empty((x.shape[0], Hkv), dtype=torch.float32)
+            step = 256
+
+            def one(p0):
+                a, s_ = quant_block(x[p0:p0 + step])
+                q8[p0:p0 + step] = a
+                sc[p0:p0 + step] = s_
+
+            starts = list(range(0, x.shape[0], step))
+            with cf.ThreadPoolExecutor(max_workers=max(1, min(len(starts), os.cpu_count() or 1,
+                                                               32))) as ex:
+                list(ex.map(one, starts))
+            return q8, sc.contiguous()
+
         k_cache, k_scale = quant(_randn_bf16(shape, g))
         v_cache, v_scale = quant(_randn_bf16(shape, g))
 

@@ -57,3 +57,29 @@ def test_windowed_algorithmic_bytes():
                 for c, q in zip(ctx, ql))
     rows = sum(ql) * w.num_q_heads
     assert W.decode_algorithmic_bytes(w) == kv + rows * w.head_dim * 4 + rows * 4 + pages * 4
+
+
+@pytest.mark.parametrize("make", [
+    lambda: W.prefill_bf16(sparse=True, shrink=16),
+    lambda: W.prefill_bf16(sparse=False, shrink=16),
+    lambda: W.hybrid_bf16(shrink=16),
+])
+def test_bench_per_row_visible_keys_sum_to_the_workload_pairs(make):
+    """The bench's CPU-baseline accounting (visible keys per sampled row) adds
+    up, over every row, to the FLOP accounting of the workload itself."""
+    import bench
+    w = make()
+    total = 0
+    for b in range(w.num_seqs):
+        total += int(bench.visible_keys_per_row(w, b, range(int(w.q_lens[b]))).sum())
+    assert total == W.visible_pairs(w)
+
+
+def test_bench_windowed_visible_keys():
+    import bench
+    w = W.make_workload("win", [100, 37, 500], [3, 1, 2], num_q_heads=4, num_kv_heads=2,
+                        head_dim=64, page_size=16, seed=3)
+    w.window = 50
+    got = [bench.visible_keys_per_row(w, b, range(int(w.q_lens[b]))).tolist()
+           for b in range(w.num_seqs)]
+    assert got == [[50, 50, 50], [37], [50, 50]]
