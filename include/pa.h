@@ -128,9 +128,8 @@ typedef struct pa_problem {
     float sm_scale;            /* softmax scale applied to q.k; finite and >= 0      */
     int32_t window;            /* sliding window ("HiLS-Attention", 二.1 local
                                   branch): 0 = none, else the query at position p
-                                  sees only the keys p - window < j <= p.  Decode
-                                  mode with bf16 K/V only so far; elsewhere
-                                  PA_ERR_UNSUPPORTED.  Negative: invalid.       */
+                                  sees only the keys p - window < j <= p.  Both
+                                  modes, bf16 and E4M3 K/V.  Negative: invalid. */
 } pa_problem;
 
 /* Human-readable name of a pa_status or PA_DEV_* code set. */
@@ -241,7 +240,9 @@ PA_API pa_status pa_combine(const pa_problem* problem, int mode, const void* ass
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it.  Make that
- * first call on every device before any stream capture starts.
+ * first call on every device before any stream capture starts.  The cached
+ * address belongs to the device's current context: after cudaDeviceReset on a
+ * device this entry point must not be called there again in the same process.
  *
  * Sharing: all calls on one device use the same array.  Two calls that may
  * run at the same time on one device (different streams without ordering,
@@ -269,8 +270,9 @@ PA_API pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, con
  * KV head, persistent fixed grid).  Walks the task map of
  * pa_assign(PA_MODE_PREFILL) with 256-row GQA-packed q tiles and 128-token KV
  * tiles on the tcgen05 tensor cores (accumulators in tensor memory).
- * Arguments as pa_decode_splitk, plus block_mask (the one given to pa_assign,
- * or NULL).  In a batch without a block mask, the sequences with
+ * Arguments as pa_decode_splitk, plus block_mask: the mask given to pa_assign,
+ * non-NULL exactly when problem->mask_q_tiles > 0 (else PA_ERR_INVALID_ARG);
+ * the kernels follow the active-tile lists pa_assign built from it.  In a batch without a block mask, the sequences with
  * 1 <= G*q_lens[b] <= 16 (the decode steps of a mixed chunked-prefill + decode
  * batch) run first, on the decode kernel of pa_decode_splitk over their own
  * task map: such a unit would fill a few of the 128 rows of a tensor-core

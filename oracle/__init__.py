@@ -251,7 +251,7 @@ MIXED_DECODE_ROWS = 16
 
 
 def assign_prefill(num_seqs, num_q_heads, num_kv_heads, num_ctas, balance_rows,
-                   context_lens, q_lens, block_mask=None, decode_ctas=None):
+                   context_lens, q_lens, block_mask=None, decode_ctas=None, window=0):
     """Prefill-mode Assign as pa_assign(PA_MODE_PREFILL) defines it.
 
     Returns (prefill_map, decode_map).  Each map is the plain Assign over the
@@ -259,17 +259,18 @@ def assign_prefill(num_seqs, num_q_heads, num_kv_heads, num_ctas, balance_rows,
     prefill units, and its decode units hold no query and no tile.  decode_map
     is None when the batch has a block mask or G > MIXED_DECODE_ROWS (every
     sequence then stays in the prefill map).  decode_ctas: the decode map's CTA
-    count (default num_ctas)."""
+    count (default num_ctas).  window: the sliding window, passed to both maps
+    (a unit's tiles start at the first one its first query can see)."""
     G = num_q_heads // num_kv_heads
     ql = [int(x) for x in q_lens]
     if block_mask is not None or G > MIXED_DECODE_ROWS:
         return assign(1, num_seqs, num_q_heads, num_kv_heads, num_ctas, 128, balance_rows,
-                      context_lens, ql, block_mask), None
+                      context_lens, ql, block_mask, window=window), None
     small_q = MIXED_DECODE_ROWS // G
     ql_pre = [q if q > small_q else 0 for q in ql]
     ql_dec = [q if q <= small_q else 0 for q in ql]
     pre = assign(1, num_seqs, num_q_heads, num_kv_heads, num_ctas, 128, balance_rows,
-                 context_lens, ql_pre)
+                 context_lens, ql_pre, window=window)
     dec = assign(0, num_seqs, num_q_heads, num_kv_heads, decode_ctas or num_ctas, 64,
-                 balance_rows, context_lens, ql_dec)
+                 balance_rows, context_lens, ql_dec, window=window)
     return pre, dec

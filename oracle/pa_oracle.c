@@ -20,7 +20,7 @@
  *  [OCP8]  OCP 8-bit floating point specification, E4M3 ("fn") encoding:
  *          bias 7, no infinities, S.1111.111 is NaN, max normal 448.
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - context_lens[b] is the total KV length including the q_lens[b] new
  *    tokens; query i of sequence b sits at absolute position
  *    p = ctx[b] - ql[b] + i and sees keys j <= p (bottom-right causal).

@@ -93,9 +93,7 @@ pa_status check_problem(const pa_problem* pp, int mode) {
         p.mask_q_tiles < 0 || p.mask_kv_tiles < 0 || p.num_ctas < 0 || p.balance_rows < 0 ||
         !std::isfinite(p.sm_scale) || p.sm_scale < 0.f || p.window < 0)
         return PA_ERR_INVALID_ARG;
-    // sliding window: the bf16 decode kernel only, so far
-    if (p.window > 0 && (mode != PA_MODE_DECODE || p.kv_dtype != PA_BF16))
-        return PA_ERR_UNSUPPORTED;
+
     if (p.layout != PA_NHD && p.layout != PA_HND) return PA_ERR_INVALID_ARG;
     if (p.kv_dtype != PA_BF16 && p.kv_dtype != PA_FP8_E4M3) return PA_ERR_INVALID_ARG;
     if ((p.mask_q_tiles > 0) != (p.mask_kv_tiles > 0)) return PA_ERR_INVALID_ARG;
@@ -581,10 +579,12 @@ pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cac
                      const float* v_scale, const uint8_t* block_mask, const void* assign_ws,
                      size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
                      void* out, float* lse, void* stream) {
-    (void)block_mask;  // the active-tile lists in assign_ws already encode the mask
     PrefillLayout M;
     pa_status st = make_prefill_layout(problem, M);
     if (st != PA_OK) return st;
+    // the kernels read the active-tile lists pa_assign built from the mask;
+    // the mask itself must be given exactly when the problem declares one
+    if ((problem->mask_q_tiles > 0) != (block_mask != nullptr)) return PA_ERR_INVALID_ARG;
     const WsLayout& L = M.L;
     const pa_problem& p = *problem;
     if (p.total_q_tokens == 0) return PA_OK;   // no query row: nothing to compute

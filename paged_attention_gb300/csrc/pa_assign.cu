@@ -19,6 +19,8 @@
 // Closed form used in 3: with C the total cost and N CTAs, CTA c owns
 // [a_c, a_{c+1}), a_c = floor(c*C/N); the owner of cost x (0 <= x < C) is
 // floor(((x+1)*N - 1) / C).
+#include <mutex>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -186,7 +188,10 @@ __global__ void assign_units_kernel(WsLayout L, const int32_t* __restrict__ ctx,
         keys = (int64_t)c_b - q_b + q0 + nq;
     }
     const int nreach = (int)ceil_div64(keys, L.kv_tile);
-    int n = nreach;
+    // with a sliding window the unit's tiles start at the first one its first
+    // query (position ctx - q_len + q0) can see
+    const int first = nq > 0 ? window_first_tile(L.window, c_b - q_b + q0, L.kv_tile) : 0;
+    int n = nreach - first;
     if (L.has_mask) {
         // active-KV-tile compaction: ballot the kept predicates of 32 tiles,
         // popcount them, write each kept tile at its prefix rank
@@ -194,7 +199,7 @@ __global__ void assign_units_kernel(WsLayout L, const int32_t* __restrict__ ctx,
         const uint8_t* mrow = mask + ((int64_t)b * L.mask_q_tiles + mq) * L.mask_kv_tiles;
         int32_t* out = active + (int64_t)u * L.max_kv_tiles;
         int base = 0;
-        for (int k0 = 0; k0 < nreach; k0 += 32) {
+        for (int k0 = first; k0 < nreach; k0 += 32) {
             const int kt = k0 + lane;
             const bool keep = kt < nreach && kt < L.mask_kv_tiles && mq < L.mask_q_tiles &&
                               mrow[kt] != 0;
@@ -419,16 +424,20 @@ cudaError_t launch_assign(const WsLayout& L, const int32_t* ctx, const int32_t* 
     const int warps = 8;
     const int grid = (L.unit_cap + warps - 1) / warps;
     assign_units_kernel<<<grid > 0 ? grid : 1, warps * 32, 0, stream>>>(L, ctx, ql, mask, ws);
-    // the shared-memory opt-in, once per device
+    // the shared-memory opt-in, once per device (host threads may race here)
+    static std::mutex attr_mu;
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(assign_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMapCacheBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    {
+        std::lock_guard<std::mutex> lk(attr_mu);
+        if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+            e = cudaFuncSetAttribute(assign_map_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kMapCacheBytes);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) attr_set[dev] = true;
+        }
     }
     assign_map_kernel<<<1, kScanThreads, kMapCacheBytes, stream>>>(L, ws);
     return cudaGetLastError();

@@ -216,8 +216,9 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
             const int tok_base = rec.cuq + q0;
             const int pbase = ctx_b - ql_b + q0;
             // this thread's rows are 8nt + 2q4 + e; the last key each may see
-            // (-1 for padding rows)
-            int lastk[NT][2];
+            // (-1 for padding rows) and, with a sliding window, the first
+            // ("HiLS-Attention", 二.1 local branch: keys p - window < j <= p)
+            int lastk[NT][2], firstk[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -225,7 +226,12 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     const int r = 8 * nt + 2 * q4 + e;
                     const int pr = pbase + r / G;
                     lastk[nt][e] = r < R ? (pr < ctx_b - 1 ? pr : ctx_b - 1) : -1;
+                    firstk[nt][e] = L.window > 0 ? pr - L.window + 1 : 0;
                 }
+            // task positions count from the unit's first visible tile; every
+            // row of the unit sees a key when it is >= first_open
+            const int first = window_first_tile(L.window, pbase, kDecodeTile);
+            const int first_open = L.window > 0 ? pbase + nq - L.window : 0;
 
             // ---- Q of the unit: bf16 slot -> f16 rows in head_dim order, then
             // release the slot.  Every consumer warp has left the previous
@@ -285,7 +291,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     // tokens past the context (slots after the last one of the
                     // sequence, or pages not loaded): P is 0 there, but E4M3 NaN
                     // codes would still poison the product
-                    const int tok_v = t * kDecodeTile + 16 * ts;
+                    const int tok_v = (t + first) * kDecodeTile + 16 * ts;
                     if (tok_v + 15 >= ctx_b) {
                         const int dt[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
 #pragma unroll
@@ -332,12 +338,13 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                 if (!kEarlyV) load_v();
 
                 // ---- mask + online softmax (log2 domain, lazily moved max)
-                const int tok = t * kDecodeTile + 16 * ts + g;   // token of sacc[.][0..1]
+                const int tok0 = (t + first) * kDecodeTile + 16 * ts;   // the slice's first token
+                const int tok = tok0 + g;                                // token of sacc[.][0..1]
                 const float cs = scale_log2 * ksc;
                 float sv[NT][4];
                 bool need = false;
                 // every row sees every token of the slice: no mask to apply
-                const bool open = R == kRows && t * kDecodeTile + 16 * ts + 15 <= pbase;
+                const bool open = R == kRows && tok0 + 15 <= pbase && tok0 >= first_open;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -346,8 +353,11 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                                                       : sacc[0][nt][e];
                         const float s2 = kChains == 2 ? sacc[0][nt][2 + e] + sacc[1][nt][2 + e]
                                                       : sacc[0][nt][2 + e];
-                        sv[nt][e] = open || tok <= lastk[nt][e] ? s0 * cs : -INFINITY;
-                        sv[nt][2 + e] = open || tok + 8 <= lastk[nt][e] ? s2 * cs : -INFINITY;
+                        sv[nt][e] = open || (tok <= lastk[nt][e] && tok >= firstk[nt][e])
+                                        ? s0 * cs : -INFINITY;
+                        sv[nt][2 + e] =
+                            open || (tok + 8 <= lastk[nt][e] && tok + 8 >= firstk[nt][e])
+                                ? s2 * cs : -INFINITY;
                         need |= fmaxf(sv[nt][e], sv[nt][2 + e]) > m[nt][e] + 8.f;
                     }
                 if (__any_sync(0xffffffffu, need)) {

@@ -171,8 +171,12 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     const int G = L.G, Hq = L.Hq;
     const int half_tokens = kPrefillHalfRows / G;   // query tokens per 128-row half
 
-    auto tile_of = [&](int u, int t) -> int {
-        return L.has_mask ? active[(int64_t)u * L.max_kv_tiles + t] : t;
+    // KV tile at position t of unit u's list: the active list with a block
+    // mask; else the tiles from the first one the unit's first query can see
+    // (position p0 = ctx - q_len + q0; 0 without a sliding window) onwards
+    auto tile_of = [&](int u, int t, int p0) -> int {
+        return L.has_mask ? active[(int64_t)u * L.max_kv_tiles + t]
+                          : t + window_first_tile(L.window, p0, kPrefillTile);
     };
 
     if (warp < 4) {
@@ -224,8 +228,9 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             // window's ids are requested one window ahead
             int win_lo = -(1 << 30), win_val = -1;
             int nxt_lo = -(1 << 30), nxt_val = -1;
+            const int p0 = ctx_b - rec.ql + q0;
             for (int t = rec.tk.y; t < rec.tk.z; ++t) {
-                const int kt = tile_of(u, t);
+                const int kt = tile_of(u, t, p0);
                 uint32_t bytes = 0;
                 int pg[8];
 #pragma unroll
@@ -366,7 +371,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 {
                     // zero V rows of keys past the context (P is 0 there, 0 * NaN is
                     // not): warp 1 writes, both MMA warps meet before their PV
-                    const int kt = tile_of(u, rec.tk.y + j);
+                    const int kt = tile_of(u, rec.tk.y + j, ctx_b - rec.ql + rec.un.z);
                     const int first_bad = ctx_b - kt * kPrefillTile;
                     if (first_bad < kPrefillTile) {
                         if (h == 0) {
@@ -441,6 +446,10 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             const int ctx_b = rec.ctx;
             const int p_row = ctx_b - rec.ql + q0 + r / G;   // last key this row sees
             const int key_last = p_row < ctx_b - 1 ? p_row : ctx_b - 1;
+            // first key this row sees: p - window + 1 with a sliding window
+            // ("HiLS-Attention", 二.1 local branch)
+            const int key_first = L.window > 0 ? p_row - L.window + 1 : -(1 << 30);
+            const int p0 = ctx_b - rec.ql + q0;
             const int n = rec.tk.z - rec.tk.y;
             // a warp whose 32 rows are all padding (units of a few rows: short
             // sequences of a masked batch, or the last q tile of a sequence)
@@ -449,7 +458,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             const bool warp_live = __any_sync(0xffffffffu, row_ok);
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
-                const int kt = tile_of(u, rec.tk.y + j);
+                const int kt = tile_of(u, rec.tk.y + j, p0);
                 wait(&s_full[h], (uint32_t)(s_cnt & 1));
                 ++s_cnt;
                 tc_fence_after();
@@ -463,6 +472,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     continue;
                 }
                 const int limc = row_ok ? key_last - kt * kPrefillTile : -1;   // valid: c <= limc
+                const int lowc = key_first - kt * kPrefillTile;                // and c >= lowc
                 // pass 1: row max of the raw scores (sm_scale >= 0 keeps the order),
                 // 32 columns at a time; the two softmax warps on each SM
                 // sub-partition hide each other's TMEM latency
@@ -473,14 +483,15 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     tmem_ld32(tS + c4 * 32, s);
                     tmem_wait_ld();
                     reg_fence32(s);
-                    const int lim = limc - c4 * 32;
-                    if (lim >= 31) {
+                    const int lim = limc - c4 * 32, low = lowc - c4 * 32;
+                    if (lim >= 31 && low <= 0) {
 #pragma unroll
                         for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            mx4[c & 3] = fmaxf(mx4[c & 3], c <= lim ? s[c] : -INFINITY);
+                            mx4[c & 3] =
+                                fmaxf(mx4[c & 3], (c <= lim && c >= low) ? s[c] : -INFINITY);
                     }
                 }
                 const float mx =
@@ -507,9 +518,9 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     tmem_ld32(tS + c4 * 32, s);
                     tmem_wait_ld();
                     reg_fence32(s);
-                    const int lim = limc - c4 * 32;
+                    const int lim = limc - c4 * 32, low = lowc - c4 * 32;
                     uint32_t pk[16];
-                    if (lim >= 31) {
+                    if (lim >= 31 && low <= 0) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
                             const uint32_t e2 = ex2_h2(fmaf(s[c], scale_log2, -mu),
@@ -521,11 +532,12 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
-                            const float p0 = c <= lim ? ex2(fmaf(s[c], scale_log2, -mu)) : 0.f;
-                            const float p1 =
-                                c + 1 <= lim ? ex2(fmaf(s[c + 1], scale_log2, -mu)) : 0.f;
-                            sum4[(c >> 1) & 3] += p0 + p1;
-                            pk[c >> 1] = pack_bf16x2(p0, p1);
+                            const float e0 = (c <= lim && c >= low)
+                                                 ? ex2(fmaf(s[c], scale_log2, -mu)) : 0.f;
+                            const float e1 = (c + 1 <= lim && c + 1 >= low)
+                                                 ? ex2(fmaf(s[c + 1], scale_log2, -mu)) : 0.f;
+                            sum4[(c >> 1) & 3] += e0 + e1;
+                            pk[c >> 1] = pack_bf16x2(e0, e1);
                         }
                     }
                     tmem_st16(tS + c4 * 16, pk);

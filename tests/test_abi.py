@@ -87,9 +87,9 @@ def test_invalid_problems_rejected_on_host(lib):
     win = B.PaProblem.from_buffer_copy(p)
     win.window = 100                          # sliding window: bf16 decode is built
     assert B.pa_assign_workspace_size(win, B.PA_MODE_DECODE) > 0
-    assert B.pa_assign_workspace_size(win, B.PA_MODE_PREFILL) == 0   # not yet
-    win.kv_dtype = 1                          # E4M3 decode with a window: not yet
-    assert B.pa_assign_workspace_size(win, B.PA_MODE_DECODE) == 0
+    assert B.pa_assign_workspace_size(win, B.PA_MODE_PREFILL) > 0    # and prefill
+    win.kv_dtype = 1                          # E4M3 decode with a window: built
+    assert B.pa_assign_workspace_size(win, B.PA_MODE_DECODE) > 0
     bad = B.PaProblem.from_buffer_copy(p)
     bad.window = -1
     assert B.pa_assign_workspace_size(bad, B.PA_MODE_DECODE) == 0

@@ -40,7 +40,8 @@ def check(w, mode, num_ctas=0, balance_rows=0):
     Nd = B.pa_num_ctas(pd, B.PA_MODE_DECODE) if has_part else N
     pre, dec = oracle.assign_prefill(w.num_seqs, w.num_q_heads, w.num_kv_heads, N,
                                      balance_rows or 128, w.context_lens, w.q_lens,
-                                     w.block_mask, decode_ctas=Nd)
+                                     w.block_mask, decode_ctas=Nd,
+                                     window=int(getattr(w, "window", 0)))
     task_map_equal(gpu, pre, with_active=w.block_mask is not None)
     gpu_d = B.pa_read_task_map(bufs.problem, B.PA_MAP_DECODE_PART, bufs.assign_ws)
     if dec is None:
@@ -123,3 +124,16 @@ def test_prefill_map_beyond_the_shared_memory_cache():
     w = W.make_workload("manyp", ctx, ql, num_q_heads=32, num_kv_heads=8, head_dim=64,
                         page_size=16, seed=78, mode="prefill")
     check(w, B.PA_MODE_PREFILL)
+
+
+@pytest.mark.parametrize("window,sparse", [(1, False), (300, False), (1000, True), (4096, True)])
+def test_prefill_map_with_sliding_window(window, sparse):
+    """Prefill-mode maps with a sliding window: each unit's tiles (or its
+    active list under a block mask) start at the first tile its first query
+    can see; bit-exact with the oracle, decode part included."""
+    w = W.prefill_bf16(sparse=sparse, shrink=4)
+    w.window = window
+    check(w, B.PA_MODE_PREFILL)
+    h = W.hybrid_bf16(shrink=8)
+    h.window = window
+    check(h, B.PA_MODE_PREFILL, num_ctas=37)

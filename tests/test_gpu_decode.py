@@ -122,6 +122,33 @@ def test_decode_sliding_window(window, ps, ql, D):
     run_and_compare(w, num_ctas=19)
 
 
+@pytest.mark.parametrize("window,ps,ql,G,layout", [(1, 64, 1, 8, W.HND), (64, 64, 3, 8, W.HND),
+                                                    (100, 16, 2, 4, W.NHD),
+                                                    (1000, 32, 4, 8, W.HND),
+                                                    (5000, 64, 3, 8, W.NHD),
+                                                    (37, 128, 4, 4, W.NHD)])
+def test_decode_fp8_sliding_window(window, ps, ql, G, layout):
+    """The sliding window on the E4M3 decode kernel: every row-tile variant
+    (8 to 32 rows), windows below, at and far above a 64-token tile, MTP rows
+    whose windows start at different keys, pages of 16 to 128 tokens, both
+    layouts, split units (19 CTAs)."""
+    ctx = [37, 700, 1500, 4096, 129, 9000]
+    w = W.make_workload(f"win8_{window}", ctx, [ql] * 6, num_q_heads=8 * G, num_kv_heads=8,
+                        head_dim=128, page_size=ps, layout=layout, kv_dtype=W.FP8_E4M3,
+                        seed=7 * window + ps + ql)
+    w.window = window
+    run_and_compare(w, num_ctas=19)
+
+
+def test_decode_fp8_window_full_size_sampled():
+    """The E4M3 workload (q_len 3) with a 2048-key window at full size."""
+    w = W.decode_fp8()
+    w.window = 2048
+    rng = np.random.default_rng(12)
+    rows = np.sort(rng.choice(w.total_q * w.num_q_heads, size=4096, replace=False))
+    run_and_compare(w, rows=rows)
+
+
 def test_decode_is_deterministic():
     w = W.decode_bf16(mtp=3, shrink=8).to("cuda")
     a = B.run_decode(w)

@@ -164,3 +164,33 @@ def test_prefill_deterministic():
     B.run_prefill(w, a)
     torch.cuda.synchronize()
     assert torch.equal(o1, a.out) and torch.equal(l1, a.lse)
+
+
+@pytest.mark.parametrize("window,G,ps,masked", [(1, 4, 64, False), (100, 8, 16, False),
+                                                (128, 1, 32, False), (333, 4, 64, True),
+                                                (1000, 2, 128, False), (4096, 8, 64, True)])
+def test_prefill_sliding_window(window, G, ps, masked):
+    """Sliding window on the tensor-core prefill path ("HiLS-Attention", 二.1
+    local branch: query p sees the keys p - window < j <= p): windows shorter
+    than a row of a tile, a tile long and across many tiles, chunks over
+    history, decode-shaped sequences (their own kernel), block masks, split
+    units."""
+    ctx = [1000, 700, 300, 2000, 57]
+    ql = [300, 5, 100, 1000, 1]
+    mask = None
+    if masked:
+        g = torch.Generator().manual_seed(window)
+        mask = (torch.rand((5, -(-max(ql) // 128), -(-max(ctx) // 128)), generator=g)
+                < 0.6).to(torch.uint8)
+    w = W.make_workload(f"pwin{window}", ctx, ql, num_q_heads=2 * G, num_kv_heads=2,
+                        head_dim=128, page_size=ps, seed=window + G, block_mask=mask,
+                        mode="prefill")
+    w.window = window
+    run_and_compare(w, num_ctas=23)
+
+
+def test_prefill_window_quarter_size_sampled():
+    """The dense prefill workload at quarter size with a 1000-key window."""
+    w = W.prefill_bf16(sparse=False, shrink=4)
+    w.window = 1000
+    run_and_compare(w, rows=sample_rows(w, per_seq=512, seed=5))

@@ -291,3 +291,46 @@ def test_prefill_split_worked_example(oracle_mod):
         assert tm.unit_nsplit.tolist() == e["unit_nsplit"]
         assert tm.unit_slot0.tolist() == e["unit_slot0"]
         assert tm.num_slots == e["num_slots"]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_prefill_split_with_window(oracle_mod, seed):
+    """Both prefill-mode maps take the sliding window ("HiLS-Attention", 二.1
+    local branch: keys p - window < j <= p): a unit's tiles start at the tile
+    holding its first query's first visible key, p0 - window + 1, and end
+    where they would without a window; with a block mask the active list is
+    the kept tiles of that range."""
+    rng = np.random.default_rng(3000 + seed)
+    Hkv = int(rng.choice([1, 2]))
+    G = int(rng.choice([1, 4, 8]))
+    B = int(rng.integers(1, 7))
+    N = int(rng.integers(1, 20))
+    window = int(rng.choice([1, 50, 128, 300, 700]))
+    ctx, ql = [], []
+    for _ in range(B):
+        c = int(rng.integers(1, 900))
+        q = int(rng.integers(1, min(c, 4) + 1)) if rng.random() < 0.5 else \
+            int(rng.integers(1, min(c, 300) + 1))
+        ctx.append(c)
+        ql.append(q)
+    masked = seed % 3 == 0
+    mask = None
+    if masked:
+        qt = -(-max(ql) // 128)
+        kt = -(-max(ctx) // 128)
+        mask = (rng.random((B, qt, kt)) < 0.6).astype(np.uint8)
+    pre, dec = oracle_mod.assign_prefill(B, G * Hkv, Hkv, N, 128, np.array(ctx, np.int32),
+                                         np.array(ql, np.int32), block_mask=mask,
+                                         window=window)
+    for u, ((b, hk, q0, nq), n) in enumerate(zip(pre.units.tolist(), pre.unit_ntiles.tolist())):
+        first = max(0, ctx[b] - ql[b] + q0 - window + 1) // 128
+        end = -(-(ctx[b] - ql[b] + q0 + nq) // 128)
+        want = [t for t in range(first, end)
+                if mask is None or (t < mask.shape[2] and mask[b, q0 // 128, t])]
+        assert n == len(want)
+        if mask is not None:
+            assert pre.active[u, :n].tolist() == want
+    if dec is not None:
+        for (b, hk, q0, nq), n in zip(dec.units.tolist(), dec.unit_ntiles.tolist()):
+            first = max(0, ctx[b] - ql[b] - window + 1) // 64
+            assert n == ((-(-ctx[b] // 64) - first) if nq > 0 else 0)

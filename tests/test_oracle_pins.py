@@ -413,7 +413,7 @@ def test_block_mask_skip_ratio_matches_pages():
 # ------------------------------------------------ sliding window (local branch)
 # "HiLS-Attention" page, 二.1 (the local sliding-window branch): query p sees
 # the keys p - window < j <= p.  The bounds are our reading (the page gives
-# none); the kernels do not take a window yet.
+# none).
 
 def _windowed(w, window):
     w.window = window
