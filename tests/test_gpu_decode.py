@@ -90,6 +90,13 @@ def test_decode_bf16_full_size_mtp1():
     run_and_compare(W.decode_bf16(mtp=1))
 
 
+@pytest.mark.parametrize("mtp", [2, 3])
+def test_decode_bf16_full_size_mtp(mtp):
+    """The bf16 decode workload at q_len 3 and 4 at full size (12 and 16 rows
+    per unit), checked on every row."""
+    run_and_compare(W.decode_bf16(mtp=mtp))
+
+
 def test_decode_fp8_full_size_sampled():
     w = W.decode_fp8()
     rng = np.random.default_rng(3)

@@ -121,19 +121,57 @@ def test_chunk_over_history_with_mask():
     run_and_compare(w, num_ctas=7)
 
 
-def test_prefill_dense_full_size_sampled():
+def kv_head_rows(w, seed=0):
+    """Every row of one (sequence, KV head) per sequence: all new tokens x the
+    G q heads of a KV head picked per sequence (so every 256-row unit and
+    both 128-row tensor-core halves of that head are checked end to end)."""
+    rng = np.random.default_rng(seed)
+    G = w.num_q_heads // w.num_kv_heads
+    ql = [int(x) for x in w.q_lens]
+    cu = np.concatenate([[0], np.cumsum(ql)])
+    rows = []
+    for b in range(w.num_seqs):
+        hk = int(rng.integers(0, w.num_kv_heads))
+        toks = np.arange(cu[b], cu[b + 1], dtype=np.int64)
+        heads = hk * G + np.arange(G, dtype=np.int64)
+        rows.append((toks[:, None] * w.num_q_heads + heads[None, :]).reshape(-1))
+    return np.sort(np.concatenate(rows))
+
+
+def all_head_rows(w, per_seq=64, seed=0):
+    """Sampled tokens of every sequence (first and last included) with all
+    their q heads."""
+    rng = np.random.default_rng(seed)
+    ql = [int(x) for x in w.q_lens]
+    cu = np.concatenate([[0], np.cumsum(ql)])
+    rows = []
+    for b in range(w.num_seqs):
+        if ql[b] == 0:
+            continue
+        toks = np.unique(np.concatenate([[cu[b], cu[b + 1] - 1],
+                                         rng.integers(cu[b], cu[b + 1], size=per_seq)]))
+        rows.append((toks[:, None] * w.num_q_heads
+                     + np.arange(w.num_q_heads)[None, :]).reshape(-1))
+    return np.sort(np.concatenate(rows)).astype(np.int64)
+
+
+def test_prefill_dense_full_size_kv_head_rows():
+    """The dense prefill workload at full size, in the launch configuration
+    the bench times: all 8192 x 8 rows of one KV head per sequence."""
     w = W.prefill_bf16(sparse=False)
-    run_and_compare(w, rows=sample_rows(w, per_seq=300))
+    run_and_compare(w, rows=kv_head_rows(w, seed=0))
 
 
-def test_prefill_sparse_full_size_sampled():
+def test_prefill_sparse_full_size_kv_head_rows():
     w = W.prefill_bf16(sparse=True)
-    run_and_compare(w, rows=sample_rows(w, per_seq=300, seed=1))
+    run_and_compare(w, rows=kv_head_rows(w, seed=1))
 
 
 def test_hybrid_full_size_sampled():
+    """Full-size hybrid batch: every head of every decode sequence's token,
+    and sampled chunk tokens with all their heads."""
     w = W.hybrid_bf16()
-    run_and_compare(w, rows=sample_rows(w, per_seq=64, seed=2))
+    run_and_compare(w, rows=all_head_rows(w, per_seq=64, seed=2))
 
 
 def test_masked_tiles_never_loaded():
