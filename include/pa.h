@@ -303,6 +303,23 @@ PA_API pa_status pa_read_task_map(const pa_problem* problem, int mode, const voi
                            int32_t* unit_nsplit, int32_t* unit_slot0, int32_t* active,
                            void* stream);
 
+/*
+ * Test hook (the pages describe no such call; it exists to exercise the
+ * failure path of the bounded waits without a GPU fault).  The next compute
+ * launch in this process (the decode kernel of pa_decode_splitk or
+ * pa_decode_noalloc, or the tensor-core kernel of pa_prefill -- not the
+ * decode kernel pa_prefill runs first for a mixed batch's decode-shaped
+ * sequences) runs with every pipeline wait limited to
+ * wait_limit_ns, and in its CTA 0 the producer leaves K/V ring entry number
+ * skip_entry (counted from 0 in issue order) unfilled.  The consumer waiting
+ * for that entry runs out of time: the launch records PA_DEV_WAIT_TIMEOUT,
+ * every CTA stops waiting, waits for the tensor copies it issued, frees its
+ * tensor memory and finishes; the outputs of that call are unspecified.  The
+ * hook disarms itself after that one launch.  skip_entry < 0 disarms it.
+ * wait_limit_ns: 1e6 .. 1e9 (else PA_ERR_INVALID_ARG).
+ */
+PA_API pa_status pa_test_inject_wait_timeout(int32_t skip_entry, int64_t wait_limit_ns);
+
 /* Read (and keep) the device error word of assign_ws into *code (host);
  * synchronises `stream`.  Returns PA_OK when *code == PA_DEV_OK, else
  * PA_ERR_DEVICE_CHECK (or PA_ERR_TIMEOUT when only the timeout bit is set). */

@@ -34,6 +34,7 @@ EXPORTED = (
     "pa_status_string", "pa_version", "pa_num_ctas", "pa_assign_workspace_size",
     "pa_partial_workspace_size", "pa_assign", "pa_decode_splitk", "pa_combine", "pa_prefill",
     "pa_read_task_map", "pa_last_device_error", "pa_decode_noalloc",
+    "pa_test_inject_wait_timeout",
 )
 
 PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # size of the library's fixed scratch
@@ -107,6 +108,7 @@ def load(build_if_missing: bool = True):
             "pa_read_task_map": (i32, [PP, i32, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pa_last_device_error": (i32, [vp, ctypes.POINTER(ctypes.c_int32), vp]),
             "pa_decode_noalloc": (i32, [PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "pa_test_inject_wait_timeout": (i32, [ctypes.c_int32, ctypes.c_int64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -244,6 +246,13 @@ def pa_read_task_map(problem, mode, assign_ws, stream=None) -> dict:
         c(out["active"]) if out["active"] is not None else None, _stream(stream)),
         "pa_read_task_map")
     return out
+
+
+def pa_test_inject_wait_timeout(skip_entry: int, wait_limit_ns: int = 20_000_000):
+    """Test hook: the next compute launch leaves one K/V ring entry unfilled in
+    CTA 0 and limits its waits to wait_limit_ns (see include/pa.h)."""
+    _check(load().pa_test_inject_wait_timeout(int(skip_entry), int(wait_limit_ns)),
+           "pa_test_inject_wait_timeout")
 
 
 def pa_last_device_error(assign_ws, stream=None) -> int:

@@ -3,6 +3,7 @@
 // entry point are in include/pa.h.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -25,7 +26,7 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
                                    const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, bool take_hook = true);
 int prefill_smem_bytes(int D, bool fp8);
 const void* prefill_kernel_ptr(int D, bool fp8);
 cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, const void* q,
@@ -297,7 +298,17 @@ int combine_grid(const WsLayout& L) {
     return grid < 1 ? 1 : (int)grid;
 }
 
+std::atomic<int32_t> g_test_skip{-1};
+std::atomic<uint64_t> g_test_limit{0};
+
 }  // namespace
+
+void take_test_hook(int32_t* skip_entry, uint64_t* wait_limit_ns) {
+    const int32_t s = g_test_skip.exchange(-1);
+    const uint64_t l = g_test_limit.exchange(0);
+    *skip_entry = s;
+    *wait_limit_ns = (s >= 0 && l > 0) ? l : kWaitLimitNs;
+}
 
 bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L) {
     std::memset(&L, 0, sizeof(L));
@@ -610,16 +621,30 @@ pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cac
             return PA_ERR_INVALID_ARG;
         const bool one_box = encode_kv_map_one_box(M.pd, k_cache, &tkd) &&
                              encode_kv_map_one_box(M.pd, v_cache, &tvd);
+        // (the wait-timeout test hook is left for the prefill kernel)
         e = launch_decode_from_api(M.pd, M.Ld, tqd, one_box ? tkd : tk, one_box ? tvd : tv,
                                    one_box, block_table, context_lens, q_lens, k_scale, v_scale,
                                    const_cast<void*>(assign_ws),
-                                   static_cast<char*>(partial_ws) + M.part_off, out, lse, s);
+                                   static_cast<char*>(partial_ws) + M.part_off, out, lse, s,
+                                   false);
     }
     if (e == cudaSuccess)
         e = launch_prefill_from_api(p, L, q, tq, tk, tv, block_table, context_lens, q_lens,
                                     k_scale, v_scale, const_cast<void*>(assign_ws), partial_ws,
                                     out, lse, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_test_inject_wait_timeout(int32_t skip_entry, int64_t wait_limit_ns) {
+    if (skip_entry < 0) {
+        g_test_skip.store(-1);
+        g_test_limit.store(0);
+        return PA_OK;
+    }
+    if (wait_limit_ns < 1000000 || wait_limit_ns > 1000000000) return PA_ERR_INVALID_ARG;
+    g_test_limit.store((uint64_t)wait_limit_ns);
+    g_test_skip.store(skip_entry);
+    return PA_OK;
 }
 
 pa_status pa_read_task_map(const pa_problem* problem, int mode, const void* assign_ws,

@@ -61,7 +61,8 @@ struct DecodeCfg {
     static constexpr int kOffMerge = kOffQ + 2 * kQSlotBytes;
     static constexpr int kOffBar = (kOffMerge + kMergeBytes + 15) / 16 * 16;
     static constexpr int kNumBars = 2 * STAGES + 4;
-    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+    static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;   // after the abort flag
+    static constexpr int kSmemBytes = kOffArmed + (4 * (STAGES + 2) + 15) / 16 * 16 + 1024;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(kQHalfBytes % 1024 == 0, "Q slot alignment");
     // Group g consumes the tiles with index % NG == g.  Every ring stage must
@@ -86,6 +87,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     uint64_t* q_full = empty + STAGES;       // 2 slots
     uint64_t* q_empty = q_full + 2;          // 2 slots
     volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
+    int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // last phase armed per stage
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
     int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);   // device faults
@@ -107,13 +109,14 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
             mbar_init(&q_empty[s], Cfg::kConsumerWarps);
         }
         *abort_flag = 0;
+        for (int s = 0; s < STAGES + 2; ++s) armed[s] = -1;
         fence_mbar_init();
     }
     __syncthreads();
 
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (*abort_flag) return;
-        if (!mbar_wait(bar, parity, lim)) {
+        if (!mbar_wait_or_abort(bar, parity, lim, abort_flag)) {
             *abort_flag = 1;
             set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
         }
@@ -128,7 +131,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
 
     if (warp < Cfg::kProducerWarps) {
         decode_produce<Cfg>(P, &tmq, &tmk, &tmv, smem, full, empty, q_full, q_empty, nullptr,
-                            abort_flag, err_hdr, k_begin, k_end, warp, lane, wait);
+                            abort_flag, armed, err_hdr, k_begin, k_end, warp, lane, wait);
     } else {
         // ------------------------------------------------------- consumers
         const int cw = warp - Cfg::kProducerWarps;
@@ -388,13 +391,11 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         }
     }
     grid_launch_dependents();   // Combine may become resident meanwhile
+    // every warp is done; after an abort the producers wait for their copies
+    // still in flight before the CTA exits
     __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) {
-        // the consumers stopped waiting: give copies already issued time to land
-        const uint64_t t0 = globaltimer();
-        while (globaltimer() - t0 < 200000ull) {
-        }
-    }
+    if (warp < Cfg::kProducerWarps) decode_drain<Cfg>(full, q_full, armed, abort_flag, warp, lane);
+    __syncthreads();
 }
 
 template <int D, int RT, int NG, int STAGES>
@@ -495,7 +496,7 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
                                    const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, bool take_hook) {
     DecodeParams P;
     P.L = L;
     P.block_table = block_table;
@@ -516,7 +517,9 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
     P.q_box_tokens = p.max_q_len > 0 ? p.max_q_len : 1;
     P.kv_one_box = kv_one_box ? 1 : 0;
     P.sm_scale = p.sm_scale;
-    P.wait_limit_ns = 1000000000ull;
+    P.test_skip_it = -1;
+    P.wait_limit_ns = kWaitLimitNs;
+    if (take_hook) take_test_hook(&P.test_skip_it, &P.wait_limit_ns);
     if (is_fp8(p)) {
         if (p.head_dim != 128) return cudaErrorInvalidValue;
         return launch_decode_fp8(P, decode_fp8_row_tiles(unit_rows(p)), tq, tk, tv, stream);

@@ -31,6 +31,7 @@ struct DecodeParams {
     int32_t boxes_per_tile;   // 64 / rows_per_box
     int32_t q_box_tokens;     // tokens per Q TMA box (max q_len)
     int32_t kv_one_box;       // 1: one 5-D TMA box fills both column blocks of a tile
+    int32_t test_skip_it;     // test hook: CTA 0 leaves this KV tile's stage unfilled (-1 none)
     float sm_scale;
     uint64_t wait_limit_ns;
 };
@@ -56,16 +57,19 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // kHalves (128-byte column blocks per K/V row), kHalfBytes, kKBytes (V follows
 // K in a stage), kStageBytes, kElem, kQHalves, kQHalfBytes, kQSlotBytes,
 // kOffQ.  `wait` is the kernel's bounded mbarrier wait (it turns into a no-op
-// once the CTA has aborted, so the loop structure is kept and every barrier is
-// still arrived).
+// once the CTA has aborted, so the loop structure is kept).  After an abort
+// the producers arm no barrier and issue no copy; `armed` (shared, kStages + 2
+// ints, -1 at start) records per ring stage and per Q slot the last phase
+// armed with a copy, so that decode_drain can wait for every copy still in
+// flight before the CTA exits.
 template <class Cfg, class Wait>
 __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUtensorMap* tmq,
                                                const CUtensorMap* tmk, const CUtensorMap* tmv,
                                                uint8_t* smem, uint64_t* full, uint64_t* empty,
                                                uint64_t* q_full, uint64_t* q_empty,
                                                float* scales, volatile int* abort_flag,
-                                               int32_t* err_hdr, int k_begin, int k_end,
-                                               int pw, int lane, Wait& wait) {
+                                               int* armed, int32_t* err_hdr, int k_begin,
+                                               int k_end, int pw, int lane, Wait& wait) {
     static_assert(Cfg::kStages % Cfg::kProducerWarps == 0,
                   "every ring stage must stay with one producer warp");
     const WsLayout& L = P.L;
@@ -100,9 +104,9 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
             // lane 0 arms the slot, then lane h copies column block h (a tensor
             // copy holds its issuing thread for hundreds of cycles)
             const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
-            if (lane == 0) {
-                if (go) mbar_arrive_expect_tx(&q_full[qs], q_bytes);
-                else mbar_arrive(&q_full[qs]);
+            if (lane == 0 && go) {
+                armed[Cfg::kStages + qs] = task_it >> 1;
+                mbar_arrive_expect_tx(&q_full[qs], q_bytes);
             }
             __syncwarp();
             if (go && lane < Cfg::kQHalves)
@@ -161,8 +165,11 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
             }
             uint8_t* stK = smem + s * Cfg::kStageBytes;
             uint8_t* stV = stK + Cfg::kKBytes;
-            const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
-            if (lane == 0) {
+            // test hook: CTA 0 leaves one stage unfilled, so that its consumers'
+            // bounded wait runs out (the abort path, exercised without a fault)
+            const bool skip = P.test_skip_it == it && blockIdx.x == 0;
+            const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0 && !skip;
+            if (lane == 0 && go) {
                 if (Cfg::kFP8) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -170,8 +177,8 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                         scales[(s * 2 + 1) * 4 + j] = pg[j] >= 0 ? vsc[j] : 0.f;
                     }
                 }
-                if (go) mbar_arrive_expect_tx(&full[s], bytes);
-                else mbar_arrive(&full[s]);
+                armed[s] = it / Cfg::kStages;
+                mbar_arrive_expect_tx(&full[s], bytes);
             }
             __syncwarp();
             // one box per lane: a tensor copy holds its issuing thread for
@@ -202,6 +209,23 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
             __syncwarp();
         }
     }
+}
+
+// After an abort: wait (bounded) until every copy this producer warp armed
+// has landed -- for each of its ring stages (and, warp 0, the Q slots) the
+// phase last armed with a copy -- so that no tensor copy is still writing
+// shared memory when the CTA exits.  Nothing arms a barrier after the abort,
+// so each such phase completes exactly when its bytes arrive.
+template <class Cfg>
+__device__ __forceinline__ void decode_drain(uint64_t* full, uint64_t* q_full, const int* armed,
+                                             const volatile int* abort_flag, int pw, int lane) {
+    if (!*abort_flag || lane != 0) return;
+    for (int s = pw; s < Cfg::kStages; s += Cfg::kProducerWarps)
+        if (armed[s] >= 0) mbar_wait(&full[s], (uint32_t)(armed[s] & 1), kDrainLimitNs);
+    if (pw == 0)
+        for (int qs = 0; qs < 2; ++qs)
+            if (armed[Cfg::kStages + qs] >= 0)
+                mbar_wait(&q_full[qs], (uint32_t)(armed[Cfg::kStages + qs] & 1), kDrainLimitNs);
 }
 
 }  // namespace pa

@@ -90,7 +90,8 @@ struct DecodeFp8Cfg {
     static constexpr int kOffScale = kOffML + kMLBytes;
     static constexpr int kOffBar = (kOffScale + kScaleBytes + 15) / 16 * 16;
     static constexpr int kNumBars = 2 * STAGES + 4;
-    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+    static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;   // after the abort flag
+    static constexpr int kSmemBytes = kOffArmed + (4 * (STAGES + 2) + 15) / 16 * 16 + 1024;
     static_assert(NT >= 1 && NT <= 4, "rows per unit");
     // every ring stage is always consumed by the same group (a group that
     // reused a stage after the other could wait two phases ahead)
@@ -132,6 +133,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     uint64_t* q_full = empty + STAGES;       // 2 slots
     uint64_t* q_empty = q_full + 2;          // 2 slots
     volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
+    int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // last phase armed per stage
     float* scales = reinterpret_cast<float*>(smem + Cfg::kOffScale);   // [stage][k|v][box]
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
@@ -154,13 +156,14 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
             mbar_init(&q_empty[s], kCW);
         }
         *abort_flag = 0;
+        for (int s = 0; s < STAGES + 2; ++s) armed[s] = -1;
         fence_mbar_init();
     }
     __syncthreads();
 
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (*abort_flag) return;
-        if (!mbar_wait(bar, parity, lim)) {
+        if (!mbar_wait_or_abort(bar, parity, lim, abort_flag)) {
             *abort_flag = 1;
             set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
         }
@@ -172,7 +175,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     if (warp < 4) {
         regs_dec<Cfg::kRegsProducer>();
         decode_produce<Cfg>(P, &tmq, &tmk, &tmv, smem, full, empty, q_full, q_empty, scales,
-                            abort_flag, err_hdr, k_begin, k_end, warp, lane, wait);
+                            abort_flag, armed, err_hdr, k_begin, k_end, warp, lane, wait);
     } else {
         regs_inc<Cfg::kRegsConsumer>();
         // ------------------------------------------------------- consumers
@@ -531,13 +534,11 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
         }
     }
     grid_launch_dependents();   // Combine may become resident meanwhile
+    // every warp is done; after an abort the producers wait for their copies
+    // still in flight before the CTA exits
     __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) {
-        // the consumers stopped waiting: give copies already issued time to land
-        const uint64_t t0 = globaltimer();
-        while (globaltimer() - t0 < 200000ull) {
-        }
-    }
+    if (warp < Cfg::kProducerWarps) decode_drain<Cfg>(full, q_full, armed, abort_flag, warp, lane);
+    __syncthreads();
 }
 
 // (8-row tiles, ring stages) built

@@ -86,6 +86,13 @@ struct WsLayout {
 // fills `L` for (problem, mode, N); returns false on invalid dims
 bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L);
 
+// Bounded-wait limit of a normal launch.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// The wait-timeout test hook (pa_test_inject_wait_timeout): returns the ring
+// entry CTA 0's producer should leave unfilled (-1: none) and the wait limit
+// for the next compute launch, and disarms the hook.
+void take_test_hook(int32_t* skip_entry, uint64_t* wait_limit_ns);
+
 template <typename T>
 __host__ __device__ inline T* ws_ptr(void* ws, int64_t off) {
     return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
@@ -183,6 +190,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
         if ((it & 255u) == 0 && globaltimer() - t0 > limit_ns) return false;
     }
 }
+// The same, but it also gives up as soon as the CTA's abort flag is raised
+// (another warp's wait ran out): the CTA then winds down without waiting for
+// data that will not come.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   uint64_t limit_ns, const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && (*abort || globaltimer() - t0 > limit_ns)) return false;
+    }
+}
+
+// Limit of each wait while a CTA that gave up drains its own copies in
+// flight (a tensor copy lands within microseconds; this only bounds the
+// wait should one never land).
+constexpr uint64_t kDrainLimitNs = 100000000ull;
 
 // TMA ----------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,

@@ -65,6 +65,7 @@ struct PrefillParams {
     int32_t max_pages_per_seq;
     int32_t rows_per_box;    // min(page_size, 64)
     int32_t boxes_per_tile;  // 128 / rows_per_box
+    int32_t test_skip_it;    // test hook: CTA 0 leaves this K/V ring entry unfilled (-1 none)
     float sm_scale;
     uint64_t wait_limit_ns;
 };
@@ -81,7 +82,10 @@ struct PrefillCfg {
     static constexpr int kOffKV = kOffQ + kQBytes;
     static constexpr int kOffBar = kOffKV + kEntries * kKVBytes;
     static constexpr int kNumBars = 2 + 2 * kEntries + 9;
-    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+    // after the TMEM slot and the abort flag: the last phase each producer warp
+    // armed with a copy, per ring entry, and that of the Q buffer
+    static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;
+    static constexpr int kSmemBytes = kOffArmed + (4 * (2 * kEntries + 1) + 15) / 16 * 16 + 1024;
     static constexpr int kThreads = 384;
     static constexpr int kRegsLaunch = 168;          // 65536 / 384, rounded down to 8
     static constexpr int kRegsProducer = 88;
@@ -117,6 +121,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     uint64_t* mma_done = o_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // [2][E] entries, then Q
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
     int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);   // device faults
@@ -143,6 +148,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         }
         mbar_init(mma_done, 2);
         *abort_flag = 0;
+        for (int i = 0; i < 2 * E + 1; ++i) armed[i] = -1;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -156,7 +162,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
 
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (*abort_flag) return;
-        if (!mbar_wait(bar, parity, lim)) {
+        if (!mbar_wait_or_abort(bar, parity, lim, abort_flag)) {
             *abort_flag = 1;
             set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
         }
@@ -212,9 +218,9 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 // lane 0 arms the Q buffer, then lane h * kHalves + c copies half
                 // h's column block c (one tensor copy per lane)
                 const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
-                if (lane == 0) {
-                    if (go) mbar_arrive_expect_tx(q_full, (uint32_t)H * Cfg::kQTileBytes);
-                    else mbar_arrive(q_full);
+                if (lane == 0 && go) {
+                    armed[2 * E] = task_it;
+                    mbar_arrive_expect_tx(q_full, (uint32_t)H * Cfg::kQTileBytes);
                 }
                 __syncwarp();
                 if (go && lane < H * Cfg::kHalves) {
@@ -264,10 +270,13 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     // issues one box (page j = pw + 2 (lane / kHalves), column block
                     // lane % kHalves).  A tensor copy holds its issuing thread for
                     // hundreds of cycles, so small pages need many issuing lanes.
-                    const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
-                    if (lane == 0) {
-                        if (go) mbar_arrive_expect_tx(&kv_full[e], bytes);   // this warp's pages
-                        else mbar_arrive(&kv_full[e]);
+                    // test hook: CTA 0 leaves one entry unfilled, so that the MMA
+                    // warps' bounded wait runs out (the abort path, without a fault)
+                    const bool skip = P.test_skip_it == e_it && blockIdx.x == 0;
+                    const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0 && !skip;
+                    if (lane == 0 && go) {
+                        armed[pw * E + e] = e_it / E;
+                        mbar_arrive_expect_tx(&kv_full[e], bytes);   // this warp's pages
                     }
                     __syncwarp();
                     if (go && lane < 4 * Cfg::kHalves) {
@@ -615,6 +624,23 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // After an abort, wait (bounded) for every copy the producers armed before
+    // the CTA exits.  Nothing arms a barrier after the abort; an entry's phase
+    // needs both producer warps' arrivals, and one of them may have stopped a
+    // phase short (it never runs more than one phase ahead of the other), so
+    // the missing arrival is added before waiting.  The MMA warps already
+    // waited for all their MMAs (the mma_done commit).
+    if (*abort_flag && threadIdx.x == 0) {
+        for (int e = 0; e < E; ++e) {
+            const int a0 = armed[e], a1 = armed[E + e];
+            const int ph = a0 > a1 ? a0 : a1;
+            if (ph < 0) continue;
+            if (a0 != a1) mbar_arrive(&kv_full[e]);
+            mbar_wait(&kv_full[e], (uint32_t)(ph & 1), kDrainLimitNs);
+        }
+        if (armed[2 * E] >= 0) mbar_wait(q_full, (uint32_t)(armed[2 * E] & 1), kDrainLimitNs);
+    }
+    __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
@@ -659,7 +685,7 @@ cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, cons
     P.rows_per_box = p.page_size < 64 ? p.page_size : 64;
     P.boxes_per_tile = kPrefillTile / P.rows_per_box;
     P.sm_scale = p.sm_scale;
-    P.wait_limit_ns = 1000000000ull;
+    take_test_hook(&P.test_skip_it, &P.wait_limit_ns);
     const void* kern = prefill_kernel_ptr(p.head_dim, false);
     const int smem = prefill_smem_bytes(p.head_dim, false);
     if (!kern || smem <= 0) return cudaErrorInvalidValue;
