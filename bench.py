@@ -272,11 +272,16 @@ def oracle_sample(w, name, target_s, keep_first=True):
 # ------------------------------------------------------------------ native
 
 def launches_per_step(w, mode):
+    """Kernels one step launches.  Decode mode: Assign and the decode kernel
+    (bf16: it finalizes its split units and pa_combine launches nothing;
+    E4M3: also Combine).  Prefill mode: Assign (3 kernels), the prefill kernel
+    and Combine, and without a block mask (G <= 16) the decode part's Assign
+    and decode kernel."""
     from paged_attention_gb300 import binding as B
     if mode == B.PA_MODE_DECODE:
-        return 3
+        return 2 if w.kv_dtype == 0 else 3
     G = w.num_q_heads // w.num_kv_heads
-    return 5 + (3 if w.block_mask is None and G <= 16 else 0)
+    return 5 + (2 if w.block_mask is None and G <= 16 else 0)
 
 
 class Case:
@@ -599,9 +604,6 @@ def run_native(args, rank, world, dist):
                 "serial_ms_per_step": round(serial_ms, 4),
                 "serial_value": round(case.rate(serial_ms, world), 2)},
         "roofline": case.roofline(kern_ms, peaks),
-        # decode mode: Assign, compute, Combine.  Prefill mode: Assign (3) +
-        # prefill kernel + Combine, and without a block mask (G <= 16) the
-        # decode part too: its Assign, the decode kernel and its Combine
         "gpu_launches": launches_per_step(case.w_cpu, case.mode) * args.steps,
         "clocks": clk,
         "graph": graph,

@@ -181,8 +181,13 @@ PA_API pa_status pa_assign(const pa_problem* problem, int mode, const int32_t* c
  * Persistent CTAs walk the task map of pa_assign(PA_MODE_DECODE): per 64-token
  * KV tile a page lookup, a TMA load of K and V into a multi-stage shared-memory
  * ring, S = sm_scale * Q K^T, online softmax (fp32), O += P V.  An unsplit
- * unit writes out / lse directly; a split unit writes normalised partial O and
- * its LSE to partial_ws for pa_combine.
+ * unit writes out / lse directly.  A split unit's tasks write normalised
+ * partial O and LSE to partial_ws.  With bf16 K/V each then counts itself
+ * done on a completion counter in assign_ws, and the last one to finish
+ * merges the unit's partials into out / lse ("基于Triton-TLE…", 三.3), so the
+ * call leaves nothing for pa_combine and no task ever waits for another CTA.
+ * With E4M3 K/V the partials are left to pa_combine (in that kernel the
+ * finalizer costs more than the launch it saves).
  *   q: bf16 [total_q_tokens][Hq][D]
  *   k_cache, v_cache: bf16 or E4M3 bytes, NHD or HND (see above)
  *   block_table: int32 [B][max_pages_per_seq]; only entries of pages holding a
@@ -205,19 +210,62 @@ PA_API pa_status pa_decode_splitk(const pa_problem* problem, const void* q, cons
  * tasks: m = max_k lse_k, O = sum_k e^(lse_k - m) O_k / sum_k e^(lse_k - m),
  * lse = m + ln sum_k e^(lse_k - m).  Units with no visible key get O = 0,
  * lse = -inf.  Units written directly by the compute pass are not touched.
- * In prefill mode both task maps of the workspace are finished.
+ * The bf16 decode kernel finalizes its own split units, and a decode-mode
+ * unit always sees at least one key, so for a bf16 decode-mode workspace (and
+ * for the decode part of a prefill-mode one) nothing is left: the call
+ * validates its arguments and returns PA_OK without launching.  It finishes
+ * E4M3 decode-mode maps and, in prefill mode, the prefill map.
  *   mode: the mode assign_ws was built with.
  */
 PA_API pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
                      size_t assign_ws_bytes, const void* partial_ws, size_t partial_ws_bytes,
                      void* out, float* lse, void* stream);
 
+/*
+ * Static split-K decode ("基于Triton-TLE…", 一.2, the Static Split-K
+ * paragraph: a fixed split count, no Assign, a shorter launch chain; 三.3:
+ * the regular split mapping is resolved from the program id, no task map is
+ * built or read).  Every unit (sequence, KV head) is cut into the same number
+ * S of splits: of the U * S tasks (U = B * Hkv), persistent CTA c of N runs
+ * tasks c, c + N, c + 2N, ...; task i is split s = i % S of unit u = i / S
+ * and covers the unit's 64-token KV tiles [s*n/S, (s+1)*n/S) of its n (a unit
+ * of fewer than S tiles has empty splits, which carry no weight).  The compute
+ * is that of pa_decode_splitk (same kernels, same semantics, sliding window
+ * included); split units are finalized in the kernel by the last of their
+ * tasks to finish, so this is one memset and one kernel launch per call.  It
+ * does not rebalance ragged batches: the dynamic path (pa_assign +
+ * pa_decode_splitk) does.
+ *   num_splits: S in 1 .. 64, or 0 for the library's choice (a power of two
+ *     giving each CTA about two tasks or more, at most 16); see
+ *     pa_static_num_splits.
+ *   ws: >= pa_static_workspace_size(problem, num_splits) bytes, 256-byte
+ *     aligned; its first 256 bytes hold the device error word that
+ *     pa_last_device_error reads.  The call clears the error word and the
+ *     completion counters itself (a memset on `stream`); the rest needs no
+ *     initialisation.
+ *   Other arguments as pa_decode_splitk.  Lengths are checked on the device
+ *   as pa_assign checks them (PA_DEV_BAD_LENGTHS; such a sequence's rows are
+ *   not written).
+ */
+PA_API size_t pa_static_workspace_size(const pa_problem* problem, int32_t num_splits);
+/* The split count S that pa_decode_static uses for (problem, num_splits) on
+ * the current device; *splits: host out. */
+PA_API pa_status pa_static_num_splits(const pa_problem* problem, int32_t num_splits,
+                                      int32_t* splits);
+PA_API pa_status pa_decode_static(const pa_problem* problem, int32_t num_splits, const void* q,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, const int32_t* context_lens,
+                                  const int32_t* q_lens, const float* k_scale,
+                                  const float* v_scale, void* ws, size_t ws_bytes, void* out,
+                                  float* lse, void* stream);
+
 /* Size of the fixed device scratch array behind pa_decode_noalloc: 32 MiB. */
 #define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /*
- * Whole decode (Assign, Split-K compute, Combine: the same three passes and
- * results as pa_assign + pa_decode_splitk + pa_combine in PA_MODE_DECODE)
+ * Whole decode (Assign, Split-K compute and, for E4M3 K/V, Combine: the
+ * same passes and results as pa_assign + pa_decode_splitk + pa_combine in
+ * PA_MODE_DECODE)
  * with every workspace taken from a fixed scratch array inside the library
  * instead of caller buffers.  The call allocates nothing: no cudaMalloc, no
  * cudaFree, no allocating library routine.  The pages describe no such entry
@@ -254,7 +302,7 @@ PA_API pa_status pa_combine(const pa_problem* problem, int mode, const void* ass
  *   Arguments as pa_decode_splitk (out and lse receive the final result).
  *   device_error: int32, DEVICE pointer or NULL.  When given, the device
  *     error word of this call (PA_DEV_* bits) is copied there, on `stream`,
- *     after Combine.
+ *     after the last pass.
  */
 PA_API pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void* k_cache,
                                    const void* v_cache, const int32_t* block_table,

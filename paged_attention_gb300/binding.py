@@ -34,7 +34,8 @@ EXPORTED = (
     "pa_status_string", "pa_version", "pa_num_ctas", "pa_assign_workspace_size",
     "pa_partial_workspace_size", "pa_assign", "pa_decode_splitk", "pa_combine", "pa_prefill",
     "pa_read_task_map", "pa_last_device_error", "pa_decode_noalloc",
-    "pa_test_inject_wait_timeout",
+    "pa_test_inject_wait_timeout", "pa_static_workspace_size", "pa_static_num_splits",
+    "pa_decode_static",
 )
 
 PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # size of the library's fixed scratch
@@ -109,6 +110,10 @@ def load(build_if_missing: bool = True):
             "pa_last_device_error": (i32, [vp, ctypes.POINTER(ctypes.c_int32), vp]),
             "pa_decode_noalloc": (i32, [PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pa_test_inject_wait_timeout": (i32, [ctypes.c_int32, ctypes.c_int64]),
+            "pa_static_workspace_size": (sz, [PP, ctypes.c_int32]),
+            "pa_static_num_splits": (i32, [PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+            "pa_decode_static": (i32, [PP, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                       vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -214,6 +219,25 @@ def pa_decode_noalloc(problem, q, k_cache, v_cache, block_table, context_lens, q
     _check(status, "pa_decode_noalloc")
 
 
+def pa_static_workspace_size(problem: PaProblem, num_splits: int = 0) -> int:
+    return int(load().pa_static_workspace_size(ctypes.byref(problem), int(num_splits)))
+
+
+def pa_static_num_splits(problem: PaProblem, num_splits: int = 0) -> int:
+    n = ctypes.c_int32(0)
+    _check(load().pa_static_num_splits(ctypes.byref(problem), int(num_splits), ctypes.byref(n)),
+           "pa_static_num_splits")
+    return int(n.value)
+
+
+def pa_decode_static(problem, num_splits, q, k_cache, v_cache, block_table, context_lens, q_lens,
+                     k_scale, v_scale, ws, out, lse, stream=None):
+    _check(load().pa_decode_static(
+        ctypes.byref(problem), int(num_splits), _p(q), _p(k_cache), _p(v_cache), _p(block_table),
+        _p(context_lens), _p(q_lens), _p(k_scale), _p(v_scale), _p(ws), _nbytes(ws), _p(out),
+        _p(lse), _stream(stream)), "pa_decode_static")
+
+
 def pa_prefill(problem, q, k_cache, v_cache, block_table, context_lens, q_lens, k_scale, v_scale,
                block_mask, assign_ws, partial_ws, out, lse, stream=None):
     _check(load().pa_prefill(
@@ -296,6 +320,33 @@ def run_decode(w, bufs: Optional[Buffers] = None, stream=None) -> Buffers:
                      w.k_scale, w.v_scale, bufs.assign_ws, bufs.partial_ws, bufs.out, bufs.lse,
                      stream)
     pa_combine(p, PA_MODE_DECODE, bufs.assign_ws, bufs.partial_ws, bufs.out, bufs.lse, stream)
+    return bufs
+
+
+class StaticBuffers:
+    """Workspace and outputs of the static split-K path (device memory from torch)."""
+
+    def __init__(self, w, num_splits: int = 0, num_ctas: int = 0):
+        self.problem = problem_from(w, num_ctas=num_ctas)
+        self.num_splits = num_splits
+        n = pa_static_workspace_size(self.problem, num_splits)
+        if n == 0:
+            raise PaError(1, "pa_static_workspace_size")
+        self.ws = torch.empty(n, dtype=torch.uint8, device=w.q.device)
+        self.out = torch.empty((w.total_q, w.num_q_heads, w.head_dim), dtype=torch.bfloat16,
+                               device=w.q.device)
+        self.lse = torch.empty((w.total_q, w.num_q_heads), dtype=torch.float32,
+                               device=w.q.device)
+
+
+def run_decode_static(w, bufs: Optional["StaticBuffers"] = None, num_splits: int = 0,
+                      stream=None) -> "StaticBuffers":
+    """Static split-K decode (one call, no Assign) for a device-resident workload."""
+    if bufs is None:
+        bufs = StaticBuffers(w, num_splits)
+    pa_decode_static(bufs.problem, bufs.num_splits, w.q, w.k_cache, w.v_cache, w.block_table,
+                     w.context_lens, w.q_lens, w.k_scale, w.v_scale, bufs.ws, bufs.out, bufs.lse,
+                     stream)
     return bufs
 
 

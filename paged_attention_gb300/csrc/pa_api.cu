@@ -26,7 +26,8 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
                                    const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
-                                   cudaStream_t stream, bool take_hook = true);
+                                   cudaStream_t stream, bool take_hook = true,
+                                   int static_splits = 0);
 int prefill_smem_bytes(int D, bool fp8);
 const void* prefill_kernel_ptr(int D, bool fp8);
 cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, const void* q,
@@ -273,7 +274,7 @@ pa_status make_prefill_layout(const pa_problem* p, PrefillLayout& M) {
     const int64_t base = align256(M.L.total_bytes);
     for (int64_t* o : {&Ld.off_header, &Ld.off_cta_ptr, &Ld.off_tasks, &Ld.off_task_cta,
                        &Ld.off_units, &Ld.off_ntiles, &Ld.off_prefix, &Ld.off_nsplit,
-                       &Ld.off_slot0, &Ld.off_task0, &Ld.off_fix, &Ld.off_active, &Ld.off_cu_q,
+                       &Ld.off_slot0, &Ld.off_done, &Ld.off_fix, &Ld.off_active, &Ld.off_cu_q,
                        &Ld.off_seq_unit0})
         *o += base;
     Ld.off_err_header = M.L.off_header;
@@ -286,6 +287,36 @@ pa_status make_prefill_layout(const pa_problem* p, PrefillLayout& M) {
     M.total_bytes = base + Ld.total_bytes;
     M.part_off = align256(M.L.partial_bytes);
     M.partial_bytes = M.part_off + Ld.partial_bytes;
+    return PA_OK;
+}
+
+// Static split-K workspace: a 256-byte header (its error word is where
+// pa_last_device_error reads it), the completion counters of the in-kernel
+// finalizer (kDoneWords per unit), then, for S > 1, the partials of the U * S
+// static tasks.  The header and counters are cleared at every call.
+constexpr int kMaxStaticSplits = 64;
+
+int static_splits_for(const pa_problem& p, int num_splits, int N) {
+    if (num_splits > 0) return num_splits;
+    const int64_t U = (int64_t)p.num_seqs * p.num_kv_heads;
+    int64_t want = (2 * (int64_t)N + U - 1) / U;   // about two tasks per CTA at least
+    int S = 1;
+    while (S < want && S < 16) S *= 2;
+    return S;
+}
+
+pa_status make_static_layout(const pa_problem* p, int num_splits, WsLayout& L, int& S) {
+    pa_status st = make_layout(p, PA_MODE_DECODE, L);
+    if (st != PA_OK) return st;
+    if (num_splits < 0 || num_splits > kMaxStaticSplits) return PA_ERR_INVALID_ARG;
+    S = static_splits_for(*p, num_splits, L.N);
+    const int64_t U = (int64_t)p->num_seqs * p->num_kv_heads;
+    L.off_header = 0;
+    L.off_err_header = 0;
+    L.off_done = kHeaderWords * 4;
+    L.total_bytes = align256(L.off_done + U * kDoneWords * 4);
+    L.partial_slots = S > 1 ? U * S : 0;
+    L.partial_bytes = L.partial_slots * (int64_t)L.rows_cap * (L.D + 1) * 4;
     return PA_OK;
 }
 
@@ -359,7 +390,7 @@ bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L)
     L.off_prefix = take((int64_t)L.unit_cap * 8);
     L.off_nsplit = take((int64_t)L.unit_cap * 4);
     L.off_slot0 = take((int64_t)L.unit_cap * 4);
-    L.off_task0 = take((int64_t)L.unit_cap * 4);
+    L.off_done = take((int64_t)L.unit_cap * kDoneWords * 4);
     L.off_fix = take((int64_t)L.unit_cap * 4);
     L.off_active = take(L.has_mask ? (int64_t)L.unit_cap * L.max_kv_tiles * 4 : 4);
     L.off_cu_q = take((int64_t)(p.num_seqs + 1) * 4);
@@ -527,11 +558,14 @@ pa_status pa_combine(const pa_problem* problem, int mode, const void* assign_ws,
     if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
     if (partial_ws_bytes < (size_t)M.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
         return PA_ERR_WORKSPACE;
+    // The bf16 decode kernel finalizes its split units itself (the last task
+    // of a unit to finish merges its partials), and a decode-mode unit always
+    // has a visible key: nothing is left for a bf16 decode-mode map, nor for
+    // the decode part of a prefill-mode workspace (always bf16).  E4M3 decode
+    // maps and the prefill kernel's map need this pass.
+    if (mode == PA_MODE_DECODE && problem->kv_dtype == PA_BF16) return PA_OK;
     const cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_combine(M.L, assign_ws, partial_ws, out, lse, combine_grid(M.L), s);
-    if (e == cudaSuccess && M.split)
-        e = launch_combine(M.Ld, assign_ws, static_cast<const char*>(partial_ws) + M.part_off,
-                           out, lse, combine_grid(M.Ld), s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -571,16 +605,69 @@ pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void
     void* ws = scratch;
     void* partial = scratch + part_off;
     const cudaStream_t s = (cudaStream_t)stream;
-    // Assign resets the error word and rewrites every word read below
+    // Assign resets the error word and the completion counters and rewrites
+    // every word read below
     cudaError_t e = launch_assign(L, context_lens, q_lens, nullptr, ws, s);
     if (e == cudaSuccess)
         e = launch_decode_from_api(p, L, tq, tk, tv, one_box, block_table,
                                    context_lens, q_lens, k_scale, v_scale, ws, partial, out, lse,
                                    s);
-    if (e == cudaSuccess) e = launch_combine(L, ws, partial, out, lse, combine_grid(L), s);
+    // (the bf16 decode kernel finalizes split units itself; E4M3 needs Combine)
+    if (e == cudaSuccess && p.kv_dtype == PA_FP8_E4M3)
+        e = launch_combine(L, ws, partial, out, lse, combine_grid(L), s);
     if (e == cudaSuccess && device_error)
         e = cudaMemcpyAsync(device_error, scratch + L.off_header + H_ERROR * 4, 4,
                             cudaMemcpyDeviceToDevice, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_static_workspace_size(const pa_problem* problem, int32_t num_splits) {
+    WsLayout L;
+    int S = 0;
+    if (make_static_layout(problem, num_splits, L, S) != PA_OK) return 0;
+    return (size_t)(L.total_bytes + L.partial_bytes);
+}
+
+pa_status pa_static_num_splits(const pa_problem* problem, int32_t num_splits, int32_t* out) {
+    if (!out) return PA_ERR_INVALID_ARG;
+    WsLayout L;
+    int S = 0;
+    pa_status st = make_static_layout(problem, num_splits, L, S);
+    if (st != PA_OK) return st;
+    *out = S;
+    return PA_OK;
+}
+
+pa_status pa_decode_static(const pa_problem* problem, int32_t num_splits, const void* q,
+                           const void* k_cache, const void* v_cache, const int32_t* block_table,
+                           const int32_t* context_lens, const int32_t* q_lens,
+                           const float* k_scale, const float* v_scale, void* ws, size_t ws_bytes,
+                           void* out, float* lse, void* stream) {
+    WsLayout L;
+    int S = 0;
+    pa_status st = make_static_layout(problem, num_splits, L, S);
+    if (st != PA_OK) return st;
+    const pa_problem& p = *problem;
+    if (!ws || !aligned(ws, 256)) return PA_ERR_INVALID_ARG;
+    if (ws_bytes < (size_t)(L.total_bytes + L.partial_bytes)) return PA_ERR_WORKSPACE;
+    const cudaStream_t s = (cudaStream_t)stream;
+    // the error word and the completion counters start at zero
+    if (cudaMemsetAsync(ws, 0, (size_t)L.total_bytes, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (p.total_q_tokens == 0) return PA_OK;   // no query row: nothing to compute
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !out ||
+        !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(q_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (p.kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+    CUtensorMap tq, tk, tv;
+    if (!encode_q_map(p, q, p.max_q_len > 0 ? p.max_q_len : 1, &tq)) return PA_ERR_INVALID_ARG;
+    bool one_box = encode_kv_map_one_box(p, k_cache, &tk) && encode_kv_map_one_box(p, v_cache, &tv);
+    if (!one_box && (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv)))
+        return PA_ERR_INVALID_ARG;
+    cudaError_t e = launch_decode_from_api(p, L, tq, tk, tv, one_box, block_table, context_lens,
+                                           q_lens, k_scale, v_scale, ws,
+                                           static_cast<char*>(ws) + L.total_bytes, out, lse, s,
+                                           true, S);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

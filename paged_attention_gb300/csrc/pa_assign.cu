@@ -260,6 +260,7 @@ __device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm, int32_
     int32_t* task_cta = ws_ptr<int32_t>(ws, L.off_task_cta);
     int32_t* cta_ptr = ws_ptr<int32_t>(ws, L.off_cta_ptr);
     int32_t* fix = ws_ptr<int32_t>(ws, L.off_fix);
+    int32_t* done = ws_ptr<int32_t>(ws, L.off_done);
     const int U = header[H_UNITS];
     const int N = L.N;
     const int tid = threadIdx.x;
@@ -299,6 +300,9 @@ __device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm, int32_
             for_each_owner(run, n, w, C, N, [&](int, int, int) { ++S; });
             run += (int64_t)n * w;
             nsplit[u] = S;
+            // completion counters of the in-kernel finalizer of split units
+#pragma unroll
+            for (int i = 0; i < kDoneWords; ++i) done[(int64_t)u * kDoneWords + i] = 0;
             if (cached) c_s[u] = S;
             cnt[0] += S;
             cnt[1] += S > 1 ? S : 0;

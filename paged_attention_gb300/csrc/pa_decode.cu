@@ -37,8 +37,9 @@
 namespace pa {
 
 
-template <int D, int RT, int NG, int STAGES>
+template <int D, int RT, int NG, int STAGES, bool STATIC = false>
 struct DecodeCfg {
+    static constexpr bool kStatic = STATIC;   // static split-K task source (no Assign map)
     static constexpr int kStages = STAGES;
     static constexpr int kProducerWarps = STAGES % 4 == 0 ? 4 : 2;
     static constexpr bool kFP8 = false;
@@ -62,7 +63,8 @@ struct DecodeCfg {
     static constexpr int kOffBar = (kOffMerge + kMergeBytes + 15) / 16 * 16;
     static constexpr int kNumBars = 2 * STAGES + 4;
     static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;   // after the abort flag
-    static constexpr int kSmemBytes = kOffArmed + (4 * (STAGES + 2) + 15) / 16 * 16 + 1024;
+    static constexpr int kOffFlag = kOffArmed + (4 * (STAGES + 2) + 15) / 16 * 16;  // [RT]
+    static constexpr int kSmemBytes = kOffFlag + 16 + 1024;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(kQHalfBytes % 1024 == 0, "Q slot alignment");
     // Group g consumes the tiles with index % NG == g.  Every ring stage must
@@ -74,11 +76,11 @@ struct DecodeCfg {
 };
 
 
-template <int D, int RT, int NG, int STAGES>
+template <int D, int RT, int NG, int STAGES, bool STATIC>
 __global__ void __launch_bounds__(DecodeCfg<D, RT, NG, STAGES>::kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap tmq,
               const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-    using Cfg = DecodeCfg<D, RT, NG, STAGES>;
+    using Cfg = DecodeCfg<D, RT, NG, STAGES, STATIC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -88,6 +90,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     uint64_t* q_empty = q_full + 2;          // 2 slots
     volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
     int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // last phase armed per stage
+    volatile int* fin_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffFlag);
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
     int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);   // device faults
@@ -95,7 +98,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     const uint64_t lim = P.wait_limit_ns;
 
     grid_dependency_wait();   // Assign's task map is complete
-    if (header[H_CTAS] != (int)gridDim.x) {
+    if (!STATIC && header[H_CTAS] != (int)gridDim.x) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(err_hdr, PA_DEV_BAD_LENGTHS);
         return;
     }
@@ -122,11 +125,9 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         }
     };
 
-    const int32_t* cta_ptr = ws_ptr<int32_t>(P.ws, L.off_cta_ptr);
-    const int4* tasks = ws_ptr<int4>(P.ws, L.off_tasks);
-    const int4* units = ws_ptr<int4>(P.ws, L.off_units);
-    const int32_t* cu_q = ws_ptr<int32_t>(P.ws, L.off_cu_q);
-    const int k_begin = cta_ptr[blockIdx.x], k_end = cta_ptr[blockIdx.x + 1];
+    int32_t* done = ws_ptr<int32_t>(P.ws, L.off_done);
+    int k_begin, k_end;
+    cta_task_range<STATIC>(P, k_begin, k_end);
     const int G = L.G, Hq = L.Hq;
 
     if (warp < Cfg::kProducerWarps) {
@@ -144,7 +145,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
             if (((k - k_begin) & 31) == 0)
-                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+                mine = fetch_task_rec<STATIC>(P, k + lane, k_end, lane, err_hdr);
             const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
             const int4 tk = rec.tk;
             const int4 un = rec.un;
@@ -387,15 +388,32 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                     }
                 }
             }
+            if (tk.w >= 0) {
+                // a split unit: the last of its tasks to finish merges the
+                // partials of this row tile into the output (no Combine pass)
+                const int u = tk.x;
+                const int2 sp = unit_splits<STATIC>(P, u);   // (S, first slot)
+                if (split_task_done(done + (int64_t)u * kDoneWords + rt, sp.x, 5 + rt, 128 * NG,
+                                    slice == 0 && lane == 0, fin_flag + rt)) {
+                    constexpr int kRowsPerWarp = 16 / (4 * NG);
+#pragma unroll
+                    for (int i = 0; i < kRowsPerWarp; ++i) {
+                        const int r = 16 * rt + slice * kRowsPerWarp + i;
+                        if (r < R)
+                            finalize_split_row<D / 32>(
+                                P, sp.y, sp.x, r,
+                                (int64_t)(tok_base + r / G) * Hq + hk * G + r % G, lane);
+                    }
+                }
+            }
             named_bar_sync(5 + rt, 128 * NG);
         }
     }
-    grid_launch_dependents();   // Combine may become resident meanwhile
-    // every warp is done; after an abort the producers wait for their copies
-    // still in flight before the CTA exits
+    grid_launch_dependents();
+    // every warp is done: after an abort the producers wait for their copies
+    // still in flight
     __syncthreads();
     if (warp < Cfg::kProducerWarps) decode_drain<Cfg>(full, q_full, armed, abort_flag, warp, lane);
-    __syncthreads();
 }
 
 template <int D, int RT, int NG, int STAGES>
@@ -403,7 +421,8 @@ static cudaError_t launch_variant(const DecodeParams& P, const CUtensorMap& tq,
                                   const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream) {
     using Cfg = DecodeCfg<D, RT, NG, STAGES>;
-    auto kern = decode_kernel<D, RT, NG, STAGES>;
+    auto kern = P.static_splits > 0 ? decode_kernel<D, RT, NG, STAGES, true>
+                                    : decode_kernel<D, RT, NG, STAGES, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -474,7 +493,7 @@ const void* decode_kernel_ptr(const pa_problem& p) {
                                  : nullptr;
     const int D = p.head_dim, RT = bf16_row_tiles(unit_rows(p));
 #define X(d, rt, ng, st) \
-    if (D == d && RT == rt) return (const void*)decode_kernel<d, rt, ng, st>;
+    if (D == d && RT == rt) return (const void*)decode_kernel<d, rt, ng, st, false>;
     PA_DECODE_VARIANTS(X)
 #undef X
     return nullptr;
@@ -496,7 +515,7 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
                                    const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
-                                   cudaStream_t stream, bool take_hook) {
+                                   cudaStream_t stream, bool take_hook, int static_splits) {
     DecodeParams P;
     P.L = L;
     P.block_table = block_table;
@@ -517,6 +536,7 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
     P.q_box_tokens = p.max_q_len > 0 ? p.max_q_len : 1;
     P.kv_one_box = kv_one_box ? 1 : 0;
     P.sm_scale = p.sm_scale;
+    P.static_splits = static_splits;
     P.test_skip_it = -1;
     P.wait_limit_ns = kWaitLimitNs;
     if (take_hook) take_test_hook(&P.test_skip_it, &P.wait_limit_ns);

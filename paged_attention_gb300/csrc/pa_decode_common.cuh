@@ -32,9 +32,94 @@ struct DecodeParams {
     int32_t q_box_tokens;     // tokens per Q TMA box (max q_len)
     int32_t kv_one_box;       // 1: one 5-D TMA box fills both column blocks of a tile
     int32_t test_skip_it;     // test hook: CTA 0 leaves this KV tile's stage unfilled (-1 none)
+    int32_t static_splits;    // 0: tasks from the Assign map; S > 0: static split-K, S splits
     float sm_scale;
     uint64_t wait_limit_ns;
 };
+
+// Static split-K ("基于Triton-TLE…", 一 Static Split-K: a fixed split count,
+// the mapping resolved from the program id, no task map built or read).  Of
+// the U * S static tasks (U = B * Hkv units), CTA c runs c, c + N, c + 2N, ...
+// (N CTAs); task i is split s = i % S of unit u = i / S and covers the unit's
+// KV tiles [s*n/S, (s+1)*n/S) (n tiles; fewer than S leaves empty splits).
+template <bool kMayBeStatic>
+__device__ __forceinline__ void cta_task_range(const DecodeParams& P, int& k_begin, int& k_end) {
+    if (kMayBeStatic && P.static_splits > 0) {
+        const int64_t T = (int64_t)P.L.B * P.L.Hkv * P.static_splits;
+        const int64_t c = blockIdx.x, N = gridDim.x;
+        k_begin = 0;
+        k_end = c < T ? (int)((T - c + N - 1) / N) : 0;
+    } else {
+        const int32_t* cta_ptr = ws_ptr<int32_t>(P.ws, P.L.off_cta_ptr);
+        k_begin = cta_ptr[blockIdx.x];
+        k_end = cta_ptr[blockIdx.x + 1];
+    }
+}
+
+// Record of static task k (k < k_end) of this CTA, for lane `lane`; all 32
+// lanes call it together (the query offset cu_q of the task's sequence -- the
+// sum of the q_lens before it -- is a warp-wide prefix over q_lens).  Lengths
+// are checked as Assign checks them; a sequence that fails gets empty tasks
+// and PA_DEV_BAD_LENGTHS.
+__device__ __forceinline__ TaskRec static_task_rec(const DecodeParams& P, int k, int k_end,
+                                                   int lane, int32_t* err_hdr) {
+    const WsLayout& L = P.L;
+    const int S = P.static_splits;
+    const bool valid = k < k_end;
+    const int64_t i = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+    const int u = valid ? (int)(i / S) : 0, s = valid ? (int)(i % S) : 0;
+    const int b = u / L.Hkv, hk = u - b * L.Hkv;
+    const int q = valid ? P.ql[b] : 0, c = valid ? P.ctx[b] : 0;
+    int cuq = 0, run = 0;
+    const int bmax = __reduce_max_sync(0xffffffffu, valid ? b : 0);
+    for (int c0 = 0; c0 <= bmax; c0 += 32) {
+        const int qq = c0 + lane < L.B ? P.ql[c0 + lane] : 0;
+        const int v = max(0, min(qq, L.max_q_len));
+        int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const int ex = __shfl_sync(0xffffffffu, inc - v, (b - c0) & 31);
+        if (b >= c0 && b < c0 + 32) cuq = run + ex;
+        run += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    TaskRec r;
+    r.tk = make_int4(u, 0, 0, -1);
+    r.un = make_int4(b, hk, 0, 0);
+    r.ctx = c;
+    r.ql = q;
+    r.cuq = cuq;
+    const bool bad = q < 0 || c < q || c > L.max_ctx || q > L.max_q_len || cuq + q > L.total_q;
+    if (valid && bad) set_device_error(err_hdr, PA_DEV_BAD_LENGTHS);
+    if (!valid || bad || q == 0) return r;
+    const int n = (c + kDecodeTile - 1) / kDecodeTile - window_first_tile(L.window, c - q, kDecodeTile);
+    r.tk = make_int4(u, (int)((int64_t)s * n / S), (int)((int64_t)(s + 1) * n / S),
+                     S > 1 ? u * S + s : -1);
+    r.un.w = q;
+    return r;
+}
+
+// Record of task k of this CTA's list, for lane `lane` (all 32 lanes call it):
+// from the Assign map, or the static split-K mapping.  Only the kernel
+// instantiations built with kMayBeStatic carry the static-path code.
+template <bool kMayBeStatic>
+__device__ __forceinline__ TaskRec fetch_task_rec(const DecodeParams& P, int k, int k_end,
+                                                  int lane, int32_t* err_hdr) {
+    if (kMayBeStatic && P.static_splits > 0) return static_task_rec(P, k, k_end, lane, err_hdr);
+    const WsLayout& L = P.L;
+    return load_task_rec(ws_ptr<int4>(P.ws, L.off_tasks), ws_ptr<int4>(P.ws, L.off_units), P.ctx,
+                         P.ql, ws_ptr<int32_t>(P.ws, L.off_cu_q), k, k_end);
+}
+
+// Split count and first partial slot of split unit u.
+template <bool kMayBeStatic>
+__device__ __forceinline__ int2 unit_splits(const DecodeParams& P, int u) {
+    if (kMayBeStatic && P.static_splits > 0) return make_int2(P.static_splits, u * P.static_splits);
+    return make_int2(ws_ptr<int32_t>(P.ws, P.L.off_nsplit)[u],
+                     ws_ptr<int32_t>(P.ws, P.L.off_slot0)[u]);
+}
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a tile written by TMA
 // with the 128-byte swizzle (128-byte rows, 1024-byte aligned tile).
@@ -74,9 +159,6 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                   "every ring stage must stay with one producer warp");
     const WsLayout& L = P.L;
     const int G = L.G;
-    const int4* tasks = ws_ptr<int4>(P.ws, L.off_tasks);
-    const int4* units = ws_ptr<int4>(P.ws, L.off_units);
-    const int32_t* cu_q = ws_ptr<int32_t>(P.ws, L.off_cu_q);
     if (lane == 0) {
         prefetch_tmap(tmq);
         prefetch_tmap(tmk);
@@ -89,7 +171,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
     TaskRec mine;
     for (int k = k_begin; k < k_end; ++k, ++task_it) {
         if (((k - k_begin) & 31) == 0)
-            mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+            mine = fetch_task_rec<Cfg::kStatic>(P, k + lane, k_end, lane, err_hdr);
         const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
         const int4 tk = rec.tk;
         const int4 un = rec.un;
@@ -209,6 +291,76 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
             __syncwarp();
         }
     }
+}
+
+// In-kernel finalizer of split units ("基于Triton-TLE…", 三.3: the partial
+// states of one output are merged by whoever completes it, in place of a
+// separate Combine pass).  Called by every thread of a named-barrier group
+// (bar_id, nthreads) right after the group wrote its rows of a split task's
+// normalised partial: each writer fences, one leader thread counts the task
+// done on done_word, and the group learns (through *flag, shared) whether it
+// was the unit's last task to finish -- S tasks in all -- and so must merge.
+// Nobody waits for another CTA.
+__device__ __forceinline__ bool split_task_done(int32_t* done_word, int S, int bar_id,
+                                                int nthreads, bool leader, volatile int* flag) {
+    __threadfence();
+    named_bar_sync(bar_id, nthreads);
+    if (leader) *flag = atomicAdd(done_word, 1) == S - 1 ? 1 : 0;
+    named_bar_sync(bar_id, nthreads);
+    const bool last = *flag != 0;
+    if (last) __threadfence();
+    return last;
+}
+
+// Row r of a split unit, finalized: m = max_k lse_k, w_k = e^(lse_k - m),
+// out = sum_k w_k O_k / sum_k w_k, lse = m + ln sum_k w_k over its S partials
+// (slots s0 .. s0+S-1).  One warp per row, DPL head_dim elements per lane.
+// The partials were written by other CTAs: read through L2 (ld.cg).
+template <int DPL>
+__device__ __forceinline__ void finalize_split_row(const DecodeParams& P, int s0, int S, int r,
+                                                int64_t out_row, int lane) {
+    const WsLayout& L = P.L;
+    float M = -INFINITY;
+    for (int k = 0; k < S; ++k)
+        M = fmaxf(M, __ldcg(P.part_lse + (int64_t)(s0 + k) * L.rows_cap + r));
+    float den = 0.f;
+    float acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+    if (M != -INFINITY) {
+        for (int k = 0; k < S; ++k) {
+            const int64_t prow = (int64_t)(s0 + k) * L.rows_cap + r;
+            const float lk = __ldcg(P.part_lse + prow);
+            if (lk == -INFINITY) continue;
+            const float w = ex2((lk - M) * kLog2e);
+            den += w;
+            const float* src = P.part_o + prow * L.D + lane * DPL;
+            if constexpr (DPL == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                acc[0] += w * v.x;
+                acc[1] += w * v.y;
+                acc[2] += w * v.z;
+                acc[3] += w * v.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[e] += w * __ldcg(src + e);
+            }
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __nv_bfloat16* dst = P.out + out_row * L.D + lane * DPL;
+    if constexpr (DPL == 4) {
+        uint2 v;
+        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = v;
+    } else {
+#pragma unroll
+        for (int e = 0; e < DPL; e += 2)
+            *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    }
+    if (P.lse != nullptr && lane == 0)
+        P.lse[out_row] = den > 0.f ? M + lg2(den) * kLn2 : -INFINITY;
 }
 
 // After an abort: wait (bounded) until every copy this producer warp armed

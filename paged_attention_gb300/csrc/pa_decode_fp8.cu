@@ -50,8 +50,12 @@
 
 namespace pa {
 
-template <int NT, int STAGES>
+// GENERAL: the instantiation that also takes the static split-K task source
+// and the sliding window; the plain one (the dynamic map, no window) carries
+// neither in its loops.
+template <int NT, int STAGES, bool GENERAL = false>
 struct DecodeFp8Cfg {
+    static constexpr bool kStatic = GENERAL;   // may take the static split-K task source
     static constexpr int D = 128;
     // geometry the shared producer reads
     static constexpr int kStages = STAGES;
@@ -91,7 +95,8 @@ struct DecodeFp8Cfg {
     static constexpr int kOffBar = (kOffScale + kScaleBytes + 15) / 16 * 16;
     static constexpr int kNumBars = 2 * STAGES + 4;
     static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;   // after the abort flag
-    static constexpr int kSmemBytes = kOffArmed + (4 * (STAGES + 2) + 15) / 16 * 16 + 1024;
+    static constexpr int kOffFlag = kOffArmed + (4 * (STAGES + 2) + 15) / 16 * 16;
+    static constexpr int kSmemBytes = kOffFlag + 16 + 1024;
     static_assert(NT >= 1 && NT <= 4, "rows per unit");
     // every ring stage is always consumed by the same group (a group that
     // reused a stage after the other could wait two phases ahead)
@@ -113,11 +118,11 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-template <int NT, int STAGES>
+template <int NT, int STAGES, bool GENERAL>
 __global__ void __launch_bounds__(384, 1)
 decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-    using Cfg = DecodeFp8Cfg<NT, STAGES>;
+    using Cfg = DecodeFp8Cfg<NT, STAGES, GENERAL>;
     static_assert(Cfg::kThreads == 384, "launch bounds");
     constexpr int NG = Cfg::NG;
     constexpr int D = Cfg::D;
@@ -134,6 +139,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     uint64_t* q_empty = q_full + 2;          // 2 slots
     volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
     int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // last phase armed per stage
+    volatile int* fin_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffFlag);
     float* scales = reinterpret_cast<float*>(smem + Cfg::kOffScale);   // [stage][k|v][box]
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
@@ -142,7 +148,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     const uint64_t lim = P.wait_limit_ns;
 
     grid_dependency_wait();   // Assign's task map is complete
-    if (header[H_CTAS] != (int)gridDim.x) {
+    if ((!GENERAL || P.static_splits == 0) && header[H_CTAS] != (int)gridDim.x) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(err_hdr, PA_DEV_BAD_LENGTHS);
         return;
     }
@@ -169,8 +175,8 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
         }
     };
 
-    const int32_t* cta_ptr = ws_ptr<int32_t>(P.ws, L.off_cta_ptr);
-    const int k_begin = cta_ptr[blockIdx.x], k_end = cta_ptr[blockIdx.x + 1];
+    int k_begin, k_end;
+    cta_task_range<GENERAL>(P, k_begin, k_end);
 
     if (warp < 4) {
         regs_dec<Cfg::kRegsProducer>();
@@ -183,9 +189,6 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
         const int grp = cw >> 2, ts = cw & 3;
         const int g = lane >> 2, q4 = lane & 3;
         const int G = L.G, Hq = L.Hq;
-        const int4* tasks = ws_ptr<int4>(P.ws, L.off_tasks);
-        const int4* units = ws_ptr<int4>(P.ws, L.off_units);
-        const int32_t* cu_q = ws_ptr<int32_t>(P.ws, L.off_cu_q);
         const float scale_log2 = P.sm_scale * kLog2e;
         uint8_t* qh = smem + Cfg::kOffQh;
         float* mbuf = reinterpret_cast<float*>(smem + Cfg::kOffMerge);
@@ -209,7 +212,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
         TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
             if (((k - k_begin) & 31) == 0)
-                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+                mine = fetch_task_rec<GENERAL>(P, k + lane, k_end, lane, err_hdr);
             const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
             const int4 tk = rec.tk;
             const int4 un = rec.un;
@@ -218,10 +221,12 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
             const int ctx_b = rec.ctx, ql_b = rec.ql;
             const int tok_base = rec.cuq + q0;
             const int pbase = ctx_b - ql_b + q0;
-            // this thread's rows are 8nt + 2q4 + e; the last key each may see
-            // (-1 for padding rows) and, with a sliding window, the first
-            // ("HiLS-Attention", 二.1 local branch: keys p - window < j <= p)
-            int lastk[NT][2], firstk[NT][2];
+            // this thread's rows are 8nt + 2q4 + e; the last key each may see,
+            // its own position p (p <= ctx - 1 in decode; -1 for padding
+            // rows).  With a sliding window ("HiLS-Attention", 二.1 local
+            // branch) the row sees the keys p - window < j <= p: tok is visible
+            // iff tok <= lastk and tok + win > lastk (win is huge without one).
+            int lastk[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -229,12 +234,12 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     const int r = 8 * nt + 2 * q4 + e;
                     const int pr = pbase + r / G;
                     lastk[nt][e] = r < R ? (pr < ctx_b - 1 ? pr : ctx_b - 1) : -1;
-                    firstk[nt][e] = L.window > 0 ? pr - L.window + 1 : 0;
                 }
+            const int win = GENERAL && L.window > 0 ? L.window : (1 << 30);
             // task positions count from the unit's first visible tile; every
             // row of the unit sees a key when it is >= first_open
-            const int first = window_first_tile(L.window, pbase, kDecodeTile);
-            const int first_open = L.window > 0 ? pbase + nq - L.window : 0;
+            const int first = GENERAL ? window_first_tile(L.window, pbase, kDecodeTile) : 0;
+            const int first_open = GENERAL && L.window > 0 ? pbase + nq - L.window : 0;
 
             // ---- Q of the unit: bf16 slot -> f16 rows in head_dim order, then
             // release the slot.  Every consumer warp has left the previous
@@ -347,7 +352,8 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                 float sv[NT][4];
                 bool need = false;
                 // every row sees every token of the slice: no mask to apply
-                const bool open = R == kRows && tok0 + 15 <= pbase && tok0 >= first_open;
+                const bool open = GENERAL ? R == kRows && tok0 + 15 <= pbase && tok0 >= first_open
+                                          : R == kRows && tok0 + 15 <= pbase;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -356,11 +362,16 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                                                       : sacc[0][nt][e];
                         const float s2 = kChains == 2 ? sacc[0][nt][2 + e] + sacc[1][nt][2 + e]
                                                       : sacc[0][nt][2 + e];
-                        sv[nt][e] = open || (tok <= lastk[nt][e] && tok >= firstk[nt][e])
-                                        ? s0 * cs : -INFINITY;
-                        sv[nt][2 + e] =
-                            open || (tok + 8 <= lastk[nt][e] && tok + 8 >= firstk[nt][e])
-                                ? s2 * cs : -INFINITY;
+                        bool vis0, vis8;
+                        if constexpr (GENERAL) {
+                            vis0 = tok <= lastk[nt][e] && tok + win > lastk[nt][e];
+                            vis8 = tok + 8 <= lastk[nt][e] && tok + 8 + win > lastk[nt][e];
+                        } else {
+                            vis0 = tok <= lastk[nt][e];
+                            vis8 = tok + 8 <= lastk[nt][e];
+                        }
+                        sv[nt][e] = open || vis0 ? s0 * cs : -INFINITY;
+                        sv[nt][2 + e] = open || vis8 ? s2 * cs : -INFINITY;
                         need |= fmaxf(sv[nt][e], sv[nt][2 + e]) > m[nt][e] + 8.f;
                     }
                 if (__any_sync(0xffffffffu, need)) {
@@ -531,14 +542,29 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     if (lane == 0) P.part_lse[prow] = lse_nat;
                 }
             }
+            if constexpr (GENERAL) {
+                // static split-K: the last of a unit's tasks to finish merges
+                // its partials (there is no Combine pass on that path).  With
+                // an Assign map the partials are left to pa_combine: in this
+                // kernel's loop the finalizer costs more than that launch.
+                if (tk.w >= 0 && P.static_splits > 0) {
+                    const int u = tk.x;
+                    const int2 sp = unit_splits<GENERAL>(P, u);   // (S, first slot)
+                    if (split_task_done(ws_ptr<int32_t>(P.ws, L.off_done) + (int64_t)u * kDoneWords,
+                                        sp.x, kBarConsumers, kCT, threadIdx.x == 128, fin_flag))
+                        for (int r = cw; r < R; r += kCW)
+                            finalize_split_row<4>(
+                                P, sp.y, sp.x, r,
+                                (int64_t)(tok_base + r / G) * Hq + hk * G + r % G, lane);
+                }
+            }
         }
     }
-    grid_launch_dependents();   // Combine may become resident meanwhile
-    // every warp is done; after an abort the producers wait for their copies
-    // still in flight before the CTA exits
+    grid_launch_dependents();
+    // every warp is done: after an abort the producers wait for their copies
+    // still in flight
     __syncthreads();
     if (warp < Cfg::kProducerWarps) decode_drain<Cfg>(full, q_full, armed, abort_flag, warp, lane);
-    __syncthreads();
 }
 
 // (8-row tiles, ring stages) built
@@ -568,7 +594,7 @@ int decode_fp8_threads(int nt) {
 
 const void* decode_fp8_kernel_ptr(int nt) {
 #define X(n, st) \
-    if (nt == n) return (const void*)decode_fp8_kernel<n, st>;
+    if (nt == n) return (const void*)decode_fp8_kernel<n, st, false>;
     PA_DECODE_FP8_VARIANTS(X)
 #undef X
     return nullptr;
@@ -579,7 +605,8 @@ static cudaError_t launch_fp8_variant(const DecodeParams& P, const CUtensorMap& 
                                       const CUtensorMap& tk, const CUtensorMap& tv,
                                       cudaStream_t stream) {
     using Cfg = DecodeFp8Cfg<NT, STAGES>;
-    auto kern = decode_fp8_kernel<NT, STAGES>;
+    auto kern = P.static_splits > 0 || P.L.window > 0 ? decode_fp8_kernel<NT, STAGES, true>
+                                                      : decode_fp8_kernel<NT, STAGES, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -30,6 +30,10 @@ constexpr int kDefaultBalanceRows = 128;
 // to the decode kernel, through a second, decode-mode task map.
 constexpr int kMixedDecodeRows = 16;
 constexpr int kHeaderWords = 64;
+// Completion counters per unit in the Assign workspace: one per 16-row tile
+// of a decode unit (the bf16 decode kernel finalizes split units per row
+// tile).
+constexpr int kDoneWords = 4;
 
 // header word indices inside the Assign workspace
 enum HeaderWord {
@@ -76,8 +80,8 @@ struct WsLayout {
     int32_t window;   // sliding window (0 = none): the query at p sees keys p - window < j <= p
     int64_t off_err_header;   // header whose error word device faults go to
     int64_t off_header, off_cta_ptr, off_tasks, off_task_cta, off_units, off_ntiles,
-        off_prefix, off_nsplit, off_slot0, off_task0, off_fix, off_active, off_cu_q,
-        off_seq_unit0;
+        off_prefix, off_nsplit, off_slot0, off_done, off_fix, off_active, off_cu_q,
+        off_seq_unit0;   // off_done: completion counters, kDoneWords per unit
     int64_t total_bytes;
     int64_t partial_slots;
     int64_t partial_bytes;

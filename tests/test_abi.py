@@ -127,3 +127,18 @@ def test_noalloc_host_checks(lib):
     assert B.PA_NOALLOC_SCRATCH_BYTES == 32 * 1024 * 1024
     header = open(os.path.join(ROOT, "include", "pa.h")).read()
     assert "#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)" in header
+
+
+def test_static_workspace_sizes_host_only(lib):
+    """Static split-K: a 256-byte header and 4 completion counters per unit
+    (one per 16-row tile; 256-byte aligned), then U * S partial slots of 16
+    rows x (D + 1) floats for S > 1."""
+    w = W.decode_bf16(mtp=1, shrink=16)
+    p = B.problem_from(w, num_ctas=152)
+    U = w.num_seqs * w.num_kv_heads
+    head = -(-(256 + U * 4 * 4) // 256) * 256
+    assert B.pa_static_workspace_size(p, 1) == head
+    assert B.pa_static_workspace_size(p, 4) == head + U * 4 * 16 * 129 * 4
+    assert B.pa_static_num_splits(p, 3) == 3
+    assert B.pa_static_num_splits(p, 0) >= 1
+    assert B.pa_static_workspace_size(p, 65) == 0          # beyond 64 splits

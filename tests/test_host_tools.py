@@ -35,10 +35,13 @@ def test_launches_per_step():
     pytest.importorskip("torch")
     import bench
     from paged_attention_gb300 import binding as B
-    assert bench.launches_per_step(W.decode_bf16(mtp=1, shrink=16), B.PA_MODE_DECODE) == 3
+    # bf16 decode: Assign + the decode kernel (it finalizes its own split
+    # units); E4M3 decode: and Combine
+    assert bench.launches_per_step(W.decode_bf16(mtp=1, shrink=16), B.PA_MODE_DECODE) == 2
+    assert bench.launches_per_step(W.decode_fp8(shrink=16), B.PA_MODE_DECODE) == 3
     # unmasked prefill-mode batch: 3 Assign + prefill + Combine, and the
-    # decode part's Assign, kernel and Combine
-    assert bench.launches_per_step(W.hybrid_bf16(shrink=16), B.PA_MODE_PREFILL) == 8
+    # decode part's Assign and kernel
+    assert bench.launches_per_step(W.hybrid_bf16(shrink=16), B.PA_MODE_PREFILL) == 7
     assert bench.launches_per_step(W.prefill_bf16(sparse=True, shrink=32), B.PA_MODE_PREFILL) == 5
 
 
