@@ -43,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode attn achieved HBM GB/s; prefill attn TFLOP/s; both as % of GB300 roofline"
 WORKLOADS = ["decode_bf16", "decode_fp8", "prefill_dense", "prefill_sparse", "hybrid",
-             "tiny_mixed"]
+             "tiny_mixed", "decode_bf16_static"]
 # the "configs" object of the default line: (key, workload, mtp)
 CONFIG_SET = [
     ("tiny_mixed", "tiny_mixed", 0),
@@ -54,6 +54,7 @@ CONFIG_SET = [
     ("prefill_dense", "prefill_dense", 0),
     ("prefill_sparse", "prefill_sparse", 0),
     ("hybrid", "hybrid", 0),
+    ("decode_bf16_static", "decode_bf16_static", 1),
 ]
 PARALLELISM = "independent batch per GPU x{world}"
 
@@ -78,7 +79,7 @@ def make_workload(name: str, rank: int, shrink: int = 1, mtp: int = 0):
     2 for E4M3)."""
     from paged_attention_gb300 import workloads as W
     from paged_attention_gb300.dist import rank_seed
-    if name == "decode_bf16":
+    if name in ("decode_bf16", "decode_bf16_static"):
         return W.decode_bf16(mtp=mtp or 1, seed=rank_seed(1002, rank), shrink=shrink)
     if name == "decode_fp8":
         return W.decode_fp8(seed=rank_seed(1003, rank), shrink=shrink, mtp=mtp or 2)
@@ -112,6 +113,11 @@ def workload_config(w, name, world):
 
 def is_decode(name):
     return name.startswith("decode")
+
+
+def is_static(name):
+    """The static split-K path (pa_decode_static) on a decode workload."""
+    return name.endswith("_static")
 
 
 def bytes_metric(name):
@@ -271,13 +277,15 @@ def oracle_sample(w, name, target_s, keep_first=True):
 
 # ------------------------------------------------------------------ native
 
-def launches_per_step(w, mode):
+def launches_per_step(w, mode, static=False):
     """Kernels one step launches.  Decode mode: Assign and the decode kernel
     (bf16: it finalizes its split units and pa_combine launches nothing;
     E4M3: also Combine).  Prefill mode: Assign (3 kernels), the prefill kernel
     and Combine, and without a block mask (G <= 16) the decode part's Assign
     and decode kernel."""
     from paged_attention_gb300 import binding as B
+    if static:
+        return 1
     if mode == B.PA_MODE_DECODE:
         return 2 if w.kv_dtype == 0 else 3
     G = w.num_q_heads // w.num_kv_heads
@@ -301,14 +309,27 @@ class Case:
         self.w = self.w_cpu.to(dev)
         self.work, self.kind = work_of(self.w_cpu, name)
         self.mode = B.PA_MODE_DECODE if is_decode(name) else B.PA_MODE_PREFILL
-        self.bufs = B.make_buffers(self.w, self.mode)
         self.stream = torch.cuda.current_stream()
-        self.runner = B.run_decode if self.mode == B.PA_MODE_DECODE else B.run_prefill
+        if is_static(name):
+            self.bufs = B.StaticBuffers(self.w, 0)
+            self.splits = B.pa_static_num_splits(self.bufs.problem, 0)
+            self.runner = lambda w, bufs: B.run_decode_static(w, bufs)
+        else:
+            self.bufs = B.make_buffers(self.w, self.mode)
+            self.runner = B.run_decode if self.mode == B.PA_MODE_DECODE else B.run_prefill
 
     def step(self, ev=None, w=None, bufs=None):
         B = self.B
         w = w or self.w
         bufs = bufs or self.bufs
+        if is_static(self.name):
+            # one call: the error-word memset and the kernel (no Assign, no Combine)
+            if ev is not None:
+                ev[0].record(self.stream)
+            B.run_decode_static(w, bufs)
+            if ev is not None:
+                ev[1].record(self.stream)
+            return
         p, mode = bufs.problem, self.mode
         B.pa_assign(p, mode, w.context_lens, w.q_lens,
                     w.block_mask if mode == B.PA_MODE_PREFILL else None, bufs.assign_ws)
@@ -327,7 +348,8 @@ class Case:
         B.pa_combine(p, mode, bufs.assign_ws, bufs.partial_ws, bufs.out, bufs.lse)
 
     def device_error(self):
-        return self.B.pa_last_device_error(self.bufs.assign_ws)
+        ws = self.bufs.ws if is_static(self.name) else self.bufs.assign_ws
+        return self.B.pa_last_device_error(ws)
 
     def timed(self, args, dist, uuid):
         """W warm-up steps, then exactly K steps bracketed by a barrier and a
@@ -389,7 +411,9 @@ class Case:
                     "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
         roof["peak_source"] = peaks["source"]
-        roof["kernel"] = "pa_decode_splitk" if self.mode == self.B.PA_MODE_DECODE else "pa_prefill"
+        roof["kernel"] = ("pa_decode_static" if is_static(self.name) else
+                          "pa_decode_splitk" if self.mode == self.B.PA_MODE_DECODE else
+                          "pa_prefill")
         roof["kernel_ms"] = round(kern_ms, 4)
         roof["algorithmic_" + self.kind + "_per_launch"] = int(self.work)
         roof["traffic"] = load_traffic(roof["kernel"], self.name,
@@ -449,7 +473,8 @@ def e2e_measure(case, args, dist, dev):
             wk.block_table = torch.empty_like(w.block_table)
             wk.context_lens = torch.empty_like(w.context_lens)
             wk.q_lens = torch.empty_like(w.q_lens)
-        bk = case.bufs if k == 0 else B.make_buffers(w, case.mode)
+        bk = case.bufs if k == 0 else (B.StaticBuffers(w, 0) if is_static(case.name)
+                                       else B.make_buffers(w, case.mode))
         hout = torch.empty(bk.out.shape, dtype=bk.out.dtype).pin_memory()
         hlse = torch.empty(bk.lse.shape, dtype=bk.lse.dtype).pin_memory()
         sets.append((wk, bk, hout, hlse))
@@ -497,7 +522,8 @@ def e2e_measure(case, args, dist, dev):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
     for wk, bk, hout, hlse in sets:
-        if B.pa_last_device_error(bk.assign_ws) != 0:
+        ws = bk.ws if is_static(case.name) else bk.assign_ws
+        if B.pa_last_device_error(ws) != 0:
             raise SystemExit("device error during the end-to-end run")
     ref = case.bufs.out.cpu()
     for wk, bk, hout, hlse in sets:
@@ -558,10 +584,16 @@ def config_entry(key, name, mtp, args, dev, peaks, uuid):
     entry = {"workload": name, "value": round(case.rate(ms), 2), "unit": case.unit(),
              "ms_per_step": round(ms, 4), "kernel_ms": round(kern_ms, 4),
              "roofline": case.roofline(kern_ms, peaks), "clocks": clk,
-             "gpu_launches": launches_per_step(case.w_cpu, case.mode) * args.steps,
+             "gpu_launches": launches_per_step(case.w_cpu, case.mode, is_static(name))
+             * args.steps,
              "config": workload_config(case.w_cpu, name, 1)}
     if name == "tiny_mixed":
         entry["note"] = "launch-bound: parity workload, time reported only"
+    if is_static(name):
+        entry["static_splits"] = case.splits
+        entry["note"] = ("static split-K (no Assign, no Combine; splits of a unit on one "
+                         "cluster, merged through DSM when S is 2, 4 or 8); the step is one "
+                         "memset and one kernel, timed whole as kernel_ms")
     if not args.no_cpu_baseline:
         s = oracle_sample(case.w_cpu, name, args.config_cpu_seconds)
         entry["cpu_baseline"] = {"value": round(s["value"], 4), "unit": s["unit"],
@@ -604,7 +636,7 @@ def run_native(args, rank, world, dist):
                 "serial_ms_per_step": round(serial_ms, 4),
                 "serial_value": round(case.rate(serial_ms, world), 2)},
         "roofline": case.roofline(kern_ms, peaks),
-        "gpu_launches": launches_per_step(case.w_cpu, case.mode) * args.steps,
+        "gpu_launches": launches_per_step(case.w_cpu, case.mode, is_static(name)) * args.steps,
         "clocks": clk,
         "graph": graph,
     }

@@ -235,9 +235,17 @@ PA_API pa_status pa_combine(const pa_problem* problem, int mode, const void* ass
  * tasks to finish, so this is one memset and one kernel launch per call.  It
  * does not rebalance ragged batches: the dynamic path (pa_assign +
  * pa_decode_splitk) does.
- *   num_splits: S in 1 .. 64, or 0 for the library's choice (a power of two
- *     giving each CTA about two tasks or more, at most 16); see
- *     pa_static_num_splits.
+ *   num_splits: S in 1 .. 64, or 0 for the library's choice (the smallest
+ *     power of two giving each CTA eight tasks or more, at most 4); see
+ *     pa_static_num_splits.  With S = 2, 4 or 8 and a grid that is a multiple
+ *     of S (the library's grid, or problem->num_ctas), and where the kernel
+ *     variant has room for it (bf16 units of <= 16 rows, E4M3 units of <= 24),
+ *     the S splits of a unit run on the S CTAs of one thread-block cluster and
+ *     merge on chip through distributed shared memory (三.3): each CTA
+ *     publishes its split's rows in a shared-memory mailbox, and the CTA of
+ *     rank q merges the rows r = q (mod S) from all mailboxes and writes them;
+ *     no partials go through global memory.  Otherwise the splits merge
+ *     through ws and completion counters.
  *   ws: >= pa_static_workspace_size(problem, num_splits) bytes, 256-byte
  *     aligned; its first 256 bytes hold the device error word that
  *     pa_last_device_error reads.  The call clears the error word and the

@@ -64,7 +64,14 @@ struct DecodeCfg {
     static constexpr int kNumBars = 2 * STAGES + 4;
     static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;   // after the abort flag
     static constexpr int kOffFlag = kOffArmed + (4 * (STAGES + 2) + 15) / 16 * 16;  // [RT]
-    static constexpr int kSmemBytes = kOffFlag + 16 + 1024;
+    // static split-K on a cluster: the DSM mailbox of one task's rows and its
+    // two mbarriers (only where it fits, and for one row tile)
+    static constexpr int kOffMail = kOffFlag + 16;
+    static constexpr int kMailWanted = kQRows * (D + kMailPad) * 4;
+    static constexpr bool kHasMail =
+        STATIC && RT == 1 && kOffMail + kMailWanted + 16 + 1024 <= 232448;
+    static constexpr int kOffMailBar = kOffMail + (kHasMail ? kMailWanted : 0);
+    static constexpr int kSmemBytes = kOffMailBar + 16 + 1024;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(kQHalfBytes % 1024 == 0, "Q slot alignment");
     // Group g consumes the tiles with index % NG == g.  Every ring stage must
@@ -91,6 +98,12 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
     int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // last phase armed per stage
     volatile int* fin_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffFlag);
+    float* mbox = reinterpret_cast<float*>(smem + Cfg::kOffMail);
+    uint64_t* mail_full = reinterpret_cast<uint64_t*>(smem + Cfg::kOffMailBar);
+    uint64_t* mail_empty = mail_full + 1;
+    // static split-K on clusters of S CTAs: split states merged through DSM
+    const bool use_cluster = Cfg::kHasMail && P.cluster_size > 1;
+    const int C = use_cluster ? P.cluster_size : 1;
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
     int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);   // device faults
@@ -113,13 +126,25 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         }
         *abort_flag = 0;
         for (int s = 0; s < STAGES + 2; ++s) armed[s] = -1;
+        if (use_cluster) {
+            mbar_init(mail_full, C);    // one arrival from each CTA of the cluster
+            mbar_init(mail_empty, C);
+        }
         fence_mbar_init();
     }
     __syncthreads();
+    if (use_cluster) cluster_sync_all();   // every peer's barriers initialised
 
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (*abort_flag) return;
         if (!mbar_wait_or_abort(bar, parity, lim, abort_flag)) {
+            *abort_flag = 1;
+            set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
+        }
+    };
+    auto wait_cluster = [&](uint64_t* bar, uint32_t parity) {
+        if (*abort_flag) return;
+        if (!mbar_wait_cluster(bar, parity, lim, abort_flag)) {
             *abort_flag = 1;
             set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
         }
@@ -141,7 +166,8 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         const int g = lane >> 2, q4 = lane & 3;
         const float scale_log2 = P.sm_scale * kLog2e;
         float* merge = reinterpret_cast<float*>(smem + Cfg::kOffMerge);
-        int it = 0, task_it = 0;
+        int it = 0, task_it = 0, mround = 0;
+        const uint32_t rank = use_cluster ? cluster_ctarank() : 0u;
         TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
             if (((k - k_begin) & 31) == 0)
@@ -336,6 +362,10 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                     make_float2(o[j][2], o[j][3]);
             }
             named_bar_sync(5 + rt, 128 * NG);
+            // the mailbox is rewritten below: every peer has read this CTA's
+            // previous round
+            if (use_cluster && tk.w >= 0 && mround > 0)
+                wait_cluster(mail_empty, (uint32_t)((mround - 1) & 1));
             {
                 constexpr int DPL = D / 32;            // elements of D per lane
                 constexpr int kSlices = 4 * NG;
@@ -378,6 +408,11 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                             }
                             if (P.lse != nullptr && lane == 0)
                                 P.lse[(int64_t)token * Hq + head] = lse_nat;
+                        } else if (use_cluster) {
+                            float* dst = mbox + r * (D + kMailPad);
+#pragma unroll
+                            for (int e = 0; e < DPL; ++e) dst[lane * DPL + e] = acc[e] * inv;
+                            if (lane == 0) dst[D] = lse_nat;
                         } else {
                             const int64_t prow = (int64_t)tk.w * L.rows_cap + r;
                             float* dst = P.part_o + prow * D + lane * DPL;
@@ -388,7 +423,23 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                     }
                 }
             }
-            if (tk.w >= 0) {
+            if (use_cluster && tk.w >= 0) {
+                // the cluster's S CTAs hold the S splits of this unit: merge
+                // them through DSM, rows sharded by rank (one row tile here)
+                fence_acq_rel_cluster();
+                named_bar_sync(5 + rt, 128 * NG);
+                if (slice == 0 && lane == 0)
+                    for (int q = 0; q < C; ++q)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(mail_full), (uint32_t)q));
+                wait_cluster(mail_full, (uint32_t)(mround & 1));
+                cluster_merge_rows<D>(P, mbox, R, (int)rank, C, slice, 4 * NG, tok_base, G, Hq,
+                                      hk, lane);
+                named_bar_sync(5 + rt, 128 * NG);
+                if (slice == 0 && lane == 0)
+                    for (int q = 0; q < C; ++q)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(mail_empty), (uint32_t)q));
+                ++mround;
+            } else if (tk.w >= 0) {
                 // a split unit: the last of its tasks to finish merges the
                 // partials of this row tile into the output (no Combine pass)
                 const int u = tk.x;
@@ -414,6 +465,8 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
     // still in flight
     __syncthreads();
     if (warp < Cfg::kProducerWarps) decode_drain<Cfg>(full, q_full, armed, abort_flag, warp, lane);
+    // no CTA leaves while a peer may still read its mailbox or arrive on it
+    if (use_cluster) cluster_sync_all();
 }
 
 template <int D, int RT, int NG, int STAGES>
@@ -421,14 +474,31 @@ static cudaError_t launch_variant(const DecodeParams& P, const CUtensorMap& tq,
                                   const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream) {
     using Cfg = DecodeCfg<D, RT, NG, STAGES>;
-    auto kern = P.static_splits > 0 ? decode_kernel<D, RT, NG, STAGES, true>
-                                    : decode_kernel<D, RT, NG, STAGES, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::kSmemBytes);
+    using CfgS = DecodeCfg<D, RT, NG, STAGES, true>;
+    const bool st = P.static_splits > 0;
+    auto kern = st ? decode_kernel<D, RT, NG, STAGES, true> : decode_kernel<D, RT, NG, STAGES, false>;
+    const int smem = st ? CfgS::kSmemBytes : Cfg::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(kern, dim3(P.L.N), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, P, tq,
-                         tk, tv);
+    if (st && P.cluster_size > 1)
+        e = launch_in_clusters(kern, dim3(P.L.N), dim3(Cfg::kThreads), smem, stream,
+                               P.cluster_size, P, tq, tk, tv);
+    else
+        e = launch_dependent(kern, dim3(P.L.N), dim3(Cfg::kThreads), smem, stream, P, tq, tk, tv);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Static split-K on clusters of C CTAs: 0 if the variant has no DSM mailbox,
+// else the largest grid of co-resident clusters (C * clusters).
+template <int D, int RT, int NG, int STAGES>
+static int cluster_grid_variant(int C) {
+    using CfgS = DecodeCfg<D, RT, NG, STAGES, true>;
+    if (!CfgS::kHasMail) return 0;
+    auto kern = decode_kernel<D, RT, NG, STAGES, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             CfgS::kSmemBytes) != cudaSuccess)
+        return 0;
+    return max_cluster_grid((const void*)kern, CfgS::kThreads, CfgS::kSmemBytes, C);
 }
 
 // (head_dim, row tiles, tile groups, stages) built
@@ -509,13 +579,41 @@ static cudaError_t launch_decode(const DecodeParams& P, int D, int RT, const CUt
     return cudaErrorInvalidValue;
 }
 
+int decode_fp8_cluster_grid(int nt, int C);
+bool decode_fp8_has_mail(int nt);
+
+// Static split-K on clusters of C CTAs for this problem: whether the kernel
+// variant carries the DSM mailbox, and the persistent grid (0 if not).
+bool decode_has_mail(const pa_problem& p) {
+    if (is_fp8(p)) return p.head_dim == 128 && decode_fp8_has_mail(decode_fp8_row_tiles(unit_rows(p)));
+    const int D = p.head_dim, RT = bf16_row_tiles(unit_rows(p));
+#define X(d, rt, ng, st) \
+    if (D == d && RT == rt) return DecodeCfg<d, rt, ng, st, true>::kHasMail;
+    PA_DECODE_VARIANTS(X)
+#undef X
+    return false;
+}
+
+int decode_cluster_grid(const pa_problem& p, int C) {
+    if (is_fp8(p))
+        return p.head_dim == 128 ? decode_fp8_cluster_grid(decode_fp8_row_tiles(unit_rows(p)), C)
+                                 : 0;
+    const int D = p.head_dim, RT = bf16_row_tiles(unit_rows(p));
+#define X(d, rt, ng, st) \
+    if (D == d && RT == rt) return cluster_grid_variant<d, rt, ng, st>(C);
+    PA_DECODE_VARIANTS(X)
+#undef X
+    return 0;
+}
+
 cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
                                    const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, bool kv_one_box,
                                    const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
-                                   cudaStream_t stream, bool take_hook, int static_splits) {
+                                   cudaStream_t stream, bool take_hook, int static_splits,
+                                   int cluster_size) {
     DecodeParams P;
     P.L = L;
     P.block_table = block_table;
@@ -537,6 +635,7 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
     P.kv_one_box = kv_one_box ? 1 : 0;
     P.sm_scale = p.sm_scale;
     P.static_splits = static_splits;
+    P.cluster_size = cluster_size;
     P.test_skip_it = -1;
     P.wait_limit_ns = kWaitLimitNs;
     if (take_hook) take_test_hook(&P.test_skip_it, &P.wait_limit_ns);

@@ -33,6 +33,7 @@ struct DecodeParams {
     int32_t kv_one_box;       // 1: one 5-D TMA box fills both column blocks of a tile
     int32_t test_skip_it;     // test hook: CTA 0 leaves this KV tile's stage unfilled (-1 none)
     int32_t static_splits;    // 0: tasks from the Assign map; S > 0: static split-K, S splits
+    int32_t cluster_size;     // static split-K on clusters of S CTAs (DSM merge); else 1
     float sm_scale;
     uint64_t wait_limit_ns;
 };
@@ -312,6 +313,91 @@ __device__ __forceinline__ bool split_task_done(int32_t* done_word, int S, int b
     return last;
 }
 
+// Writes one output row from the merged sums of its parts: out = acc / den,
+// lse = M + ln den (den = 0: no visible key, out = 0 and lse = -inf).
+template <int DPL>
+__device__ __forceinline__ void write_merged_row(const DecodeParams& P, int64_t out_row,
+                                                 const float (&acc)[DPL], float den, float M,
+                                                 int lane) {
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __nv_bfloat16* dst = P.out + out_row * P.L.D + lane * DPL;
+    if constexpr (DPL == 4) {
+        uint2 v;
+        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = v;
+    } else {
+#pragma unroll
+        for (int e = 0; e < DPL; e += 2)
+            *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    }
+    if (P.lse != nullptr && lane == 0)
+        P.lse[out_row] = den > 0.f ? M + lg2(den) * kLn2 : -INFINITY;
+}
+
+// Cluster-DSM merge of static split-K ("基于Triton-TLE…", 三.3: the CTAs of a
+// hardware cluster publish their partial softmax states into distributed
+// shared memory, merge them on chip, and shard the merge by head).  With
+// static split-K on clusters of C = S CTAs, the C CTAs of a cluster run the
+// C splits of one unit in the same round: task i = c + j*N is split i % S of
+// unit i / S, and for c = kS .. kS+S-1 the unit is the same (N % S == 0) and
+// the split is the CTA's rank.  Each CTA writes its split's normalised rows
+// O_r and lse_r into its own mailbox (rows of D + kMailPad floats, lse at D).
+// Per round:
+//   - every consumer thread fences at cluster scope; after the group barrier
+//     one leader arrives on mail_full of every CTA of the cluster (release);
+//   - all wait for their own mail_full (acquire): C arrivals = every mailbox
+//     of the cluster written;
+//   - the CTA of rank q merges the rows r = q (mod C) from all C mailboxes
+//     through DSM and writes out / lse (no global partial, no Combine);
+//   - after the group barrier the leader arrives on every CTA's mail_empty;
+//     a CTA waits for its own mail_empty (all peers read its mailbox) before
+//     it writes its mailbox again in the next round.
+// All CTAs of a cluster run the same number of rounds (the unit of a round
+// is common to the cluster), and a cluster-wide barrier at the kernel's end
+// keeps every mailbox alive until its readers are done.
+constexpr int kMailPad = 4;   // 16-byte aligned rows
+
+template <int D>
+__device__ __forceinline__ void cluster_merge_rows(const DecodeParams& P, const float* box, int R,
+                                                   int rank, int C, int w, int nw,
+                                                   int64_t row0_out, int G, int Hq, int hk,
+                                                   int lane) {
+    constexpr int DPL = D / 32;
+    constexpr int kStride = D + kMailPad;
+    const uint32_t base = smem_u32(box);
+    for (int r = rank + C * w; r < R; r += C * nw) {
+        const uint32_t row = base + (uint32_t)(r * kStride) * 4u;
+        float M = -INFINITY;
+        for (int q = 0; q < C; ++q) M = fmaxf(M, ld_dsm_f32(mapa_shared(row + D * 4, q)));
+        float den = 0.f;
+        float acc[DPL];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+        if (M != -INFINITY) {
+            for (int q = 0; q < C; ++q) {
+                const float lq = ld_dsm_f32(mapa_shared(row + D * 4, q));
+                if (lq == -INFINITY) continue;
+                const float wq = ex2((lq - M) * kLog2e);
+                den += wq;
+                const uint32_t src = mapa_shared(row + (uint32_t)(lane * DPL) * 4u, q);
+                if constexpr (DPL == 4) {
+                    const float4 v = ld_dsm_f32x4(src);
+                    acc[0] += wq * v.x;
+                    acc[1] += wq * v.y;
+                    acc[2] += wq * v.z;
+                    acc[3] += wq * v.w;
+                } else {
+                    const float2 v = ld_dsm_f32x2(src);
+                    acc[0] += wq * v.x;
+                    acc[1] += wq * v.y;
+                }
+            }
+        }
+        write_merged_row<DPL>(P, (row0_out + r / G) * Hq + hk * G + r % G, acc, den, M, lane);
+    }
+}
+
 // Row r of a split unit, finalized: m = max_k lse_k, w_k = e^(lse_k - m),
 // out = sum_k w_k O_k / sum_k w_k, lse = m + ln sum_k w_k over its S partials
 // (slots s0 .. s0+S-1).  One warp per row, DPL head_dim elements per lane.
@@ -347,20 +433,7 @@ __device__ __forceinline__ void finalize_split_row(const DecodeParams& P, int s0
             }
         }
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    __nv_bfloat16* dst = P.out + out_row * L.D + lane * DPL;
-    if constexpr (DPL == 4) {
-        uint2 v;
-        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2*>(dst) = v;
-    } else {
-#pragma unroll
-        for (int e = 0; e < DPL; e += 2)
-            *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-    }
-    if (P.lse != nullptr && lane == 0)
-        P.lse[out_row] = den > 0.f ? M + lg2(den) * kLn2 : -INFINITY;
+    write_merged_row<DPL>(P, out_row, acc, den, M, lane);
 }
 
 // After an abort: wait (bounded) until every copy this producer warp armed

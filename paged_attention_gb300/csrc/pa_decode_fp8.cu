@@ -96,7 +96,13 @@ struct DecodeFp8Cfg {
     static constexpr int kNumBars = 2 * STAGES + 4;
     static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;   // after the abort flag
     static constexpr int kOffFlag = kOffArmed + (4 * (STAGES + 2) + 15) / 16 * 16;
-    static constexpr int kSmemBytes = kOffFlag + 16 + 1024;
+    // static split-K on a cluster: the DSM mailbox of one task's rows and its
+    // two mbarriers (only where it fits)
+    static constexpr int kOffMail = kOffFlag + 16;
+    static constexpr int kMailWanted = kRows * (D + kMailPad) * 4;
+    static constexpr bool kHasMail = GENERAL && kOffMail + kMailWanted + 16 + 1024 <= 232448;
+    static constexpr int kOffMailBar = kOffMail + (kHasMail ? kMailWanted : 0);
+    static constexpr int kSmemBytes = kOffMailBar + 16 + 1024;
     static_assert(NT >= 1 && NT <= 4, "rows per unit");
     // every ring stage is always consumed by the same group (a group that
     // reused a stage after the other could wait two phases ahead)
@@ -140,6 +146,12 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + 2);
     int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // last phase armed per stage
     volatile int* fin_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffFlag);
+    float* mbox = reinterpret_cast<float*>(smem + Cfg::kOffMail);
+    uint64_t* mail_full = reinterpret_cast<uint64_t*>(smem + Cfg::kOffMailBar);
+    uint64_t* mail_empty = mail_full + 1;
+    // static split-K on clusters of S CTAs: split states merged through DSM
+    const bool use_cluster = Cfg::kHasMail && P.static_splits > 0 && P.cluster_size > 1;
+    const int C = use_cluster ? P.cluster_size : 1;
     float* scales = reinterpret_cast<float*>(smem + Cfg::kOffScale);   // [stage][k|v][box]
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
@@ -163,13 +175,25 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
         }
         *abort_flag = 0;
         for (int s = 0; s < STAGES + 2; ++s) armed[s] = -1;
+        if (use_cluster) {
+            mbar_init(mail_full, C);    // one arrival from each CTA of the cluster
+            mbar_init(mail_empty, C);
+        }
         fence_mbar_init();
     }
     __syncthreads();
+    if (use_cluster) cluster_sync_all();   // every peer's barriers initialised
 
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (*abort_flag) return;
         if (!mbar_wait_or_abort(bar, parity, lim, abort_flag)) {
+            *abort_flag = 1;
+            set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
+        }
+    };
+    auto wait_cluster = [&](uint64_t* bar, uint32_t parity) {
+        if (*abort_flag) return;
+        if (!mbar_wait_cluster(bar, parity, lim, abort_flag)) {
             *abort_flag = 1;
             set_device_error(err_hdr, PA_DEV_WAIT_TIMEOUT);
         }
@@ -208,7 +232,8 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                                   swz(kr0 + 8, 2 * q4 + 1)};
         const uint32_t voff[4] = {swz(vr0, g), swz(vr0 + 1, g), swz(vr0 + 8, g),
                                   swz(vr0 + 9, g)};
-        int it = 0, task_it = 0;
+        int it = 0, task_it = 0, mround = 0;
+        const uint32_t rank = use_cluster ? cluster_ctarank() : 0u;
         TaskRec mine;
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
             if (((k - k_begin) & 31) == 0)
@@ -504,6 +529,10 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
             } else {
                 put(false);
             }
+            // the mailbox is rewritten below: every peer has read this CTA's
+            // previous round
+            if (use_cluster && tk.w >= 0 && mround > 0)
+                wait_cluster(mail_empty, (uint32_t)((mround - 1) & 1));
             named_bar_sync(kBarConsumers, kCT);
             // one warp per row, 4 head_dim values per lane
             for (int r = cw; r < R; r += kCW) {
@@ -535,6 +564,11 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     v.y = pack_bf16x2(acc.z * inv, acc.w * inv);
                     *reinterpret_cast<uint2*>(P.out + ((int64_t)token * Hq + head) * D + 4 * lane) = v;
                     if (P.lse != nullptr && lane == 0) P.lse[(int64_t)token * Hq + head] = lse_nat;
+                } else if (use_cluster) {
+                    float* dst = mbox + r * (D + kMailPad);
+                    *reinterpret_cast<float4*>(dst + 4 * lane) =
+                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    if (lane == 0) dst[D] = lse_nat;
                 } else {
                     const int64_t prow = (int64_t)tk.w * L.rows_cap + r;
                     *reinterpret_cast<float4*>(P.part_o + prow * D + 4 * lane) =
@@ -542,12 +576,29 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
                     if (lane == 0) P.part_lse[prow] = lse_nat;
                 }
             }
+            if (use_cluster && tk.w >= 0) {
+                // the cluster's S CTAs hold the S splits of this unit: merge
+                // them through DSM, rows sharded by rank
+                fence_acq_rel_cluster();
+                named_bar_sync(kBarConsumers, kCT);
+                if (threadIdx.x == 128)
+                    for (int q = 0; q < C; ++q)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(mail_full), (uint32_t)q));
+                wait_cluster(mail_full, (uint32_t)(mround & 1));
+                cluster_merge_rows<D>(P, mbox, R, (int)rank, C, cw, kCW, tok_base, G, Hq, hk,
+                                      lane);
+                named_bar_sync(kBarConsumers, kCT);
+                if (threadIdx.x == 128)
+                    for (int q = 0; q < C; ++q)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(mail_empty), (uint32_t)q));
+                ++mround;
+            }
             if constexpr (GENERAL) {
                 // static split-K: the last of a unit's tasks to finish merges
                 // its partials (there is no Combine pass on that path).  With
                 // an Assign map the partials are left to pa_combine: in this
                 // kernel's loop the finalizer costs more than that launch.
-                if (tk.w >= 0 && P.static_splits > 0) {
+                if (tk.w >= 0 && P.static_splits > 0 && !use_cluster) {
                     const int u = tk.x;
                     const int2 sp = unit_splits<GENERAL>(P, u);   // (S, first slot)
                     if (split_task_done(ws_ptr<int32_t>(P.ws, L.off_done) + (int64_t)u * kDoneWords,
@@ -565,6 +616,8 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     // still in flight
     __syncthreads();
     if (warp < Cfg::kProducerWarps) decode_drain<Cfg>(full, q_full, armed, abort_flag, warp, lane);
+    // no CTA leaves while a peer may still read its mailbox or arrive on it
+    if (use_cluster) cluster_sync_all();
 }
 
 // (8-row tiles, ring stages) built
@@ -605,14 +658,45 @@ static cudaError_t launch_fp8_variant(const DecodeParams& P, const CUtensorMap& 
                                       const CUtensorMap& tk, const CUtensorMap& tv,
                                       cudaStream_t stream) {
     using Cfg = DecodeFp8Cfg<NT, STAGES>;
-    auto kern = P.static_splits > 0 || P.L.window > 0 ? decode_fp8_kernel<NT, STAGES, true>
-                                                      : decode_fp8_kernel<NT, STAGES, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::kSmemBytes);
+    using CfgG = DecodeFp8Cfg<NT, STAGES, true>;
+    const bool general = P.static_splits > 0 || P.L.window > 0;
+    auto kern = general ? decode_fp8_kernel<NT, STAGES, true> : decode_fp8_kernel<NT, STAGES, false>;
+    const int smem = general ? CfgG::kSmemBytes : Cfg::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(kern, dim3(P.L.N), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, P, tq,
-                         tk, tv);
+    if (P.static_splits > 0 && P.cluster_size > 1)
+        e = launch_in_clusters(kern, dim3(P.L.N), dim3(Cfg::kThreads), smem, stream,
+                               P.cluster_size, P, tq, tk, tv);
+    else
+        e = launch_dependent(kern, dim3(P.L.N), dim3(Cfg::kThreads), smem, stream, P, tq, tk, tv);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int NT, int STAGES>
+static int fp8_cluster_grid_variant(int C) {
+    using CfgG = DecodeFp8Cfg<NT, STAGES, true>;
+    if (!CfgG::kHasMail) return 0;
+    auto kern = decode_fp8_kernel<NT, STAGES, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             CfgG::kSmemBytes) != cudaSuccess)
+        return 0;
+    return max_cluster_grid((const void*)kern, CfgG::kThreads, CfgG::kSmemBytes, C);
+}
+
+bool decode_fp8_has_mail(int nt) {
+#define X(n, st) \
+    if (nt == n) return DecodeFp8Cfg<n, st, true>::kHasMail;
+    PA_DECODE_FP8_VARIANTS(X)
+#undef X
+    return false;
+}
+
+int decode_fp8_cluster_grid(int nt, int C) {
+#define X(n, st) \
+    if (nt == n) return fp8_cluster_grid_variant<n, st>(C);
+    PA_DECODE_FP8_VARIANTS(X)
+#undef X
+    return 0;
 }
 
 cudaError_t launch_decode_fp8(const DecodeParams& P, int nt, const CUtensorMap& tq,

@@ -100,7 +100,9 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D>
+// WINDOW: the instantiation that takes a sliding window; the other one
+// carries no window arithmetic in its softmax.
+template <int D, bool WINDOW>
 __global__ void __launch_bounds__(384, 1)
 prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ CUtensorMap tmq,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -182,7 +184,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     // (position p0 = ctx - q_len + q0; 0 without a sliding window) onwards
     auto tile_of = [&](int u, int t, int p0) -> int {
         return L.has_mask ? active[(int64_t)u * L.max_kv_tiles + t]
-                          : t + window_first_tile(L.window, p0, kPrefillTile);
+                          : t + (WINDOW ? window_first_tile(L.window, p0, kPrefillTile) : 0);
     };
 
     if (warp < 4) {
@@ -457,7 +459,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             const int key_last = p_row < ctx_b - 1 ? p_row : ctx_b - 1;
             // first key this row sees: p - window + 1 with a sliding window
             // ("HiLS-Attention", 二.1 local branch)
-            const int key_first = L.window > 0 ? p_row - L.window + 1 : -(1 << 30);
+            const int key_first = WINDOW ? p_row - L.window + 1 : -(1 << 30);
             const int p0 = ctx_b - rec.ql + q0;
             const int n = rec.tk.z - rec.tk.y;
             // a warp whose 32 rows are all padding (units of a few rows: short
@@ -493,14 +495,14 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     tmem_wait_ld();
                     reg_fence32(s);
                     const int lim = limc - c4 * 32, low = lowc - c4 * 32;
-                    if (lim >= 31 && low <= 0) {
+                    if (lim >= 31 && (!WINDOW || low <= 0)) {
 #pragma unroll
                         for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            mx4[c & 3] =
-                                fmaxf(mx4[c & 3], (c <= lim && c >= low) ? s[c] : -INFINITY);
+                            mx4[c & 3] = fmaxf(mx4[c & 3], (c <= lim && (!WINDOW || c >= low))
+                                                               ? s[c] : -INFINITY);
                     }
                 }
                 const float mx =
@@ -529,7 +531,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     reg_fence32(s);
                     const int lim = limc - c4 * 32, low = lowc - c4 * 32;
                     uint32_t pk[16];
-                    if (lim >= 31 && low <= 0) {
+                    if (lim >= 31 && (!WINDOW || low <= 0)) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
                             const uint32_t e2 = ex2_h2(fmaf(s[c], scale_log2, -mu),
@@ -541,9 +543,9 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
-                            const float e0 = (c <= lim && c >= low)
+                            const float e0 = (c <= lim && (!WINDOW || c >= low))
                                                  ? ex2(fmaf(s[c], scale_log2, -mu)) : 0.f;
-                            const float e1 = (c + 1 <= lim && c + 1 >= low)
+                            const float e1 = (c + 1 <= lim && (!WINDOW || c + 1 >= low))
                                                  ? ex2(fmaf(s[c + 1], scale_log2, -mu)) : 0.f;
                             sum4[(c >> 1) & 3] += e0 + e1;
                             pk[c >> 1] = pack_bf16x2(e0, e1);
@@ -655,8 +657,8 @@ int prefill_threads() { return 384; }
 
 const void* prefill_kernel_ptr(int D, bool fp8) {
     if (fp8) return nullptr;
-    if (D == 128) return (const void*)prefill_kernel<128>;
-    if (D == 64) return (const void*)prefill_kernel<64>;
+    if (D == 128) return (const void*)prefill_kernel<128, false>;
+    if (D == 64) return (const void*)prefill_kernel<64, false>;
     return nullptr;
 }
 
@@ -686,17 +688,26 @@ cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, cons
     P.boxes_per_tile = kPrefillTile / P.rows_per_box;
     P.sm_scale = p.sm_scale;
     take_test_hook(&P.test_skip_it, &P.wait_limit_ns);
-    const void* kern = prefill_kernel_ptr(p.head_dim, false);
+    const bool win = p.window > 0;
+    const void* kern =
+        p.head_dim == 128 ? (win ? (const void*)prefill_kernel<128, true>
+                                 : (const void*)prefill_kernel<128, false>)
+        : p.head_dim == 64 ? (win ? (const void*)prefill_kernel<64, true>
+                                  : (const void*)prefill_kernel<64, false>)
+                           : nullptr;
     const int smem = prefill_smem_bytes(p.head_dim, false);
     if (!kern || smem <= 0) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    const dim3 grid(L.N), block(PrefillCfg<128>::kThreads);
     if (p.head_dim == 128)
-        e = launch_dependent(prefill_kernel<128>, dim3(L.N), dim3(PrefillCfg<128>::kThreads), smem,
-                             stream, P, tq, tk, tv);
+        e = win ? launch_dependent(prefill_kernel<128, true>, grid, block, smem, stream, P, tq, tk, tv)
+                : launch_dependent(prefill_kernel<128, false>, grid, block, smem, stream, P, tq, tk,
+                                   tv);
     else
-        e = launch_dependent(prefill_kernel<64>, dim3(L.N), dim3(PrefillCfg<64>::kThreads), smem,
-                             stream, P, tq, tk, tv);
+        e = win ? launch_dependent(prefill_kernel<64, true>, grid, block, smem, stream, P, tq, tk, tv)
+                : launch_dependent(prefill_kernel<64, false>, grid, block, smem, stream, P, tq, tk,
+                                   tv);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

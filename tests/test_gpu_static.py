@@ -125,3 +125,40 @@ def test_static_is_deterministic_and_replays_from_a_graph():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(bufs.out, o1) and torch.equal(bufs.lse, l1)
+
+
+@pytest.mark.parametrize("S,n", [(2, 38), (4, 152), (8, 16), (8, 0), (2, 0)])
+def test_static_cluster_dsm_merge(S, n):
+    """S in {2, 4, 8} with a grid that is a multiple of S: the splits of a
+    unit run on the S CTAs of one hardware cluster and merge through
+    distributed shared memory ("基于Triton-TLE…", 三.3).  bf16 (8 and 16 rows
+    per unit) and E4M3 (24 rows), windows, q_len 0, units with fewer tiles
+    than S."""
+    run_and_compare(W.decode_bf16(mtp=1, shrink=8), S, num_ctas=n)
+    run_and_compare(W.decode_bf16(mtp=3, shrink=16), S, num_ctas=n)
+    run_and_compare(W.decode_fp8(shrink=16), S, num_ctas=n)
+    w = W.make_workload("cl", [1, 70, 5, 900, 3000, 64], [1, 2, 0, 3, 3, 3], num_q_heads=32,
+                        num_kv_heads=8, head_dim=128, page_size=16, seed=S + n)
+    w.window = 200
+    run_and_compare(w, S, num_ctas=n)
+
+
+def test_static_cluster_and_partials_agree():
+    """The same static split through DSM (grid a multiple of S) and through the
+    partial workspace (a grid that is not) give outputs within rounding."""
+    w = W.decode_bf16(mtp=2, shrink=8).to("cuda")
+    a = B.StaticBuffers(w, 4, num_ctas=40)
+    b = B.StaticBuffers(w, 4, num_ctas=41)
+    # the partial area (after the header and counters, i.e. the whole S = 1
+    # workspace) is filled with a sentinel: the DSM path never writes it
+    head = B.pa_static_workspace_size(a.problem, 1)
+    a.ws[head:].fill_(0xA5)
+    b.ws[head:].fill_(0xA5)
+    B.run_decode_static(w, a)
+    B.run_decode_static(w, b)
+    torch.cuda.synchronize()
+    assert B.pa_last_device_error(a.ws) == 0 and B.pa_last_device_error(b.ws) == 0
+    assert bool((a.ws[head:] == 0xA5).all()), "cluster mode wrote partials"
+    assert not bool((b.ws[head:] == 0xA5).all()), "partial mode wrote no partials"
+    assert (a.out.float() - b.out.float()).abs().max().item() <= 1e-2
+    assert (a.lse - b.lse).abs().max().item() <= 1e-5
