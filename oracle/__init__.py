@@ -52,6 +52,9 @@ class OracleProblem(ctypes.Structure):
         ("mask_tile", ctypes.c_int32),
         ("sm_scale", ctypes.c_double),
         ("window", ctypes.c_int32),
+        ("q_dtype", ctypes.c_int32),
+        ("q_scale_mode", ctypes.c_int32),
+        ("kv_scale_mode", ctypes.c_int32),
     ]
 
 
@@ -78,7 +81,7 @@ def _load():
             vp = ctypes.c_void_p
             lib.oracle_attention.restype = ctypes.c_int
             lib.oracle_attention.argtypes = [
-                P(OracleProblem), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                P(OracleProblem), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, ctypes.c_int]
             lib.oracle_assign.restype = ctypes.c_int
             lib.oracle_assign.argtypes = [
@@ -146,7 +149,9 @@ def attention(w, rows=None, key_lo=0, key_hi=INT64_MAX, mask=True, num_threads=0
     Returns (out [n_rows, D] float64, lse [n_rows] float64).
     """
     lib = _load()
-    q = _arr(w.q, np.uint16)
+    q_dtype = int(getattr(w, "q_dtype", 0))
+    q = _arr(w.q, np.uint16 if q_dtype == 0 else np.uint8)
+    qs = _arr(w.q_scale, np.float32) if q_dtype == 1 else None
     kc = _arr(w.k_cache, np.uint16 if w.kv_dtype == 0 else np.uint8)
     vc = _arr(w.v_cache, np.uint16 if w.kv_dtype == 0 else np.uint8)
     ks = _arr(w.k_scale, np.float32) if w.kv_dtype == 1 else None
@@ -168,10 +173,13 @@ def attention(w, rows=None, key_lo=0, key_hi=INT64_MAX, mask=True, num_threads=0
         max_pages_per_seq=bt.shape[1], layout=w.layout, kv_dtype=w.kv_dtype,
         mask_q_tiles=(bm.shape[1] if bm is not None else 0),
         mask_kv_tiles=(bm.shape[2] if bm is not None else 0),
-        mask_tile=w.mask_tile, sm_scale=float(w.sm_scale), window=int(getattr(w, "window", 0)))
+        mask_tile=w.mask_tile, sm_scale=float(w.sm_scale), window=int(getattr(w, "window", 0)),
+        q_dtype=q_dtype,
+        q_scale_mode=int(getattr(w, "q_scale_mode", 0)),
+        kv_scale_mode=int(getattr(w, "kv_scale_mode", 0)))
     out = np.zeros((n_rows, w.head_dim), dtype=np.float64)
     lse = np.zeros((n_rows,), dtype=np.float64)
-    rc = lib.oracle_attention(ctypes.byref(prob), _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks),
+    rc = lib.oracle_attention(ctypes.byref(prob), _ptr(q), _ptr(qs), _ptr(kc), _ptr(vc), _ptr(ks),
                               _ptr(vs), _ptr(bt), _ptr(ctx), _ptr(ql), _ptr(bm), _ptr(rows_a),
                               n_rows, int(key_lo), int(key_hi), _ptr(out), _ptr(lse),
                               int(num_threads))

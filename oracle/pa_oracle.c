@@ -58,6 +58,10 @@ typedef struct {
     int32_t window;            /* 0: none; else sliding window: query p sees keys
                                   p - window < j <= p ("HiLS-Attention", 二.1
                                   local branch; the bounds are our reading) */
+    int32_t q_dtype;           /* 0 = bf16 bit patterns; 1 = E4M3FN bytes times q_scale */
+    int32_t q_scale_mode;      /* E4M3 Q: 0 = one scale; 1 = one per (token, q head) */
+    int32_t kv_scale_mode;     /* E4M3 K/V: 0 = one scale per (page, KV head);
+                                  1 = one scale for the whole cache             */
 } oracle_problem;
 
 /* ---------------------------------------------------------------- decoding */
@@ -117,7 +121,21 @@ static double kv_value(const oracle_problem* P, const void* cache, const float* 
 {
     if (P->kv_dtype == 0)
         return oracle_bf16_to_double(((const uint16_t*)cache)[off + d]);
-    return oracle_e4m3_to_double(((const uint8_t*)cache)[off + d]) * (double)scale[scale_idx];
+    return oracle_e4m3_to_double(((const uint8_t*)cache)[off + d]) *
+           (double)scale[P->kv_scale_mode == 1 ? 0 : scale_idx];
+}
+
+/* Element d of query row (token, h): bf16 decoded, or the E4M3 byte decoded
+ * times its scale (one for the tensor, or one per (token, q head): the two
+ * FP8 quantisation types of "基于Triton-TLE…", 二 / 三). */
+static double q_value(const oracle_problem* P, const void* q, const float* q_scale,
+                      int64_t token, int h, int d)
+{
+    const int64_t i = (token * P->num_q_heads + h) * (int64_t)P->head_dim + d;
+    if (P->q_dtype == 0)
+        return oracle_bf16_to_double(((const uint16_t*)q)[i]);
+    return oracle_e4m3_to_double(((const uint8_t*)q)[i]) *
+           (double)q_scale[P->q_scale_mode == 1 ? token * P->num_q_heads + h : 0];
 }
 
 /* Visibility of key j to local query i of sequence b: inside the context,
@@ -155,11 +173,14 @@ static int visible(const oracle_problem* P, const uint8_t* mask, int b, int i, i
  * the visibility rule of [HYB]).  key_lo/key_hi restrict the keys (used to
  * build split-K partials); pass 0 and INT64_MAX for the full range.
  *
- * q: bf16 bits [total_tokens][Hq][D].  rows == NULL means all rows in order.
+ * q: bf16 bits, or E4M3 bytes (q_dtype 1), [total_tokens][Hq][D]; q_scale:
+ * fp32 [1] or [total_tokens][Hq] (E4M3 Q only).  rows == NULL means all rows
+ * in order.
  * out: [n_rows][D], lse: [n_rows].  Returns 0, or -1 on bad arguments,
  * -2 if a block-table entry used is outside the pool, -3 if ql > ctx.
  */
-int oracle_attention(const oracle_problem* P, const uint16_t* q, const void* k_cache,
+int oracle_attention(const oracle_problem* P, const void* q, const float* q_scale,
+                     const void* k_cache,
                      const void* v_cache, const float* k_scale, const float* v_scale,
                      const int32_t* block_table, const int32_t* context_lens,
                      const int32_t* q_lens, const uint8_t* block_mask, const int64_t* rows,
@@ -173,6 +194,8 @@ int oracle_attention(const oracle_problem* P, const uint16_t* q, const void* k_c
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P->page_size <= 0)
         return -1;
     if (P->kv_dtype == 1 && (!k_scale || !v_scale))
+        return -1;
+    if (P->q_dtype == 1 && !q_scale)
         return -1;
     cu = (int64_t*)malloc(sizeof(int64_t) * (size_t)(B + 1));
     if (!cu)
@@ -214,7 +237,6 @@ int oracle_attention(const oracle_problem* P, const uint16_t* q, const void* k_c
             int64_t p;
             double m = -INFINITY, L = 0.0;
             double* o = out + r * D;
-            const uint16_t* qrow = q + (token * Hq + h) * (int64_t)D;
             if (token < 0 || token >= total) {
 #pragma omp atomic write
                 status = -1;
@@ -242,7 +264,8 @@ int oracle_attention(const oracle_problem* P, const uint16_t* q, const void* k_c
                     continue;
                 }
                 for (d = 0; d < D; ++d)
-                    acc += oracle_bf16_to_double(qrow[d]) * kv_value(P, k_cache, k_scale, off, si, d);
+                    acc += q_value(P, q, q_scale, token, h, d) *
+                           kv_value(P, k_cache, k_scale, off, si, d);
                 s[j] = P->sm_scale * acc;
                 if (!any || s[j] > m)
                     m = s[j];

@@ -71,6 +71,10 @@ class Workload:
     mask_tile: int = 128
     mode: str = "decode"                  # which Assign mode the workload is run with
     window: int = 0                       # sliding window (0 = none): keys p - window < j <= p
+    q_dtype: int = BF16                   # BF16, or FP8_E4M3 bytes times q_scale
+    q_scale: Optional[torch.Tensor] = None    # fp32 [1] or [total_q, Hq] (E4M3 Q only)
+    q_scale_mode: int = 0                 # 0: one Q scale; 1: one per (token, q head)
+    kv_scale_mode: int = 0                # E4M3 K/V: 0 per (page, KV head); 1 one per cache
     meta: dict = field(default_factory=dict)
 
     @property
@@ -133,8 +137,14 @@ def make_workload(name: str, context_lens: List[int], q_lens: List[int], *, num_
                   kv_dtype: int = BF16, sm_scale: Optional[float] = None, seed: int = 0,
                   block_mask: Optional[torch.Tensor] = None, mode: str = "decode",
                   max_pages_per_seq: Optional[int] = None, decoy_frac: float = 0.05,
-                  nan_fill: bool = True, meta: Optional[dict] = None) -> Workload:
-    """Lay out a seeded paged KV cache for the given per-sequence lengths."""
+                  nan_fill: bool = True, meta: Optional[dict] = None,
+                  q_dtype: int = BF16, quant_type: int = 0) -> Workload:
+    """Lay out a seeded paged KV cache for the given per-sequence lengths.
+
+    q_dtype FP8_E4M3 (with E4M3 K/V): the FP8 prefill quantisation types --
+    quant_type 0: Q, K and V each with one scale; quant_type 1: Q with one
+    scale per (token, q head), K and V with one scale each.  Otherwise E4M3
+    K/V carry one scale per (page, KV head)."""
     B = len(context_lens)
     assert len(q_lens) == B
     for c, q in zip(context_lens, q_lens):
@@ -158,6 +168,21 @@ def make_workload(name: str, context_lens: List[int], q_lens: List[int], *, num_
 
     total_q = sum(q_lens)
     q = _randn_bf16((total_q, num_q_heads, D), g)
+    q_scale = None
+    q_scale_mode = 0
+    if q_dtype == FP8_E4M3:
+        assert kv_dtype == FP8_E4M3, "E4M3 Q goes with E4M3 K/V"
+        qf = q.float()
+        if quant_type == 1:
+            amax = qf.abs().amax(dim=2)                     # [total_q, Hq]
+            q_scale_mode = 1
+        else:
+            amax = qf.abs().amax().reshape(1)
+        sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).float()
+        y = qf / (sc[:, :, None] if quant_type == 1 else sc)
+        q = y.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+        q_scale = sc.contiguous()
+    kv_scale_mode = 1 if q_dtype == FP8_E4M3 else 0
     if layout == NHD:
         shape = (num_pages, page_size, Hkv, D)
     else:
@@ -182,7 +207,21 @@ def make_workload(name: str, context_lens: List[int], q_lens: List[int], *, num_
             y = y.clamp(-E4M3_MAX, E4M3_MAX)
             return y.to(torch.float8_e4m3fn).view(torch.uint8), sc.float()
 
+        def quant_tensor(x: torch.Tensor):
+            # one scale for the whole cache: amax / 448, then round-to-nearest E4M3
+            amax = torch.zeros((), dtype=torch.float32)
+            for p0 in range(0, x.shape[0], 1024):
+                amax = torch.maximum(amax, x[p0:p0 + 1024].float().abs().amax())
+            sc = (amax / E4M3_MAX if float(amax) > 0 else torch.ones(())).reshape(1).float()
+            q8 = torch.empty(x.shape, dtype=torch.uint8)
+            for p0 in range(0, x.shape[0], 1024):
+                y = (x[p0:p0 + 1024].float() / sc).clamp(-E4M3_MAX, E4M3_MAX)
+                q8[p0:p0 + 1024] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+            return q8, sc.contiguous()
+
         def quant(x: torch.Tensor):
+            if kv_scale_mode == 1:
+                return quant_tensor(x)
             # pages are independent: quantise blocks of pages on host threads
             import concurrent.futures as cf
             import os
@@ -231,7 +270,8 @@ def make_workload(name: str, context_lens: List[int], q_lens: List[int], *, num_
         v_scale=v_scale, block_table=block_table,
         context_lens=torch.tensor(context_lens, dtype=torch.int32),
         q_lens=torch.tensor(q_lens, dtype=torch.int32), block_mask=block_mask, mode=mode,
-        meta=dict(meta or {}))
+        q_dtype=q_dtype, q_scale=q_scale, q_scale_mode=q_scale_mode,
+        kv_scale_mode=kv_scale_mode, meta=dict(meta or {}))
 
 
 def _log_uniform_ints(n: int, lo: int, hi: int, g: torch.Generator) -> List[int]:
@@ -307,6 +347,27 @@ def prefill_bf16(sparse: bool = False, seed: int = 1004, shrink: int = 1,
                          num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64,
                          layout=NHD, kv_dtype=BF16, seed=seed, block_mask=mask, mode="prefill",
                          meta={"sparse": sparse, "shrink": shrink})
+
+
+def prefill_fp8(quant_type: int = 1, sparse: bool = False, layout: int = NHD, seed: int = 1006,
+                shrink: int = 1, keep_prob: float = 0.26) -> Workload:
+    """The prefill workload's shape (B = 4 x 8192 causal, Hq=64, Hkv=8, D=128,
+    64-token pages) with E4M3 Q, K and V: quant_type 0 (one scale each) or 1
+    (Q per (token, q head), K and V one scale each); dense or block-sparse."""
+    B = 4 if shrink == 1 else 2
+    L = 8192 // shrink
+    mask = None
+    if sparse:
+        g = torch.Generator().manual_seed(seed * 7919 + 1)
+        t = (L + 127) // 128
+        mask = causal_block_mask(B, t, t, keep_prob, g)
+    return make_workload("prefill_fp8" + ("_sparse" if sparse else "_dense") + f"_q{quant_type}" +
+                         ("_hnd" if layout == HND else "") + (f"_s{shrink}" if shrink > 1 else ""),
+                         [L] * B, [L] * B, num_q_heads=64, num_kv_heads=8, head_dim=128,
+                         page_size=64, layout=layout, kv_dtype=FP8_E4M3, seed=seed,
+                         block_mask=mask, mode="prefill", q_dtype=FP8_E4M3,
+                         quant_type=quant_type,
+                         meta={"sparse": sparse, "shrink": shrink, "quant_type": quant_type})
 
 
 def hybrid_bf16(seed: int = 1005, shrink: int = 1) -> Workload:

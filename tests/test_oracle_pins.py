@@ -43,9 +43,22 @@ def dense_kv(w, b, hk, which):
     else:
         x = vals[pages][:, hk, :, :]
     if w.kv_dtype == W.FP8_E4M3:
-        sc = (w.k_scale if which == "k" else w.v_scale)[pages, hk].double()
-        x = x * sc[:, None, None]
+        scales = w.k_scale if which == "k" else w.v_scale
+        if w.kv_scale_mode == 1:                 # one scale for the cache
+            x = x * scales.reshape(-1)[0].double()
+        else:                                    # one per (page, KV head)
+            x = x * scales[pages, hk].double()[:, None, None]
     return x.reshape(-1, w.head_dim)[:ctx]
+
+
+def dense_q(w):
+    """float64 [total_q, Hq, D]: bf16 Q, or E4M3 bytes times their scale."""
+    if w.q_dtype == W.BF16:
+        return w.q.double()
+    q = w.q.view(torch.float8_e4m3fn).double()
+    if w.q_scale_mode == 1:                      # one per (token, q head)
+        return q * w.q_scale.double()[:, :, None]
+    return q * w.q_scale.reshape(-1)[0].double()
 
 
 def visibility(w, b):
@@ -70,9 +83,10 @@ def library_reference(w):
     G = w.gqa
     outs, lses = [], []
     cu = 0
+    qd = dense_q(w)
     for b in range(w.num_seqs):
         ql = int(w.q_lens[b])
-        q = w.q[cu:cu + ql].double()                       # [ql, Hq, D]
+        q = qd[cu:cu + ql]                                 # [ql, Hq, D]
         vis = visibility(w, b)
         o_b = torch.zeros(ql, w.num_q_heads, w.head_dim, dtype=torch.float64)
         l_b = torch.zeros(ql, w.num_q_heads, dtype=torch.float64)
@@ -104,6 +118,8 @@ def small_workloads():
         W.hybrid_bf16(shrink=32),
         W.make_workload("hnd_gqa2", [5, 64, 130], [5, 2, 3], num_q_heads=4, num_kv_heads=2,
                         head_dim=64, page_size=16, layout=W.HND, seed=7),
+        W.prefill_fp8(quant_type=0, shrink=64),
+        W.prefill_fp8(quant_type=1, sparse=True, layout=W.HND, shrink=64),
     ]
 
 
@@ -476,3 +492,50 @@ def test_keys_before_the_window_are_never_read(oracle_mod):
     o2, l2 = oracle_mod.attention(w)
     assert np.isfinite(o2).all()
     assert np.array_equal(o2, out) and np.array_equal(l2, lse)
+
+
+# ------------------------------------------------- FP8 prefill quantisation
+# "基于Triton-TLE优化Tencent HPC-Ops Attention", 二 (FP8 prefill over two
+# quantisation types) and 三 (Q per-token per-head, K/V per-tensor).  Our
+# reading of the other type: Q, K and V each with one scale.
+
+def test_fp8_q_scale_is_a_per_row_logit_scale(oracle_mod):
+    """Doubling the scale of one (token, q head) of an E4M3 Q doubles that
+    row's logits, which is exactly doubling sm_scale for that row; every
+    other row is bit-identical."""
+    w = W.prefill_fp8(quant_type=1, shrink=64)
+    row_tok, row_h = 37, 5
+    rows = np.array([row_tok * w.num_q_heads + row_h, 3 * w.num_q_heads + 1], np.int64)
+    base_o, base_l = oracle_mod.attention(w, rows=rows)
+    w2 = W.prefill_fp8(quant_type=1, shrink=64)
+    w2.q_scale = w2.q_scale.clone()
+    w2.q_scale[row_tok, row_h] *= 2.0
+    o2, l2 = oracle_mod.attention(w2, rows=rows)
+    w3 = W.prefill_fp8(quant_type=1, shrink=64)
+    w3.sm_scale = 2.0 * w3.sm_scale
+    o3, l3 = oracle_mod.attention(w3, rows=rows[:1])
+    assert np.array_equal(o2[0], o3[0]) and l2[0] == l3[0]
+    assert np.array_equal(o2[1], base_o[1]) and l2[1] == base_l[1]
+    assert not np.array_equal(o2[0], base_o[0])
+
+
+def test_fp8_per_tensor_v_scale_scales_the_output(oracle_mod):
+    """One V scale for the cache: doubling it doubles every output exactly
+    and leaves every LSE unchanged."""
+    w = W.prefill_fp8(quant_type=0, shrink=64)
+    o1, l1 = oracle_mod.attention(w)
+    w.v_scale = w.v_scale * 2.0
+    o2, l2 = oracle_mod.attention(w)
+    assert np.array_equal(o2, 2.0 * o1) and np.array_equal(l1, l2)
+
+
+def test_fp8_quantised_inputs_are_e4m3_codes_times_scales():
+    """The generator's Q bytes decode (torch float8_e4m3fn) to values whose
+    largest magnitude per scale group is about 448 * scale."""
+    w = W.prefill_fp8(quant_type=1, shrink=64)
+    q = w.q.view(torch.float8_e4m3fn).float()
+    amax = q.abs().amax(dim=2)
+    assert torch.all((amax <= 448.0) & (amax >= 240.0))
+    assert w.q_scale.shape == (w.total_q, w.num_q_heads)
+    w0 = W.prefill_fp8(quant_type=0, shrink=64)
+    assert w0.q_scale.numel() == 1 and w0.k_scale.numel() == 1 and w0.v_scale.numel() == 1
