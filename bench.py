@@ -10,13 +10,15 @@ query-key pair) / step time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                   [--workload decode_bf16|decode_fp8|prefill_dense|prefill_sparse|hybrid|
-                              tiny_mixed]
+                              tiny_mixed|decode_bf16_static|prefill_fp8_dense|
+                              prefill_fp8_sparse|prefill_fp8_dense_q0_hnd]
                   [--configs all|none]
 
 With no --workload (N = 1), the one JSON line also carries a "configs" object:
 every other workload of the metric (tiny mixed batch, bf16 decode with q_len
 3 and 4, E4M3 decode with q_len 3 and 4, dense and block-sparse prefill, the
-hybrid batch), each timed on the same contract (W warm-up steps, K timed
+hybrid batch, the static split-K decode, and the E4M3 prefill: dense and
+block-sparse with Q scales per (token, head), dense HND with one Q scale), each timed on the same contract (W warm-up steps, K timed
 steps, CUDA events on the launching stream) with its own roofline, clocks, CPU
 baseline and a parity check of sampled rows against the oracle leg's output.
 
@@ -43,7 +45,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode attn achieved HBM GB/s; prefill attn TFLOP/s; both as % of GB300 roofline"
 WORKLOADS = ["decode_bf16", "decode_fp8", "prefill_dense", "prefill_sparse", "hybrid",
-             "tiny_mixed", "decode_bf16_static"]
+             "tiny_mixed", "decode_bf16_static", "prefill_fp8_dense", "prefill_fp8_sparse",
+             "prefill_fp8_dense_q0_hnd"]
 # the "configs" object of the default line: (key, workload, mtp)
 CONFIG_SET = [
     ("tiny_mixed", "tiny_mixed", 0),
@@ -55,6 +58,9 @@ CONFIG_SET = [
     ("prefill_sparse", "prefill_sparse", 0),
     ("hybrid", "hybrid", 0),
     ("decode_bf16_static", "decode_bf16_static", 1),
+    ("prefill_fp8_dense", "prefill_fp8_dense", 0),
+    ("prefill_fp8_sparse", "prefill_fp8_sparse", 0),
+    ("prefill_fp8_dense_q0_hnd", "prefill_fp8_dense_q0_hnd", 0),
 ]
 PARALLELISM = "independent batch per GPU x{world}"
 
@@ -89,6 +95,11 @@ def make_workload(name: str, rank: int, shrink: int = 1, mtp: int = 0):
         return W.prefill_bf16(sparse=True, seed=rank_seed(1004, rank), shrink=shrink)
     if name == "hybrid":
         return W.hybrid_bf16(seed=rank_seed(1005, rank), shrink=shrink)
+    if name.startswith("prefill_fp8_"):
+        # E4M3 Q/K/V; quant type 1 (Q per token and head) unless "_q0"
+        return W.prefill_fp8(quant_type=0 if "_q0" in name else 1, sparse="_sparse" in name,
+                             layout=W.HND if name.endswith("_hnd") else W.NHD,
+                             seed=rank_seed(1006, rank), shrink=shrink)
     if name == "tiny_mixed":
         return W.tiny_mixed(seed=rank_seed(1001, rank))
     raise SystemExit(f"unknown workload {name}")
@@ -99,6 +110,7 @@ def workload_config(w, name, world):
            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
            "layout": "NHD" if w.layout == 0 else "HND",
            "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
+           "q_dtype": "bf16" if w.q_dtype == 0 else "e4m3",
            "total_q_tokens": w.total_q, "total_kv_tokens": int(w.context_lens.sum()),
            "l2": "inputs larger than L2" if w.meta.get("shrink", 1) == 1 and
            name != "tiny_mixed" else "inputs smaller than L2 (launch-bound case)",
@@ -108,6 +120,9 @@ def workload_config(w, name, world):
         cfg["q_len"] = 1 + w.meta["mtp"]
     if w.window:
         cfg["window"] = w.window
+    if w.q_dtype != 0:
+        cfg["quant_type"] = w.q_scale_mode
+        cfg["sparse"] = w.block_mask is not None
     return cfg
 
 
@@ -289,7 +304,7 @@ def launches_per_step(w, mode, static=False):
     if mode == B.PA_MODE_DECODE:
         return 2 if w.kv_dtype == 0 else 3
     G = w.num_q_heads // w.num_kv_heads
-    return 5 + (2 if w.block_mask is None and G <= 16 else 0)
+    return 5 + (2 if w.block_mask is None and G <= 16 and w.q_dtype == 0 else 0)
 
 
 class Case:
@@ -339,6 +354,10 @@ class Case:
             B.pa_decode_splitk(p, w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens,
                                w.q_lens, w.k_scale, w.v_scale, bufs.assign_ws, bufs.partial_ws,
                                bufs.out, bufs.lse)
+        elif p.q_dtype == B.PA_FP8_E4M3:
+            B.pa_prefill_fp8(p, w.q, w.q_scale, w.k_cache, w.v_cache, w.block_table,
+                             w.context_lens, w.q_lens, w.k_scale, w.v_scale, w.block_mask,
+                             bufs.assign_ws, bufs.partial_ws, bufs.out, bufs.lse)
         else:
             B.pa_prefill(p, w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.q_lens,
                          w.k_scale, w.v_scale, w.block_mask, bufs.assign_ws, bufs.partial_ws,
@@ -406,10 +425,15 @@ class Case:
             roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
         else:
-            pk = peaks["bf16_tflops"]
+            # E4M3 contractions: the measured bf16 peak x the nominal 2x of fp8
+            ratio = 2.0 if self.w_cpu.q_dtype == 1 else 1.0
+            pk = peaks["bf16_tflops"] * ratio
             roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk,
                     "unit": "TFLOP/s", "frac": round(achieved / pk, 4),
-                    "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+                    "frac_of_sustained": round(
+                        achieved / (peaks["bf16_tflops_sustained"] * ratio), 4)}
+            if ratio != 1.0:
+                roof["peak_dtype"] = "e4m3 (measured bf16 x 2, the nominal fp8/bf16 ratio)"
         roof["peak_source"] = peaks["source"]
         roof["kernel"] = ("pa_decode_static" if is_static(self.name) else
                           "pa_decode_splitk" if self.mode == self.B.PA_MODE_DECODE else
@@ -464,7 +488,9 @@ def e2e_measure(case, args, dist, dev):
     hbt = w_cpu.block_table.pin_memory()
     hctx = w_cpu.context_lens.pin_memory()
     hql = w_cpu.q_lens.pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hctx, hql))
+    # an E4M3 Q comes with its scales (one, or one per token and q head)
+    hqs = w_cpu.q_scale.pin_memory() if w_cpu.q_scale is not None else None
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hctx, hql, hqs) if t is not None)
     sets = []
     for k in range(2):
         wk = copy.copy(w)
@@ -473,6 +499,8 @@ def e2e_measure(case, args, dist, dev):
             wk.block_table = torch.empty_like(w.block_table)
             wk.context_lens = torch.empty_like(w.context_lens)
             wk.q_lens = torch.empty_like(w.q_lens)
+            if hqs is not None:
+                wk.q_scale = torch.empty_like(w.q_scale)
         bk = case.bufs if k == 0 else (B.StaticBuffers(w, 0) if is_static(case.name)
                                        else B.make_buffers(w, case.mode))
         hout = torch.empty(bk.out.shape, dtype=bk.out.dtype).pin_memory()
@@ -495,6 +523,8 @@ def e2e_measure(case, args, dist, dev):
             wk.block_table.copy_(hbt, non_blocking=True)
             wk.context_lens.copy_(hctx, non_blocking=True)
             wk.q_lens.copy_(hql, non_blocking=True)
+            if hqs is not None:
+                wk.q_scale.copy_(hqs, non_blocking=True)
             ev_in[k].record(up)
         stream.wait_event(ev_in[k])
         stream.wait_event(ev_out[k])           # step i-2's outputs have been read back
@@ -539,6 +569,8 @@ def e2e_measure(case, args, dist, dev):
         wk.block_table.copy_(hbt, non_blocking=True)
         wk.context_lens.copy_(hctx, non_blocking=True)
         wk.q_lens.copy_(hql, non_blocking=True)
+        if hqs is not None:
+            wk.q_scale.copy_(hqs, non_blocking=True)
         case.runner(wk, bk)
         hout.copy_(bk.out, non_blocking=True)
         hlse.copy_(bk.lse, non_blocking=True)

@@ -79,9 +79,16 @@ typedef enum pa_status {
 
 /* KV cache layouts ("基于Triton-TLE…", 三.2). */
 enum { PA_NHD = 0, PA_HND = 1 };
-/* KV cache element types.  FP8 is OCP E4M3FN; its fp32 scales are per
- * (page, KV head) for K and V separately. */
+/* Element types of the KV cache (and of Q, see q_dtype).  FP8 is OCP E4M3FN.
+ * Decode: E4M3 K/V with fp32 scales per (page, KV head), K and V separately,
+ * and a bf16 Q.  Prefill (pa_prefill_fp8): E4M3 Q, K and V with one fp32
+ * scale for K, one for V, and Q scales per q_scale_mode. */
 enum { PA_BF16 = 0, PA_FP8_E4M3 = 1 };
+/* E4M3 Q scales ("基于Triton-TLE…", 三: the two quantisation types of the FP8
+ * prefill): one fp32 for the whole Q (quant type 0), or one per (token, q
+ * head), laid out [total_q_tokens, Hq] (quant type 1).  K and V are per
+ * tensor in both. */
+enum { PA_SCALE_PER_TENSOR = 0, PA_SCALE_PER_ROW = 1 };
 /* Assign modes.
  *   PA_MODE_DECODE:  one unit per (sequence, KV head) holding all q_lens[b]
  *                    queries (G*max_q_len rows: at most 32 for head_dim 128,
@@ -130,6 +137,10 @@ typedef struct pa_problem {
                                   branch): 0 = none, else the query at position p
                                   sees only the keys p - window < j <= p.  Both
                                   modes, bf16 and E4M3 K/V.  Negative: invalid. */
+    int32_t q_dtype;           /* PA_BF16 (0), or PA_FP8_E4M3: the E4M3 prefill of
+                                  pa_prefill_fp8, which needs kv_dtype PA_FP8_E4M3
+                                  and head_dim 128; decode takes bf16 Q only     */
+    int32_t q_scale_mode;      /* E4M3 Q: PA_SCALE_PER_TENSOR or PA_SCALE_PER_ROW    */
 } pa_problem;
 
 /* Human-readable name of a pa_status or PA_DEV_* code set. */
@@ -340,6 +351,33 @@ PA_API pa_status pa_prefill(const pa_problem* problem, const void* q, const void
                      const float* v_scale, const uint8_t* block_mask, const void* assign_ws,
                      size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
                      void* out, float* lse, void* stream);
+
+/*
+ * FP8 prefill ("基于Triton-TLE…", 二: FP8 prefill over NHD/HND, two
+ * quantisation types, dense or block-sparse; 二.2: the warp-specialised
+ * pipeline also carries the quantisation scales).  problem->q_dtype and
+ * kv_dtype must both be PA_FP8_E4M3 and head_dim 128 (else
+ * PA_ERR_UNSUPPORTED); pa_assign, pa_assign_workspace_size and
+ * pa_partial_workspace_size take the same problem in PA_MODE_PREFILL.  Every
+ * sequence runs on the tensor-core kernel (no decode part): QK^T and PV are
+ * E4M3 tcgen05 MMAs with fp32 accumulation; the probabilities enter PV as
+ * two E4M3 terms (P and the rounding residual), about the precision of a
+ * bf16 P.  The scores are sm_scale * q_scale * k_scale * (q8 . k8) and
+ * out = v_scale * softmax(scores) V8 (bf16), lse as in pa_prefill.
+ *   q:        uint8 E4M3 [total_q_tokens, Hq, 128].
+ *   q_scale:  fp32, [1] (PA_SCALE_PER_TENSOR) or [total_q_tokens, Hq]
+ *             (PA_SCALE_PER_ROW); positive and finite.
+ *   k_scale, v_scale: fp32 [1] each, positive and finite.
+ *   Other arguments as pa_prefill (caches are uint8 E4M3).  A partial
+ *   workspace of the pa_partial_workspace_size this problem reports.
+ */
+PA_API pa_status pa_prefill_fp8(const pa_problem* problem, const void* q, const float* q_scale,
+                                const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* context_lens,
+                                const int32_t* q_lens, const float* k_scale, const float* v_scale,
+                                const uint8_t* block_mask, const void* assign_ws,
+                                size_t assign_ws_bytes, void* partial_ws,
+                                size_t partial_ws_bytes, void* out, float* lse, void* stream);
 
 /*
  * Test hook: copy the task map out of assign_ws (synchronises `stream`).

@@ -23,9 +23,10 @@ import torch
 from . import build as _build
 
 PA_OK = 0
-PA_ERR_WORKSPACE = 3
+PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE = 1, 2, 3
 PA_NHD, PA_HND = 0, 1
 PA_BF16, PA_FP8_E4M3 = 0, 1
+PA_SCALE_PER_TENSOR, PA_SCALE_PER_ROW = 0, 1
 PA_MODE_DECODE, PA_MODE_PREFILL = 0, 1
 PA_MAP_DECODE_PART = 2   # pa_read_task_map: decode part of a prefill-mode workspace
 PA_DEV_OK, PA_DEV_BAD_LENGTHS, PA_DEV_BAD_PAGE, PA_DEV_WAIT_TIMEOUT = 0, 1, 2, 4
@@ -35,7 +36,7 @@ EXPORTED = (
     "pa_partial_workspace_size", "pa_assign", "pa_decode_splitk", "pa_combine", "pa_prefill",
     "pa_read_task_map", "pa_last_device_error", "pa_decode_noalloc",
     "pa_test_inject_wait_timeout", "pa_static_workspace_size", "pa_static_num_splits",
-    "pa_decode_static",
+    "pa_decode_static", "pa_prefill_fp8",
 )
 
 PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # size of the library's fixed scratch
@@ -69,6 +70,8 @@ class PaProblem(ctypes.Structure):
         ("balance_rows", ctypes.c_int32),
         ("sm_scale", ctypes.c_float),
         ("window", ctypes.c_int32),
+        ("q_dtype", ctypes.c_int32),
+        ("q_scale_mode", ctypes.c_int32),
     ]
 
 
@@ -114,6 +117,8 @@ def load(build_if_missing: bool = True):
             "pa_static_num_splits": (i32, [PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
             "pa_decode_static": (i32, [PP, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                                        vp, vp, vp]),
+            "pa_prefill_fp8": (i32, [PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz,
+                                     vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -162,7 +167,8 @@ def problem_from(w, num_ctas: int = 0, balance_rows: int = 0) -> PaProblem:
         mask_q_tiles=(bm.shape[1] if bm is not None else 0),
         mask_kv_tiles=(bm.shape[2] if bm is not None else 0),
         num_ctas=num_ctas, balance_rows=balance_rows, sm_scale=float(w.sm_scale),
-        window=int(getattr(w, "window", 0)))
+        window=int(getattr(w, "window", 0)), q_dtype=int(getattr(w, "q_dtype", PA_BF16)),
+        q_scale_mode=int(getattr(w, "q_scale_mode", PA_SCALE_PER_TENSOR)))
 
 
 # ------------------------------------------------------------ entry points
@@ -245,6 +251,15 @@ def pa_prefill(problem, q, k_cache, v_cache, block_table, context_lens, q_lens, 
         _p(context_lens), _p(q_lens), _p(k_scale), _p(v_scale), _p(block_mask), _p(assign_ws),
         _nbytes(assign_ws), _p(partial_ws), _nbytes(partial_ws), _p(out), _p(lse),
         _stream(stream)), "pa_prefill")
+
+
+def pa_prefill_fp8(problem, q, q_scale, k_cache, v_cache, block_table, context_lens, q_lens,
+                   k_scale, v_scale, block_mask, assign_ws, partial_ws, out, lse, stream=None):
+    _check(load().pa_prefill_fp8(
+        ctypes.byref(problem), _p(q), _p(q_scale), _p(k_cache), _p(v_cache), _p(block_table),
+        _p(context_lens), _p(q_lens), _p(k_scale), _p(v_scale), _p(block_mask), _p(assign_ws),
+        _nbytes(assign_ws), _p(partial_ws), _nbytes(partial_ws), _p(out), _p(lse),
+        _stream(stream)), "pa_prefill_fp8")
 
 
 def pa_read_task_map(problem, mode, assign_ws, stream=None) -> dict:
@@ -356,8 +371,13 @@ def run_prefill(w, bufs: Optional[Buffers] = None, stream=None) -> Buffers:
         bufs = make_buffers(w, PA_MODE_PREFILL)
     p = bufs.problem
     pa_assign(p, PA_MODE_PREFILL, w.context_lens, w.q_lens, w.block_mask, bufs.assign_ws, stream)
-    pa_prefill(p, w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.q_lens, w.k_scale,
-               w.v_scale, w.block_mask, bufs.assign_ws, bufs.partial_ws, bufs.out, bufs.lse,
-               stream)
+    if p.q_dtype == PA_FP8_E4M3:
+        pa_prefill_fp8(p, w.q, w.q_scale, w.k_cache, w.v_cache, w.block_table, w.context_lens,
+                       w.q_lens, w.k_scale, w.v_scale, w.block_mask, bufs.assign_ws,
+                       bufs.partial_ws, bufs.out, bufs.lse, stream)
+    else:
+        pa_prefill(p, w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.q_lens,
+                   w.k_scale, w.v_scale, w.block_mask, bufs.assign_ws, bufs.partial_ws, bufs.out,
+                   bufs.lse, stream)
     pa_combine(p, PA_MODE_PREFILL, bufs.assign_ws, bufs.partial_ws, bufs.out, bufs.lse, stream)
     return bufs

@@ -35,9 +35,9 @@ const void* prefill_kernel_ptr(int D, bool fp8);
 cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, const void* q,
                                     const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const int32_t* block_table,
-                                    const int32_t* ctx, const int32_t* ql, const float* ks,
-                                    const float* vs, void* ws, void* partial, void* out,
-                                    float* lse, cudaStream_t stream);
+                                    const int32_t* ctx, const int32_t* ql, const float* qs,
+                                    const float* ks, const float* vs, void* ws, void* partial,
+                                    void* out, float* lse, cudaStream_t stream);
 
 namespace {
 
@@ -100,6 +100,9 @@ pa_status check_problem(const pa_problem* pp, int mode) {
 
     if (p.layout != PA_NHD && p.layout != PA_HND) return PA_ERR_INVALID_ARG;
     if (p.kv_dtype != PA_BF16 && p.kv_dtype != PA_FP8_E4M3) return PA_ERR_INVALID_ARG;
+    if (p.q_dtype != PA_BF16 && p.q_dtype != PA_FP8_E4M3) return PA_ERR_INVALID_ARG;
+    if (p.q_scale_mode != PA_SCALE_PER_TENSOR && p.q_scale_mode != PA_SCALE_PER_ROW)
+        return PA_ERR_INVALID_ARG;
     if ((p.mask_q_tiles > 0) != (p.mask_kv_tiles > 0)) return PA_ERR_INVALID_ARG;
     if (p.head_dim != 64 && p.head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (p.page_size != 16 && p.page_size != 32 && p.page_size != 64 && p.page_size != 128 &&
@@ -112,9 +115,12 @@ pa_status check_problem(const pa_problem* pp, int mode) {
         const int RT = decode_row_tiles(p);
         if (RT < 0 || (p.head_dim == 128 && RT > 2)) return PA_ERR_UNSUPPORTED;
         if (p.kv_dtype == PA_FP8_E4M3 && p.head_dim != 128) return PA_ERR_UNSUPPORTED;
+        if (p.q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     } else {
         if (G > 128 || 128 % G != 0) return PA_ERR_UNSUPPORTED;
-        if (p.kv_dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+        // the E4M3 prefill takes E4M3 Q, K and V together, head_dim 128
+        if (p.kv_dtype != p.q_dtype) return PA_ERR_UNSUPPORTED;
+        if (p.kv_dtype == PA_FP8_E4M3 && p.head_dim != 128) return PA_ERR_UNSUPPORTED;
     }
     return PA_OK;
 }
@@ -210,18 +216,21 @@ bool encode_kv_map_one_box(const pa_problem& p, const void* base, CUtensorMap* m
     return r == CUDA_SUCCESS;
 }
 
-// Q viewed as (d, head, token): box = 64 elements x G heads x box_tokens tokens
+// Q viewed as (d, head, token): box = 128 bytes of d (64 bf16 or 128 E4M3
+// elements) x G heads x box_tokens tokens
 bool encode_q_map(const pa_problem& p, const void* base, int box_tokens, CUtensorMap* map) {
     auto fn = encode_fn();
     if (!fn) return false;
     const int G = p.num_q_heads / p.num_kv_heads;
+    const cuuint64_t e = p.q_dtype == PA_FP8_E4M3 ? 1 : 2;
     const cuuint64_t D = p.head_dim, Hq = p.num_q_heads;
     const cuuint64_t T = p.total_q_tokens > 0 ? p.total_q_tokens : 1;
     cuuint64_t dims[3] = {D, Hq, T};
-    cuuint64_t strides[2] = {D * 2, Hq * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)box_tokens};
+    cuuint64_t strides[2] = {D * e, Hq * D * e};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / e), (cuuint32_t)G, (cuuint32_t)box_tokens};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+    CUresult r = fn(map, e == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    3, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -263,7 +272,8 @@ pa_status make_prefill_layout(const pa_problem* p, PrefillLayout& M) {
     M.total_bytes = M.L.total_bytes;
     M.partial_bytes = M.L.partial_bytes;
     const int G = p->num_q_heads / p->num_kv_heads;
-    if (p->mask_q_tiles > 0 || G > kMixedDecodeRows) return PA_OK;
+    // (the decode kernel takes a bf16 Q: an E4M3 batch stays on one map)
+    if (p->mask_q_tiles > 0 || G > kMixedDecodeRows || p->q_dtype != PA_BF16) return PA_OK;
     const int small_q = kMixedDecodeRows / G;
     M.pd = *p;
     if (M.pd.max_q_len > small_q) M.pd.max_q_len = small_q;
@@ -457,6 +467,63 @@ pa_status noalloc_scratch(char** out) {
     return PA_OK;
 }
 
+}  // namespace
+
+namespace {
+pa_status prefill_body(const pa_problem* problem, const void* q, const float* q_scale,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* context_lens, const int32_t* q_lens, const float* k_scale,
+                       const float* v_scale, const uint8_t* block_mask, const void* assign_ws,
+                       size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
+                       void* out, float* lse, void* stream) {
+    PrefillLayout M;
+    pa_status st = make_prefill_layout(problem, M);
+    if (st != PA_OK) return st;
+    // the kernels read the active-tile lists pa_assign built from the mask;
+    // the mask itself must be given exactly when the problem declares one
+    if ((problem->mask_q_tiles > 0) != (block_mask != nullptr)) return PA_ERR_INVALID_ARG;
+    const WsLayout& L = M.L;
+    const pa_problem& p = *problem;
+    if (p.total_q_tokens == 0) return PA_OK;   // no query row: nothing to compute
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !assign_ws ||
+        !out || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(out, 16) || !aligned(block_table, 4) || !aligned(assign_ws, 256))
+        return PA_ERR_INVALID_ARG;
+    if (p.q_dtype == PA_FP8_E4M3 &&
+        (!q_scale || !k_scale || !v_scale || !aligned(q_scale, 4) || !aligned(k_scale, 4) ||
+         !aligned(v_scale, 4)))
+        return PA_ERR_INVALID_ARG;
+    if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
+    if (partial_ws_bytes < (size_t)M.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
+        return PA_ERR_WORKSPACE;
+    CUtensorMap tq, tk, tv;
+    if (!encode_q_map(p, q, kPrefillHalfRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
+        !encode_kv_map(p, k_cache, &tk) ||
+        !encode_kv_map(p, v_cache, &tv))
+        return PA_ERR_INVALID_ARG;
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (M.split) {
+        // the decode-shaped sequences first, on the decode kernel; its 4-D
+        // K/V maps are the prefill kernel's
+        CUtensorMap tqd, tkd, tvd;
+        if (!encode_q_map(M.pd, q, M.pd.max_q_len > 0 ? M.pd.max_q_len : 1, &tqd))
+            return PA_ERR_INVALID_ARG;
+        const bool one_box = encode_kv_map_one_box(M.pd, k_cache, &tkd) &&
+                             encode_kv_map_one_box(M.pd, v_cache, &tvd);
+        // (the wait-timeout test hook is left for the prefill kernel)
+        e = launch_decode_from_api(M.pd, M.Ld, tqd, one_box ? tkd : tk, one_box ? tvd : tv,
+                                   one_box, block_table, context_lens, q_lens, k_scale, v_scale,
+                                   const_cast<void*>(assign_ws),
+                                   static_cast<char*>(partial_ws) + M.part_off, out, lse, s,
+                                   false);
+    }
+    if (e == cudaSuccess)
+        e = launch_prefill_from_api(p, L, q, tq, tk, tv, block_table, context_lens, q_lens,
+                                    q_scale, k_scale, v_scale, const_cast<void*>(assign_ws),
+                                    partial_ws, out, lse, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 }  // namespace
 
 }  // namespace pa
@@ -704,49 +771,26 @@ pa_status pa_prefill(const pa_problem* problem, const void* q, const void* k_cac
                      const float* v_scale, const uint8_t* block_mask, const void* assign_ws,
                      size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
                      void* out, float* lse, void* stream) {
-    PrefillLayout M;
-    pa_status st = make_prefill_layout(problem, M);
-    if (st != PA_OK) return st;
-    // the kernels read the active-tile lists pa_assign built from the mask;
-    // the mask itself must be given exactly when the problem declares one
-    if ((problem->mask_q_tiles > 0) != (block_mask != nullptr)) return PA_ERR_INVALID_ARG;
-    const WsLayout& L = M.L;
-    const pa_problem& p = *problem;
-    if (p.total_q_tokens == 0) return PA_OK;   // no query row: nothing to compute
-    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !q_lens || !assign_ws ||
-        !out || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-        !aligned(out, 16) || !aligned(block_table, 4) || !aligned(assign_ws, 256))
-        return PA_ERR_INVALID_ARG;
-    if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
-    if (partial_ws_bytes < (size_t)M.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
-        return PA_ERR_WORKSPACE;
-    CUtensorMap tq, tk, tv;
-    if (!encode_q_map(p, q, kPrefillHalfRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
-        !encode_kv_map(p, k_cache, &tk) ||
-        !encode_kv_map(p, v_cache, &tv))
-        return PA_ERR_INVALID_ARG;
-    const cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaSuccess;
-    if (M.split) {
-        // the decode-shaped sequences first, on the decode kernel; its 4-D
-        // K/V maps are the prefill kernel's
-        CUtensorMap tqd, tkd, tvd;
-        if (!encode_q_map(M.pd, q, M.pd.max_q_len > 0 ? M.pd.max_q_len : 1, &tqd))
-            return PA_ERR_INVALID_ARG;
-        const bool one_box = encode_kv_map_one_box(M.pd, k_cache, &tkd) &&
-                             encode_kv_map_one_box(M.pd, v_cache, &tvd);
-        // (the wait-timeout test hook is left for the prefill kernel)
-        e = launch_decode_from_api(M.pd, M.Ld, tqd, one_box ? tkd : tk, one_box ? tvd : tv,
-                                   one_box, block_table, context_lens, q_lens, k_scale, v_scale,
-                                   const_cast<void*>(assign_ws),
-                                   static_cast<char*>(partial_ws) + M.part_off, out, lse, s,
-                                   false);
-    }
-    if (e == cudaSuccess)
-        e = launch_prefill_from_api(p, L, q, tq, tk, tv, block_table, context_lens, q_lens,
-                                    k_scale, v_scale, const_cast<void*>(assign_ws), partial_ws,
-                                    out, lse, s);
-    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    // an E4M3 Q comes with its scales: pa_prefill_fp8
+    if (problem && problem->q_dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    return prefill_body(problem, q, nullptr, k_cache, v_cache, block_table, context_lens, q_lens,
+                        k_scale, v_scale, block_mask, assign_ws, assign_ws_bytes, partial_ws,
+                        partial_ws_bytes, out, lse, stream);
+}
+
+pa_status pa_prefill_fp8(const pa_problem* problem, const void* q, const float* q_scale,
+                         const void* k_cache, const void* v_cache, const int32_t* block_table,
+                         const int32_t* context_lens, const int32_t* q_lens,
+                         const float* k_scale, const float* v_scale,
+                         const uint8_t* block_mask, const void* assign_ws,
+                         size_t assign_ws_bytes, void* partial_ws, size_t partial_ws_bytes,
+                         void* out, float* lse, void* stream) {
+    if (!problem) return PA_ERR_INVALID_ARG;
+    if (problem->q_dtype != PA_FP8_E4M3 || problem->kv_dtype != PA_FP8_E4M3)
+        return PA_ERR_UNSUPPORTED;
+    return prefill_body(problem, q, q_scale, k_cache, v_cache, block_table, context_lens, q_lens,
+                        k_scale, v_scale, block_mask, assign_ws, assign_ws_bytes, partial_ws,
+                        partial_ws_bytes, out, lse, stream);
 }
 
 pa_status pa_test_inject_wait_timeout(int32_t skip_entry, int64_t wait_limit_ns) {

@@ -66,18 +66,25 @@ struct PrefillParams {
     int32_t rows_per_box;    // min(page_size, 64)
     int32_t boxes_per_tile;  // 128 / rows_per_box
     int32_t test_skip_it;    // test hook: CTA 0 leaves this K/V ring entry unfilled (-1 none)
+    // E4M3 Q/K/V: Q scale (one, or one per (token, q head)), one K and one V scale
+    const float* q_scale;
+    const float* k_scale;
+    const float* v_scale;
+    int32_t q_scale_per_row;
     float sm_scale;
     uint64_t wait_limit_ns;
 };
 
-template <int D>
+template <int D, bool FP8 = false>
 struct PrefillCfg {
-    static constexpr int kHalves = D / 64;           // 128-byte column blocks of a row
+    static constexpr int kElem = FP8 ? 1 : 2;        // bytes per Q/K/V element
+    static constexpr int kHalves = D * kElem / 128;  // 128-byte column blocks of a row
     static constexpr int kRegion = 128 * 128;        // 128 rows x 128 bytes
     static constexpr int kQTileBytes = kHalves * kRegion;
     static constexpr int kQBytes = 2 * kQTileBytes;  // two 128-row halves
     static constexpr int kKVBytes = kHalves * kRegion;
-    static constexpr int kEntries = D == 128 ? 5 : 8;  // ring entries (each a K or a V tile)
+    // ring entries (each a K or a V tile)
+    static constexpr int kEntries = FP8 ? 10 : (D == 128 ? 5 : 8);
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;
     static constexpr int kOffBar = kOffKV + kEntries * kKVBytes;
@@ -101,12 +108,20 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
 }
 
 // WINDOW: the instantiation that takes a sliding window; the other one
-// carries no window arithmetic in its softmax.
-template <int D, bool WINDOW>
+// carries no window arithmetic in its softmax.  FP8: E4M3 Q, K and V
+// ("基于Triton-TLE…", 二: FP8 prefill) -- QK^T and PV on kind::f8f6f4 (K = 32
+// per instruction): S = Q K^T straight from the E4M3 tiles (both K-major);
+// the softmax scales S by q_scale * k_scale, and writes P into tensor memory
+// as two E4M3 terms, P ~ P_hi + P_lo (P_hi = e4m3(P), P_lo = e4m3(P - P_hi):
+// about 2^-8 relative, the precision of a bf16 P); PV runs one MMA per term
+// with V read MN-major from its E4M3 tile; v_scale is applied to O in the
+// epilogue.
+template <int D, bool WINDOW, bool FP8>
 __global__ void __launch_bounds__(384, 1)
 prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ CUtensorMap tmq,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-    using Cfg = PrefillCfg<D>;
+    using Cfg = PrefillCfg<D, FP8>;
+    static_assert(!FP8 || D == 128, "E4M3 prefill: head_dim 128");
     constexpr int E = Cfg::kEntries;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -228,7 +243,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 if (go && lane < H * Cfg::kHalves) {
                     const int h = lane / Cfg::kHalves, c = lane % Cfg::kHalves;
                     tma_load_3d(smem + Cfg::kOffQ + h * Cfg::kQTileBytes + c * Cfg::kRegion, &tmq,
-                                q_full, 64 * c, hk * G, rec.cuq + q0 + h * half_tokens);
+                                q_full, (128 / Cfg::kElem) * c, hk * G,
+                                rec.cuq + q0 + h * half_tokens);
                 }
             }
             __syncwarp();
@@ -291,7 +307,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                             const int slot0 = (kt * kPrefillTile + j * rpb) % ps;
                             tma_load_4d(smem + Cfg::kOffKV + e * Cfg::kKVBytes + c * Cfg::kRegion +
                                             j * rpb * 128,
-                                        kv ? &tmv : &tmk, &kv_full[e], 64 * c, slot0, hk, page);
+                                        kv ? &tmv : &tmk, &kv_full[e], (128 / Cfg::kElem) * c,
+                                        slot0, hk, page);
                         }
                     }
                     __syncwarp();
@@ -309,8 +326,10 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         // groups then run at the same time while the tensor pipe idles.
         // Both warps release each ring entry and the Q buffer (two commits
         // per barrier phase).
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+        constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(128, 128, false, false)
+                                          : idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3_f32(128, D, false, true)
+                                          : idesc_bf16_f32(128, D, false, true);
         // Descriptor bases: the start-address field is the low bits of a
         // descriptor, so a byte offset within the buffer is added as offset >> 4.
         const uint64_t dQ = smem_desc_sw128(smem_u32(smem + Cfg::kOffQ), 16, 1024);
@@ -324,20 +343,35 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             const uint64_t a0 = dQ + (uint64_t)((h * Cfg::kQTileBytes) >> 4);
             const uint64_t b0 = dK + (uint64_t)((e * Cfg::kKVBytes) >> 4);
             const uint32_t d = tmem + h * 256;
+            // each instruction takes 32 bytes of every row's K dimension
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < D * Cfg::kElem / 32; ++kk) {
                 const uint64_t koff = (uint64_t)((((kk >> 2) * Cfg::kRegion) + (kk & 3) * 32) >> 4);
-                tc_mma_ss(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
+                if constexpr (FP8)
+                    tc_mma_ss_f8(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
+                else
+                    tc_mma_ss(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
             }
             tc_commit(&s_full[h]);
         };
         auto issue_pv = [&](int h, int e, bool first) {   // O_h += P_h V from ring entry e
             const uint64_t b0 = dV + (uint64_t)((e * Cfg::kKVBytes) >> 4);
             const uint32_t d = tmem + h * 256 + 128, a = tmem + h * 256;
+            if constexpr (FP8) {
+                // 32 keys per instruction; P's columns [16kk, 16kk + 8) hold the
+                // P_hi bytes of keys [32kk, 32kk + 32), the next 8 their P_lo
 #pragma unroll
-            for (int kk = 0; kk < kPrefillTile / 16; ++kk)
-                tc_mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
-                          (!first || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kPrefillTile / 32; ++kk) {
+                    const uint64_t b = b0 + (uint64_t)((kk * 32 * 128) >> 4);
+                    tc_mma_ts_f8(d, a + kk * 16, b, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                    tc_mma_ts_f8(d, a + kk * 16 + 8, b, idesc_pv, 1u);
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < kPrefillTile / 16; ++kk)
+                    tc_mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
+                              (!first || kk > 0) ? 1u : 0u);
+            }
             tc_commit(&o_done[h]);
         };
 
@@ -454,6 +488,14 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             if (h == 1 && R <= kPrefillHalfRows) continue;   // half 1 idle for this unit
             const int r = h * kPrefillHalfRows + row;        // row inside the unit
             const bool row_ok = r < R;
+            // the row's logit scale (E4M3: times its Q scale and the K scale)
+            float sl2 = scale_log2;
+            if constexpr (FP8) {
+                const int64_t qi = P.q_scale_per_row
+                                       ? (int64_t)(rec.cuq + q0 + r / G) * Hq + hk * G + r % G
+                                       : 0;
+                sl2 = scale_log2 * (row_ok ? __ldg(P.q_scale + qi) : 1.f) * __ldg(P.k_scale);
+            }
             const int ctx_b = rec.ctx;
             const int p_row = ctx_b - rec.ql + q0 + r / G;   // last key this row sees
             const int key_last = p_row < ctx_b - 1 ? p_row : ctx_b - 1;
@@ -506,7 +548,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     }
                 }
                 const float mx =
-                    fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+                    fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
                 // lazy max: move m (and rescale O, l) only when it grows by > 2^8
                 float alpha = 1.f;
                 bool resc = false;
@@ -531,24 +573,45 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     reg_fence32(s);
                     const int lim = limc - c4 * 32, low = lowc - c4 * 32;
                     uint32_t pk[16];
+                    // E4M3: the pair (P_c, P_c+1), as f16, becomes P_hi bytes
+                    // (columns 0-7 of the chunk's 16) and P_lo = e4m3(P - P_hi)
+                    // bytes (columns 8-15), four keys to a 32-bit column
+                    auto put_e4m3 = [&](int c, uint32_t e2) {
+                        const uint16_t hb = f16x2_to_e4m3x2(e2);
+                        const uint16_t lb = f16x2_to_e4m3x2(hsub2_u32(e2, e4m3x2_to_f16x2(hb)));
+                        const int w = c >> 2;
+                        if ((c & 2) == 0) {
+                            pk[w] = hb;
+                            pk[8 + w] = lb;
+                        } else {
+                            pk[w] |= (uint32_t)hb << 16;
+                            pk[8 + w] |= (uint32_t)lb << 16;
+                        }
+                    };
                     if (lim >= 31 && (!WINDOW || low <= 0)) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
-                            const uint32_t e2 = ex2_h2(fmaf(s[c], scale_log2, -mu),
-                                                       fmaf(s[c + 1], scale_log2, -mu));
+                            const uint32_t e2 = ex2_h2(fmaf(s[c], sl2, -mu),
+                                                       fmaf(s[c + 1], sl2, -mu));
                             const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&e2));
                             sum4[(c >> 1) & 3] += pf.x + pf.y;
-                            pk[c >> 1] = pack_bf16x2(pf.x, pf.y);
+                            if constexpr (FP8)
+                                put_e4m3(c, e2);
+                            else
+                                pk[c >> 1] = pack_bf16x2(pf.x, pf.y);
                         }
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
                             const float e0 = (c <= lim && (!WINDOW || c >= low))
-                                                 ? ex2(fmaf(s[c], scale_log2, -mu)) : 0.f;
+                                                 ? ex2(fmaf(s[c], sl2, -mu)) : 0.f;
                             const float e1 = (c + 1 <= lim && (!WINDOW || c + 1 >= low))
-                                                 ? ex2(fmaf(s[c + 1], scale_log2, -mu)) : 0.f;
+                                                 ? ex2(fmaf(s[c + 1], sl2, -mu)) : 0.f;
                             sum4[(c >> 1) & 3] += e0 + e1;
-                            pk[c >> 1] = pack_bf16x2(e0, e1);
+                            if constexpr (FP8)
+                                put_e4m3(c, pack_f16x2_sat(e0, e1));
+                            else
+                                pk[c >> 1] = pack_bf16x2(e0, e1);
                         }
                     }
                     tmem_st16(tS + c4 * 16, pk);
@@ -582,7 +645,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 ++o_cnt;
             }
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float inv = l > 0.f ? 1.f / l : 0.f;
+            if constexpr (FP8) inv *= __ldg(P.v_scale);   // one V scale for the cache
             const float lse_nat = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
             const int token = rec.cuq + q0 + r / G, head = hk * G + r % G;
 #pragma unroll 1
@@ -647,7 +711,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
 }
 
 int prefill_smem_bytes(int D, bool fp8) {
-    if (fp8) return -1;
+    if (fp8) return D == 128 ? PrefillCfg<128, true>::kSmemBytes : -1;
     if (D == 128) return PrefillCfg<128>::kSmemBytes;
     if (D == 64) return PrefillCfg<64>::kSmemBytes;
     return -1;
@@ -656,21 +720,34 @@ int prefill_smem_bytes(int D, bool fp8) {
 int prefill_threads() { return 384; }
 
 const void* prefill_kernel_ptr(int D, bool fp8) {
-    if (fp8) return nullptr;
-    if (D == 128) return (const void*)prefill_kernel<128, false>;
-    if (D == 64) return (const void*)prefill_kernel<64, false>;
+    if (fp8) return D == 128 ? (const void*)prefill_kernel<128, false, true> : nullptr;
+    if (D == 128) return (const void*)prefill_kernel<128, false, false>;
+    if (D == 64) return (const void*)prefill_kernel<64, false, false>;
     return nullptr;
 }
+
+namespace {
+template <int D, bool WINDOW, bool FP8>
+cudaError_t launch_prefill_variant(const PrefillParams& P, const CUtensorMap& tq,
+                                   const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                                   cudaStream_t stream) {
+    using Cfg = PrefillCfg<D, FP8>;
+    const void* kern = (const void*)prefill_kernel<D, WINDOW, FP8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(prefill_kernel<D, WINDOW, FP8>, dim3(grid), dim3(Cfg::kThreads),
+                            Cfg::kSmemBytes, stream, P, tq, tk, tv);
+}
+}  // namespace
 
 cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, const void* q,
                                     const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const int32_t* block_table,
-                                    const int32_t* ctx, const int32_t* ql, const float* ks,
-                                    const float* vs, void* ws, void* partial, void* out,
-                                    float* lse, cudaStream_t stream) {
+                                    const int32_t* ctx, const int32_t* ql, const float* qs,
+                                    const float* ks, const float* vs, void* ws, void* partial,
+                                    void* out, float* lse, cudaStream_t stream) {
     (void)q;
-    (void)ks;
-    (void)vs;
     PrefillParams P;
     P.L = L;
     P.block_table = block_table;
@@ -686,28 +763,24 @@ cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, cons
     P.max_pages_per_seq = p.max_pages_per_seq;
     P.rows_per_box = p.page_size < 64 ? p.page_size : 64;
     P.boxes_per_tile = kPrefillTile / P.rows_per_box;
+    P.q_scale = qs;
+    P.k_scale = ks;
+    P.v_scale = vs;
+    P.q_scale_per_row = p.q_scale_mode == PA_SCALE_PER_ROW ? 1 : 0;
     P.sm_scale = p.sm_scale;
     take_test_hook(&P.test_skip_it, &P.wait_limit_ns);
     const bool win = p.window > 0;
-    const void* kern =
-        p.head_dim == 128 ? (win ? (const void*)prefill_kernel<128, true>
-                                 : (const void*)prefill_kernel<128, false>)
-        : p.head_dim == 64 ? (win ? (const void*)prefill_kernel<64, true>
-                                  : (const void*)prefill_kernel<64, false>)
-                           : nullptr;
-    const int smem = prefill_smem_bytes(p.head_dim, false);
-    if (!kern || smem <= 0) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid(L.N), block(PrefillCfg<128>::kThreads);
-    if (p.head_dim == 128)
-        e = win ? launch_dependent(prefill_kernel<128, true>, grid, block, smem, stream, P, tq, tk, tv)
-                : launch_dependent(prefill_kernel<128, false>, grid, block, smem, stream, P, tq, tk,
-                                   tv);
-    else
-        e = win ? launch_dependent(prefill_kernel<64, true>, grid, block, smem, stream, P, tq, tk, tv)
-                : launch_dependent(prefill_kernel<64, false>, grid, block, smem, stream, P, tq, tk,
-                                   tv);
+    const bool fp8 = p.q_dtype == PA_FP8_E4M3;
+    cudaError_t e = cudaErrorInvalidValue;
+    if (fp8 && p.head_dim == 128)
+        e = win ? launch_prefill_variant<128, true, true>(P, tq, tk, tv, L.N, stream)
+                : launch_prefill_variant<128, false, true>(P, tq, tk, tv, L.N, stream);
+    else if (!fp8 && p.head_dim == 128)
+        e = win ? launch_prefill_variant<128, true, false>(P, tq, tk, tv, L.N, stream)
+                : launch_prefill_variant<128, false, false>(P, tq, tk, tv, L.N, stream);
+    else if (!fp8 && p.head_dim == 64)
+        e = win ? launch_prefill_variant<64, true, false>(P, tq, tk, tv, L.N, stream)
+                : launch_prefill_variant<64, false, false>(P, tq, tk, tv, L.N, stream);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

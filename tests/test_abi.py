@@ -142,3 +142,35 @@ def test_static_workspace_sizes_host_only(lib):
     assert B.pa_static_num_splits(p, 3) == 3
     assert B.pa_static_num_splits(p, 0) >= 1
     assert B.pa_static_workspace_size(p, 65) == 0          # beyond 64 splits
+
+
+def test_fp8_prefill_host_checks(lib):
+    """E4M3 prefill problems: accepted in prefill mode only, with E4M3 K/V and
+    head_dim 128; every sequence on the tensor-core map (no decode part)."""
+    w = W.prefill_fp8(quant_type=1, shrink=32)
+    p = B.problem_from(w, num_ctas=152)
+    assert p.q_dtype == B.PA_FP8_E4M3 and p.q_scale_mode == B.PA_SCALE_PER_ROW
+    assert B.pa_assign_workspace_size(p, B.PA_MODE_PREFILL) > 0
+    assert B.pa_assign_workspace_size(p, B.PA_MODE_DECODE) == 0    # decode takes bf16 Q
+    wd = W.prefill_bf16(sparse=False, shrink=32)
+    pd = B.problem_from(wd, num_ctas=152)
+    extra = (wd.num_seqs * wd.num_kv_heads + 152) * 16 * (128 + 1) * 4
+    assert (B.pa_partial_workspace_size(p, B.PA_MODE_PREFILL)
+            == B.pa_partial_workspace_size(pd, B.PA_MODE_PREFILL) - extra)
+    for field, value in (("head_dim", 64), ("kv_dtype", B.PA_BF16), ("q_dtype", 2),
+                         ("q_scale_mode", 2)):
+        bad = B.PaProblem.from_buffer_copy(p)
+        setattr(bad, field, value)
+        assert B.pa_assign_workspace_size(bad, B.PA_MODE_PREFILL) == 0, field
+    fake = ctypes.c_void_p(1 << 20)           # aligned, never dereferenced
+    # pa_prefill takes no Q scales: an E4M3 Q is refused
+    st = lib.pa_prefill(ctypes.byref(p), *([fake] * 8), None, fake, 1 << 30, fake, 1 << 30,
+                        fake, fake, None)
+    assert st == B.PA_ERR_INVALID_ARG
+    # pa_prefill_fp8 needs E4M3 Q and K/V, and its scales
+    st = lib.pa_prefill_fp8(ctypes.byref(pd), *([fake] * 9), None, fake, 1 << 30, fake,
+                            1 << 30, fake, fake, None)
+    assert st == B.PA_ERR_UNSUPPORTED
+    st = lib.pa_prefill_fp8(ctypes.byref(p), fake, None, *([fake] * 7), None, fake, 1 << 30,
+                            fake, 1 << 30, fake, fake, None)
+    assert st == B.PA_ERR_INVALID_ARG
