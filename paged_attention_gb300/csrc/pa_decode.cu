@@ -41,6 +41,7 @@ template <int D, int RT, int NG, int STAGES, bool STATIC = false>
 struct DecodeCfg {
     static constexpr bool kStatic = STATIC;   // static split-K task source (no Assign map)
     static constexpr int kStages = STAGES;
+    static constexpr int kTilesPerStage = 1;                  // one 64-token KV tile a stage
     static constexpr int kProducerWarps = STAGES % 4 == 0 ? 4 : 2;
     static constexpr bool kFP8 = false;
     static constexpr int kGroupWarps = 4 * RT;

@@ -142,7 +142,10 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // Cfg supplies the shared-memory geometry: kStages, kProducerWarps, kFP8,
 // kHalves (128-byte column blocks per K/V row), kHalfBytes, kKBytes (V follows
 // K in a stage), kStageBytes, kElem, kQHalves, kQHalfBytes, kQSlotBytes,
-// kOffQ.  `wait` is the kernel's bounded mbarrier wait (it turns into a no-op
+// kOffQ, and kTilesPerStage: 1, or 2 for a stage that holds the task's KV
+// tiles t and t+1 as one 128-row K block followed by one 128-row V block
+// (tile t+1 is left unloaded past the task's end; the scales of a stage are
+// then 8 per K/V, tile-major).  `wait` is the kernel's bounded mbarrier wait (it turns into a no-op
 // once the CTA has aborted, so the loop structure is kept).  After an abort
 // the producers arm no barrier and issue no copy; `armed` (shared, kStages + 2
 // ints, -1 at start) records per ring stage and per Q slot the last phase
@@ -165,6 +168,9 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
         prefetch_tmap(tmk);
         prefetch_tmap(tmv);
     }
+    constexpr int TPS = Cfg::kTilesPerStage;
+    static_assert(TPS == 1 || (TPS == 2 && Cfg::kHalves == 1), "two tiles a stage: E4M3 only");
+    constexpr int kSubBytes = kDecodeTile * 128;   // one tile's K (or V) in a two-tile stage
     const int ps = P.page_size, rpb = P.rows_per_box, nbox = P.boxes_per_tile;
     const uint32_t box_bytes = (uint32_t)rpb * 128u * Cfg::kHalves;
     const uint32_t q_bytes = (uint32_t)Cfg::kQHalves * G * P.q_box_tokens * 128u;
@@ -205,20 +211,73 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
         float win_ks = 0.f, win_vs = 0.f;
         // sliding window: task positions count from the unit's first visible tile
         const int first = window_first_tile(L.window, ctx_b - rec.ql + un.z, kDecodeTile);
-        for (int t = tk.y; t < tk.z; ++t, ++it) {
+        for (int t = tk.y; t < tk.z; t += TPS, ++it) {
             if (Cfg::kProducerWarps > 1 && it % Cfg::kProducerWarps != pw) continue;
             const int s = it % Cfg::kStages;
             wait(&empty[s], (uint32_t)((it / Cfg::kStages) & 1) ^ 1u);
             const int kt = t + first;
-            int pg[4];
-            float ksc[4], vsc[4];
+            if constexpr (TPS == 2) {
+                // Two tiles a stage (E4M3, one 128-byte column block): every
+                // step is lane-parallel -- lane = (kv, tile m, box j) finds its
+                // own page, scale and bytes, so the warp spends a few dozen
+                // instructions a stage however many boxes the pages need.
+                const int kv = lane >> 3, m = (lane >> 2) & 1, j = lane & 3;
+                const int tok0 = (kt + m) * kDecodeTile + j * rpb;
+                const bool want = lane < 16 && j < nbox && t + m < tk.z && tok0 < ctx_b;
+                const int lp = want ? tok0 / ps : 0;
+                const int lp_lo = __reduce_min_sync(0xffffffffu, want ? lp : (1 << 30));
+                const int lp_hi = __reduce_max_sync(0xffffffffu, want ? lp : -(1 << 30));
+                if (lp_lo <= lp_hi && (lp_lo < win_lo || lp_hi - win_lo >= 32)) {
+                    win_val = (lp_lo == nxt_lo) ? nxt_val
+                                                : ((lp_lo + lane < npg) ? __ldg(bt_row + lp_lo + lane) : -1);
+                    win_lo = lp_lo;
+                    nxt_lo = lp_lo + 32;
+                    nxt_val = (nxt_lo + lane < npg) ? __ldg(bt_row + nxt_lo + lane) : -1;
+                    const bool okp = win_val >= 0 && win_val < P.num_pages;
+                    const int64_t si = (int64_t)(okp ? win_val : 0) * L.Hkv + hk;
+                    win_ks = okp ? __ldg(P.k_scale + si) : 0.f;
+                    win_vs = okp ? __ldg(P.v_scale + si) : 0.f;
+                }
+                const int src = want ? lp - win_lo : 0;
+                int page = __shfl_sync(0xffffffffu, win_val, src);
+                const float ks = __shfl_sync(0xffffffffu, win_ks, src);
+                const float vs = __shfl_sync(0xffffffffu, win_vs, src);
+                if (want && (page < 0 || page >= P.num_pages)) {
+                    set_device_error(err_hdr, PA_DEV_BAD_PAGE);
+                    page = -1;
+                }
+                const bool load = want && page >= 0;
+                const uint32_t bytes =
+                    (uint32_t)__popc(__ballot_sync(0xffffffffu, load)) * box_bytes;
+                uint8_t* dst = smem + s * Cfg::kStageBytes + kv * Cfg::kKBytes + m * kSubBytes +
+                               j * rpb * 128;
+                const bool skip = P.test_skip_it == it && blockIdx.x == 0;
+                const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0 && !skip;
+                if (go && lane < 16)
+                    scales[(s * 2 + kv) * 8 + m * 4 + j] = load ? (kv ? vs : ks) : 0.f;
+                __syncwarp();
+                if (lane == 0 && go) {
+                    armed[s] = it / Cfg::kStages;
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                }
+                __syncwarp();
+                if (go && load)
+                    tma_load_4d(dst, kv ? tmv : tmk, &full[s], 0,
+                                ((kt + m) * kDecodeTile + j * rpb) % ps, hk, page);
+                __syncwarp();
+                continue;
+            }
+            int pg[4 * TPS];
+            float ksc[4 * TPS], vsc[4 * TPS];
             uint32_t bytes = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                pg[j] = -1;
-                ksc[j] = vsc[j] = 0.f;
-                if (j >= nbox) continue;
-                const int tok0 = kt * kDecodeTile + j * rpb;
+            for (int jm = 0; jm < 4 * TPS; ++jm) {
+                // box j of the stage's tile m
+                const int m = jm / 4, j = jm % 4;
+                pg[jm] = -1;
+                ksc[jm] = vsc[jm] = 0.f;
+                if (j >= nbox || t + m >= tk.z) continue;
+                const int tok0 = (kt + m) * kDecodeTile + j * rpb;
                 if (tok0 >= ctx_b) continue;
                 const int lp = tok0 / ps;
                 if (lp - win_lo < 0 || lp - win_lo >= 32) {
@@ -236,14 +295,14 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                 }
                 int page = __shfl_sync(0xffffffffu, win_val, lp - win_lo);
                 if (Cfg::kFP8) {
-                    ksc[j] = __shfl_sync(0xffffffffu, win_ks, lp - win_lo);
-                    vsc[j] = __shfl_sync(0xffffffffu, win_vs, lp - win_lo);
+                    ksc[jm] = __shfl_sync(0xffffffffu, win_ks, lp - win_lo);
+                    vsc[jm] = __shfl_sync(0xffffffffu, win_vs, lp - win_lo);
                 }
                 if (page < 0 || page >= P.num_pages) {
                     if (lane == 0) set_device_error(err_hdr, PA_DEV_BAD_PAGE);
                     page = -1;
                 }
-                pg[j] = page;
+                pg[jm] = page;
                 if (page >= 0) bytes += 2u * box_bytes;
             }
             uint8_t* stK = smem + s * Cfg::kStageBytes;
@@ -255,9 +314,9 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
             if (lane == 0 && go) {
                 if (Cfg::kFP8) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        scales[(s * 2 + 0) * 4 + j] = pg[j] >= 0 ? ksc[j] : 0.f;
-                        scales[(s * 2 + 1) * 4 + j] = pg[j] >= 0 ? vsc[j] : 0.f;
+                    for (int jm = 0; jm < 4 * TPS; ++jm) {
+                        scales[(s * 2 + 0) * 4 * TPS + jm] = pg[jm] >= 0 ? ksc[jm] : 0.f;
+                        scales[(s * 2 + 1) * 4 * TPS + jm] = pg[jm] >= 0 ? vsc[jm] : 0.f;
                     }
                 }
                 armed[s] = it / Cfg::kStages;
@@ -273,17 +332,19 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                     if (lane < 2 && pg[0] >= 0)
                         tma_load_5d(lane ? stV : stK, lane ? tmv : tmk, &full[s], 0, slot0, 0, hk,
                                     pg[0]);
-                } else if (lane < 8 * Cfg::kHalves) {
-                    // lane = (kv, page j, column block h)
-                    const int kv = lane / (4 * Cfg::kHalves);
-                    const int j = (lane / Cfg::kHalves) % 4, h = lane % Cfg::kHalves;
+                } else if (lane < 8 * TPS * Cfg::kHalves) {
+                    // lane = (kv, tile m, box j, column block h)
+                    const int kv = lane / (4 * TPS * Cfg::kHalves);
+                    const int jm = (lane / Cfg::kHalves) % (4 * TPS), h = lane % Cfg::kHalves;
+                    const int m = jm / 4, j = jm % 4;
                     int page = -1;
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        if (jj == j) page = pg[jj];
+                    for (int jj = 0; jj < 4 * TPS; ++jj)
+                        if (jj == jm) page = pg[jj];
                     if (page >= 0) {
-                        const int slot0 = (kt * kDecodeTile + j * rpb) % ps;
-                        tma_load_4d((kv ? stV : stK) + h * Cfg::kHalfBytes + j * rpb * 128,
+                        const int slot0 = ((kt + m) * kDecodeTile + j * rpb) % ps;
+                        tma_load_4d((kv ? stV : stK) + m * kSubBytes + h * Cfg::kHalfBytes +
+                                        j * rpb * 128,
                                     kv ? tmv : tmk, &full[s], h * (128 / Cfg::kElem), slot0, hk,
                                     page);
                     }

@@ -59,6 +59,7 @@ struct DecodeFp8Cfg {
     static constexpr int D = 128;
     // geometry the shared producer reads
     static constexpr int kStages = STAGES;
+    static constexpr int kTilesPerStage = 1;                  // one 64-token KV tile a stage
     static constexpr int kProducerWarps = 4;                 // the whole first warpgroup
     static constexpr bool kFP8 = true;
     static constexpr int kElem = 1;
@@ -699,8 +700,15 @@ int decode_fp8_cluster_grid(int nt, int C) {
     return 0;
 }
 
+cudaError_t launch_decode_fp8_tc(const DecodeParams& P, int rows, const CUtensorMap& tq,
+                                 const CUtensorMap& tk, const CUtensorMap& tv,
+                                 cudaStream_t stream);
+
 cudaError_t launch_decode_fp8(const DecodeParams& P, int nt, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+    // the Assign map (with or without a window) runs on the tensor-core kernel
+    // (pa_decode_fp8_tc.cu); static split-K on this file's kernel
+    if (P.static_splits == 0) return launch_decode_fp8_tc(P, 8 * nt, tq, tk, tv, stream);
 #define X(n, st) \
     if (nt == n) return launch_fp8_variant<n, st>(P, tq, tk, tv, stream);
     PA_DECODE_FP8_VARIANTS(X)
