@@ -58,9 +58,9 @@ struct DecodeTcCfg {
     // geometry the shared producer reads
     // the deepest ring that fits beside the other buffers: every stage not
     // held by QK, softmax or PV is a copy in flight
-    static constexpr int kStages = NR == 16 ? 6 : 5;
+    static constexpr int kStages = NR == 16 ? 6 : 4;
     static constexpr int kTilesPerStage = 2;
-    static constexpr int kProducerWarps = 1;
+    static constexpr int kProducerWarps = 2;
     static constexpr bool kFP8 = true;
     static constexpr int kElem = 1;
     static constexpr int kHalves = 1;
@@ -83,7 +83,8 @@ struct DecodeTcCfg {
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffQt = kOffQ + 2 * kQSlotBytes;
     static constexpr int kOffP = kOffQt + kQtBytes;           // [buffer][term]
-    static constexpr int kOffRed = kOffP + 2 * 2 * kPTermBytes;   // [warpgroup][warp][32]
+    static constexpr int kOffEpi = kOffP + 2 * 2 * kPTermBytes;   // bf16 O rows, NR x 256 B
+    static constexpr int kOffRed = kOffEpi + NR * 256;            // [warpgroup][warp][32]
     static constexpr int kOffRowM = kOffRed + 2 * 4 * 32 * 4;     // running max m per row
     static constexpr int kOffRowC = kOffRowM + 32 * 4;        // 2^-e per row
     static constexpr int kOffRowI = kOffRowC + 32 * 4;        // 1 / l per row
@@ -92,7 +93,7 @@ struct DecodeTcCfg {
     static constexpr int kNumBars = 2 * kStages + 4 + 8 + 4;
     static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;   // after TMEM slot, abort flag
     static constexpr int kSmemBytes = kOffArmed + (4 * (kStages + 2) + 15) / 16 * 16 + 1024;
-    static constexpr int kThreads = 352;   // 8 softmax, QK, PV, producer warps
+    static constexpr int kThreads = 384;   // 8 softmax, QK, PV, 2 producer warps
     static constexpr uint32_t kTmemCols = 256;
     static constexpr uint32_t kColS = 128;          // S^T buffer b at column b * kColS
     static constexpr uint32_t kColO = 224;
@@ -179,7 +180,7 @@ __device__ __forceinline__ uint32_t swz_byte(int row, int col) {
 }
 
 template <int NR>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
 decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
@@ -263,10 +264,10 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
     cta_task_range<false>(P, k_begin, k_end);
     const int G = L.G, Hq = L.Hq;
 
-    if (warp == 10) {
-        // ---------------------------------------------------------- producer
+    if (warp >= 10) {
+        // --------------------------------------------------------- producers
         decode_produce<Cfg>(P, &tmq, &tmk, &tmv, smem, full, empty, q_full, q_empty, scales,
-                            abort_flag, armed, err_hdr, k_begin, k_end, 0, lane, wait);
+                            abort_flag, armed, err_hdr, k_begin, k_end, warp - 10, lane, wait);
     } else if (warp == 8 || warp == 9) {
         // ----------------------------------------------------- MMA issuers
         // warp 8 issues the QKs, warp 9 the PVs: each commit tracks the MMAs
@@ -358,6 +359,7 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const float scale_log2 = P.sm_scale * kLog2e;
         float* redw = red + wg * 128;              // [4 warps][32] of this warpgroup
+        const int rpb_log = __ffs(P.rows_per_box) - 1;   // rows per box: a power of two
         uint8_t* qt = smem + Cfg::kOffQt;
         int g = 0, task_it = 0, o_tasks = 0;
         TaskRec mine;
@@ -478,7 +480,7 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                 wait(&s_full[b], (uint32_t)((g >> 1) & 1));
                 wait(&full[s], (uint32_t)((g / S) & 1));
                 tc_fence_after();
-                const int box = (t >> 6) * 4 + (t & 63) / P.rows_per_box;
+                const int box = (t >> 6) * 4 + ((t & 63) >> rpb_log);
                 const float ks = scales[(s * 2 + 0) * 8 + box];
                 const float vs = scales[(s * 2 + 1) * 8 + box];
                 const float lvs = valid ? lg2(vs) : 0.f;
@@ -629,7 +631,8 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                     row_i[r] = ls > 0.f ? 1.f / ls : 0.f;
                     if (r < R) {
                         const float lse_nat = ls > 0.f ? (row_m[r] + lg2(ls)) * kLn2 : -INFINITY;
-                        const int token = tok_base + r / G, head = hk * G + r % G;
+                        const int rt = r / G;
+                        const int token = tok_base + rt, head = hk * G + (r - rt * G);
                         if (tk.w < 0) {
                             if (P.lse != nullptr) P.lse[(int64_t)token * Hq + head] = lse_nat;
                         } else {
@@ -650,16 +653,31 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
 #pragma unroll
                     for (int r = 0; r < HR; ++r) o[r] = 0.f;
                 }
+                if (tk.w < 0) {
+                    // bf16 rows go out through shared memory: thread t holds head
+                    // dim t of every row, a row's 256 bytes are written as 16-byte
+                    // pieces (two-byte stores from each thread are slow)
+                    __nv_bfloat16* epi = reinterpret_cast<__nv_bfloat16*>(smem + Cfg::kOffEpi);
 #pragma unroll
-                for (int r0 = 0; r0 < HR; ++r0) {
-                    const int r = rb + r0;
-                    if (r >= R) break;
-                    const float val = o[r0] * row_i[r];
-                    if (tk.w < 0) {
-                        const int token = tok_base + r / G, head = hk * G + r % G;
-                        P.out[((int64_t)token * Hq + head) * D + t] = __float2bfloat16_rn(val);
-                    } else {
-                        P.part_o[((int64_t)tk.w * L.rows_cap + r) * D + t] = val;
+                    for (int r0 = 0; r0 < HR; ++r0)
+                        epi[(rb + r0) * D + t] = __float2bfloat16_rn(o[r0] * row_i[rb + r0]);
+                    named_bar_sync(bar_wg, 128);
+                    const int r = rb + (t >> 3);
+                    if (r < R) {
+                        const int rt = r / G;
+                        const uint4* src = reinterpret_cast<const uint4*>(epi + r * D) + (t & 7) * 2;
+                        uint4* dst = reinterpret_cast<uint4*>(
+                                         P.out + ((int64_t)(tok_base + rt) * Hq + hk * G + (r - rt * G)) * D) +
+                                     (t & 7) * 2;
+                        dst[0] = src[0];
+                        dst[1] = src[1];
+                    }
+                } else {
+#pragma unroll
+                    for (int r0 = 0; r0 < HR; ++r0) {
+                        const int r = rb + r0;
+                        if (r >= R) break;
+                        P.part_o[((int64_t)tk.w * L.rows_cap + r) * D + t] = o[r0] * row_i[r];
                     }
                 }
                 tc_fence_before();
@@ -673,7 +691,7 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 10) decode_drain<Cfg>(full, q_full, armed, abort_flag, 0, lane);
+    if (warp >= 10) decode_drain<Cfg>(full, q_full, armed, abort_flag, warp - 10, lane);
     __syncthreads();
     if (warp == 8) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
@@ -699,7 +717,7 @@ int decode_fp8_tc_smem_bytes(int rows) {
     return rows <= 16 ? DecodeTcCfg<16>::kSmemBytes
                       : rows <= 32 ? DecodeTcCfg<32>::kSmemBytes : -1;
 }
-int decode_fp8_tc_threads(int rows) { return rows <= 32 ? 352 : -1; }
+int decode_fp8_tc_threads(int rows) { return rows <= 32 ? 384 : -1; }
 const void* decode_fp8_tc_kernel_ptr(int rows) {
     return rows <= 16 ? (const void*)decode_fp8_tc_kernel<16>
                       : rows <= 32 ? (const void*)decode_fp8_tc_kernel<32> : nullptr;
