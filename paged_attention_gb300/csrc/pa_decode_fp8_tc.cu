@@ -83,12 +83,11 @@ struct DecodeTcCfg {
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffQt = kOffQ + 2 * kQSlotBytes;
     static constexpr int kOffP = kOffQt + kQtBytes;           // [buffer][term]
-    static constexpr int kOffEpi = kOffP + 2 * 2 * kPTermBytes;   // bf16 O rows, NR x 256 B
-    static constexpr int kOffRed = kOffEpi + NR * 256;            // [warpgroup][warp][32]
-    static constexpr int kOffRowM = kOffRed + 2 * 4 * 32 * 4;     // running max m per row
-    static constexpr int kOffRowC = kOffRowM + 32 * 4;        // 2^-e per row
-    static constexpr int kOffRowI = kOffRowC + 32 * 4;        // 1 / l per row
-    static constexpr int kOffScale = kOffRowI + 32 * 4;       // [stage][k|v][8 boxes]
+    static constexpr int kOffEpi = kOffP + 2 * 2 * kPTermBytes;   // f32 O rows, NR x D
+    static constexpr int kOffRed = kOffEpi + NR * D * 4;          // [warpgroup][warp][32]
+    static constexpr int kOffRowM = kOffRed + 2 * 4 * 32 * 4;     // running max per row, [2 tasks]
+    static constexpr int kOffRowC = kOffRowM + 2 * 32 * 4;    // sm_scale log2(e) 2^-e per row
+    static constexpr int kOffScale = kOffRowC + 32 * 4;       // [stage][k|v][8 boxes]
     static constexpr int kOffBar = kOffScale + kStages * 2 * 8 * 4;
     static constexpr int kNumBars = 2 * kStages + 4 + 8 + 4;
     static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;   // after TMEM slot, abort flag
@@ -210,7 +209,6 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
     float* red = reinterpret_cast<float*>(smem + Cfg::kOffRed);      // [4 warps][32 rows]
     float* row_m = reinterpret_cast<float*>(smem + Cfg::kOffRowM);
     float* row_c = reinterpret_cast<float*>(smem + Cfg::kOffRowC);
-    float* row_i = reinterpret_cast<float*>(smem + Cfg::kOffRowI);
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
     int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);
@@ -236,7 +234,7 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
             mbar_init(&p_empty[i], 1);
         }
         mbar_init(o_full, 1);
-        mbar_init(o_free, 2);                     // one per softmax warpgroup
+        mbar_init(o_free, 8);                     // one per softmax warp
         mbar_init(qt_full, 1);
         mbar_init(mma_done, 2);                   // the QK and the PV warp
         *abort_flag = 0;
@@ -361,26 +359,14 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
         float* redw = red + wg * 128;              // [4 warps][32] of this warpgroup
         const int rpb_log = __ffs(P.rows_per_box) - 1;   // rows per box: a power of two
         uint8_t* qt = smem + Cfg::kOffQt;
-        int g = 0, task_it = 0, o_tasks = 0;
-        TaskRec mine;
-        for (int k = k_begin; k < k_end; ++k, ++task_it) {
-            if (((k - k_begin) & 31) == 0)
-                mine = fetch_task_rec<false>(P, k + lane, k_end, lane, err_hdr);
-            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
-            const int4 tk = rec.tk;
-            const int hk = rec.un.y, nq = rec.un.w;
-            const int R = G * nq;
-            const int ctx_b = rec.ctx;
-            const int tok_base = rec.cuq + rec.un.z;
-            const int pbase = ctx_b - rec.ql + rec.un.z;
-            const int n = tk.z - tk.y, n2 = (n + 1) / 2;
-            const int first = window_first_tile(L.window, pbase, kDecodeTile);
-
-            // ---- Q rows -> three E4M3 terms (rows R..NR-1 are zeros).  Thread
-            // u = threadIdx.x of the 256 takes row u / 8, head dims [16 (u % 8), +16).
+        // Q rows of task number `ti` (R of them) -> three E4M3 terms (rows
+        // R..NR-1 are zeros); thread u = threadIdx.x of the 256 takes row u / 8,
+        // head dims [16 (u % 8), +16).  Also sets the rows' scale factor c and
+        // clears their running maximum (task parity ti & 1).
+        auto convert_q = [&](int ti, int R) {
             {
-                const int qs = task_it & 1;
-                wait(&q_full[qs], (uint32_t)((task_it >> 1) & 1));
+                const int qs = ti & 1;
+                wait(&q_full[qs], (uint32_t)((ti >> 1) & 1));
                 const int u = threadIdx.x;
                 const int r = u >> 3, qd = u & 7;
                 if (r < NR) {
@@ -437,7 +423,7 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                     }
                     if (qd == 0) {
                         row_c[r] = ldexpf(scale_log2, -ex);
-                        row_m[r] = kNoMax;
+                        row_m[(ti & 1) * 32 + r] = kNoMax;
                     }
                 }
                 fence_proxy_async_smem();
@@ -447,6 +433,26 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                     mbar_arrive(&q_empty[qs]);
                 }
             }
+        };
+        int g = 0, task_it = 0, o_tasks = 0;
+        TaskRec mine;
+        bool fetched = false;   // `mine` already holds the batch of the next task
+        for (int k = k_begin; k < k_end; ++k, ++task_it) {
+            if (((k - k_begin) & 31) == 0 && !fetched)
+                mine = fetch_task_rec<false>(P, k + lane, k_end, lane, err_hdr);
+            fetched = false;
+            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            const int4 tk = rec.tk;
+            const int hk = rec.un.y, nq = rec.un.w;
+            const int R = G * nq;
+            float* rm = row_m + (task_it & 1) * 32;   // this task's running maxima
+            if (k == k_begin) convert_q(task_it, R);   // later tasks: converted early
+            const int ctx_b = rec.ctx;
+            const int tok_base = rec.cuq + rec.un.z;
+            const int pbase = ctx_b - rec.ql + rec.un.z;
+            const int n = tk.z - tk.y, n2 = (n + 1) / 2;
+            const int first = window_first_tile(L.window, pbase, kDecodeTile);
+
             // m starts at -1e30 (not -inf): 2^(y - m) stays 0 for y = -inf, and
             // any finite y exceeds m + 8, so the first stage sets the maxima
             float c[HR], m[HR], m8[HR], l[HR];
@@ -535,14 +541,14 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                     if (t < HR) {
                         const float tm = fmaxf(fmaxf(redw[t], redw[32 + t]),
                                                fmaxf(redw[64 + t], redw[96 + t]));
-                        row_m[rb + t] = fmaxf(row_m[rb + t], tm);
+                        rm[rb + t] = fmaxf(rm[rb + t], tm);
                     }
                     named_bar_sync(bar_wg, 128);
                     bool resc = false;
                     float alpha[HR];
 #pragma unroll
                     for (int r = 0; r < HR; ++r) {
-                        const float mn = row_m[rb + r];
+                        const float mn = rm[rb + r];
                         alpha[r] = m[r] == mn ? 1.f : ex2(m[r] - mn);
                         resc |= alpha[r] != 1.f;
                         l[r] *= alpha[r];
@@ -619,28 +625,25 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                 if (lane == 0) mbar_arrive(&p_full[b]);
             }
 
-            // ---- epilogue: l summed over the 128 tokens, then O / l and LSE
+            // ---- the next task's Q terms now: its first QK overlaps this epilogue
+            if (k + 1 < k_end) {
+                if (((k + 1 - k_begin) & 31) == 0) {
+                    mine = fetch_task_rec<false>(P, k + 1 + lane, k_end, lane, err_hdr);
+                    fetched = true;
+                }
+                const TaskRec nrec = shfl_task_rec(mine, (k + 1 - k_begin) & 31);
+                convert_q(task_it + 1, G * nrec.un.w);
+            }
+
+            // ---- epilogue: l summed over the 128 tokens (warp sums), raw O^T of
+            // this warpgroup's rows into the f32 staging rows, one barrier, then
+            // thread t finishes row rb + t / 8, head dims [16 (t % 8), +16):
+            // O / l (bf16, or the f32 split partial) and the LSE
             {
                 const float wl = warp_reduce_rows<HR>(l, lane,
                                                       [](float x, float z) { return x + z; });
                 if (lane < HR) redw[wq * 32 + lane] = wl;
-                named_bar_sync(bar_wg, 128);
-                if (t < HR) {
-                    const int r = rb + t;
-                    const float ls = (redw[t] + redw[32 + t]) + (redw[64 + t] + redw[96 + t]);
-                    row_i[r] = ls > 0.f ? 1.f / ls : 0.f;
-                    if (r < R) {
-                        const float lse_nat = ls > 0.f ? (row_m[r] + lg2(ls)) * kLn2 : -INFINITY;
-                        const int rt = r / G;
-                        const int token = tok_base + rt, head = hk * G + (r - rt * G);
-                        if (tk.w < 0) {
-                            if (P.lse != nullptr) P.lse[(int64_t)token * Hq + head] = lse_nat;
-                        } else {
-                            P.part_lse[(int64_t)tk.w * L.rows_cap + r] = lse_nat;
-                        }
-                    }
-                }
-                named_bar_sync(bar_wg, 128);
+                float* epi = reinterpret_cast<float*>(smem + Cfg::kOffEpi);   // [NR][D]
                 float o[HR];
                 if (n2 > 0) {
                     wait(o_full, (uint32_t)(o_tasks & 1));
@@ -649,40 +652,54 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                     tmem_ld_rows<HR>(tmem + lane_off + Cfg::kColO + rb, o);
                     tmem_wait_ld();
                     reg_fence_rows<HR>(o);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(o_free);     // O^T may be overwritten
                 } else {
 #pragma unroll
                     for (int r = 0; r < HR; ++r) o[r] = 0.f;
                 }
-                if (tk.w < 0) {
-                    // bf16 rows go out through shared memory: thread t holds head
-                    // dim t of every row, a row's 256 bytes are written as 16-byte
-                    // pieces (two-byte stores from each thread are slow)
-                    __nv_bfloat16* epi = reinterpret_cast<__nv_bfloat16*>(smem + Cfg::kOffEpi);
 #pragma unroll
-                    for (int r0 = 0; r0 < HR; ++r0)
-                        epi[(rb + r0) * D + t] = __float2bfloat16_rn(o[r0] * row_i[rb + r0]);
-                    named_bar_sync(bar_wg, 128);
-                    const int r = rb + (t >> 3);
-                    if (r < R) {
-                        const int rt = r / G;
-                        const uint4* src = reinterpret_cast<const uint4*>(epi + r * D) + (t & 7) * 2;
-                        uint4* dst = reinterpret_cast<uint4*>(
-                                         P.out + ((int64_t)(tok_base + rt) * Hq + hk * G + (r - rt * G)) * D) +
-                                     (t & 7) * 2;
-                        dst[0] = src[0];
-                        dst[1] = src[1];
+                for (int r = 0; r < HR; ++r) epi[(rb + r) * D + t] = o[r];
+                named_bar_sync(bar_wg, 128);
+                const int rr = t >> 3, r = rb + rr, c16 = (t & 7) * 16;
+                if (rr < HR && r < R) {
+                    const float ls = (redw[rr] + redw[32 + rr]) + (redw[64 + rr] + redw[96 + rr]);
+                    const float inv = ls > 0.f ? 1.f / ls : 0.f;
+                    const int rt = r / G;
+                    const int token = tok_base + rt, head = hk * G + (r - rt * G);
+                    if ((t & 7) == 0) {
+                        const float lse_nat = ls > 0.f ? (rm[r] + lg2(ls)) * kLn2 : -INFINITY;
+                        if (tk.w < 0) {
+                            if (P.lse != nullptr) P.lse[(int64_t)token * Hq + head] = lse_nat;
+                        } else {
+                            P.part_lse[(int64_t)tk.w * L.rows_cap + r] = lse_nat;
+                        }
                     }
-                } else {
+                    const float4* src = reinterpret_cast<const float4*>(epi + r * D + c16);
+                    float4 v[4];
 #pragma unroll
-                    for (int r0 = 0; r0 < HR; ++r0) {
-                        const int r = rb + r0;
-                        if (r >= R) break;
-                        P.part_o[((int64_t)tk.w * L.rows_cap + r) * D + t] = o[r0] * row_i[r];
+                    for (int q = 0; q < 4; ++q) {
+                        v[q] = src[q];
+                        v[q].x *= inv;
+                        v[q].y *= inv;
+                        v[q].z *= inv;
+                        v[q].w *= inv;
+                    }
+                    if (tk.w < 0) {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            P.out + ((int64_t)token * Hq + head) * D + c16);
+                        dst[0] = make_uint4(pack_bf16x2(v[0].x, v[0].y), pack_bf16x2(v[0].z, v[0].w),
+                                            pack_bf16x2(v[1].x, v[1].y), pack_bf16x2(v[1].z, v[1].w));
+                        dst[1] = make_uint4(pack_bf16x2(v[2].x, v[2].y), pack_bf16x2(v[2].z, v[2].w),
+                                            pack_bf16x2(v[3].x, v[3].y), pack_bf16x2(v[3].z, v[3].w));
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(
+                            P.part_o + ((int64_t)tk.w * L.rows_cap + r) * D + c16);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) dst[q] = v[q];
                     }
                 }
-                tc_fence_before();
-                named_bar_sync(bar_wg, 128);
-                if (t == 0 && n2 > 0) mbar_arrive(o_free);
             }
         }
     }
