@@ -1,4 +1,6 @@
-// pa_decode_fp8.cu -- persistent split-K decode compute for E4M3 K/V caches.
+// pa_decode_fp8.cu -- split-K decode compute for E4M3 K/V caches on legacy
+// mma.sync, the kernel of the static split-K path (pa_decode_static).  The
+// Assign-map decode runs on the tcgen05 kernel of pa_decode_fp8_tc.cu.
 //
 // "基于Triton-TLE优化Tencent HPC-Ops Attention", 一.2 (Split-K Compute:
 // persistent CTAs follow the task map and emit a final or partial output with
@@ -51,8 +53,8 @@
 namespace pa {
 
 // GENERAL: the instantiation that also takes the static split-K task source
-// and the sliding window; the plain one (the dynamic map, no window) carries
-// neither in its loops.
+// and the sliding window (the only one built); with GENERAL = false the loops
+// carry neither.
 template <int NT, int STAGES, bool GENERAL = false>
 struct DecodeFp8Cfg {
     static constexpr bool kStatic = GENERAL;   // may take the static split-K task source
@@ -630,39 +632,24 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
 
 int decode_fp8_row_tiles(int rows) { return (rows + 7) / 8; }
 
-int decode_fp8_smem_bytes(int nt) {
-#define X(n, st) \
-    if (nt == n) return DecodeFp8Cfg<n, st>::kSmemBytes;
-    PA_DECODE_FP8_VARIANTS(X)
-#undef X
-    return -1;
-}
+// The Assign-map E4M3 decode runs on the tensor-core kernel
+// (pa_decode_fp8_tc.cu); these describe it for the persistent-grid query.
+int decode_fp8_tc_smem_bytes(int rows);
+int decode_fp8_tc_threads(int rows);
+const void* decode_fp8_tc_kernel_ptr(int rows);
+int decode_fp8_smem_bytes(int nt) { return decode_fp8_tc_smem_bytes(8 * nt); }
+int decode_fp8_threads(int nt) { return decode_fp8_tc_threads(8 * nt); }
+const void* decode_fp8_kernel_ptr(int nt) { return decode_fp8_tc_kernel_ptr(8 * nt); }
 
-int decode_fp8_threads(int nt) {
-#define X(n, st) \
-    if (nt == n) return DecodeFp8Cfg<n, st>::kThreads;
-    PA_DECODE_FP8_VARIANTS(X)
-#undef X
-    return -1;
-}
-
-const void* decode_fp8_kernel_ptr(int nt) {
-#define X(n, st) \
-    if (nt == n) return (const void*)decode_fp8_kernel<n, st, false>;
-    PA_DECODE_FP8_VARIANTS(X)
-#undef X
-    return nullptr;
-}
-
+// static split-K (this file's kernel, the instantiation with the static
+// task source)
 template <int NT, int STAGES>
 static cudaError_t launch_fp8_variant(const DecodeParams& P, const CUtensorMap& tq,
                                       const CUtensorMap& tk, const CUtensorMap& tv,
                                       cudaStream_t stream) {
-    using Cfg = DecodeFp8Cfg<NT, STAGES>;
-    using CfgG = DecodeFp8Cfg<NT, STAGES, true>;
-    const bool general = P.static_splits > 0 || P.L.window > 0;
-    auto kern = general ? decode_fp8_kernel<NT, STAGES, true> : decode_fp8_kernel<NT, STAGES, false>;
-    const int smem = general ? CfgG::kSmemBytes : Cfg::kSmemBytes;
+    using Cfg = DecodeFp8Cfg<NT, STAGES, true>;
+    auto kern = decode_fp8_kernel<NT, STAGES, true>;
+    const int smem = Cfg::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (P.static_splits > 0 && P.cluster_size > 1)
