@@ -415,6 +415,12 @@ __device__ __forceinline__ uint32_t ex2_h2(float lo, float hi) {
     asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
     return y;
 }
+// max(a, b, c) in one instruction (three-input max.f32 of sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -539,7 +539,12 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     const int lim = limc - c4 * 32, low = lowc - c4 * 32;
                     if (lim >= 31 && (!WINDOW || low <= 0)) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
+                        for (int c = 0; c < 32; c += 8) {   // three-input max: 2 scores a step
+                            mx4[0] = fmax3(mx4[0], s[c], s[c + 1]);
+                            mx4[1] = fmax3(mx4[1], s[c + 2], s[c + 3]);
+                            mx4[2] = fmax3(mx4[2], s[c + 4], s[c + 5]);
+                            mx4[3] = fmax3(mx4[3], s[c + 6], s[c + 7]);
+                        }
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
@@ -565,6 +570,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 // P's own bf16 rounding); keys [32c, 32c+32) go to S columns
                 // [16c, 16c+16), which every later chunk has already read
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 sl2x2 = make_float2(sl2, sl2), nmu2 = make_float2(-mu, -mu);
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {
                     float s[32];
@@ -591,10 +598,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     if (lim >= 31 && (!WINDOW || low <= 0)) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
-                            const uint32_t e2 = ex2_h2(fmaf(s[c], sl2, -mu),
-                                                       fmaf(s[c + 1], sl2, -mu));
+                            // packed f32x2: the scaled scores and the row sums
+                            const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2x2, nmu2);
+                            const uint32_t e2 = ex2_h2(a.x, a.y);
                             const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&e2));
-                            sum4[(c >> 1) & 3] += pf.x + pf.y;
+                            sum2[(c >> 1) & 1] = __fadd2_rn(sum2[(c >> 1) & 1], pf);
                             if constexpr (FP8)
                                 put_e4m3(c, e2);
                             else
@@ -634,7 +642,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         tmem_st32(tO + c4 * 32, o);
                     }
                 }
-                l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                l = l * alpha + (((sum4[0] + sum4[1]) + (sum4[2] + sum4[3])) +
+                                 ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y)));
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&p_full[h]);
