@@ -84,7 +84,8 @@ def _fingerprint() -> str:
 # Sources that decide what one kernel does on the device (its own file, the
 # shared device helpers, the launcher / tensor-map code and the ABI header).
 KERNEL_SOURCES = {
-    "pa_decode_splitk": ("pa_decode.cu", "pa_decode_fp8.cu", "pa_decode_common.cuh"),
+    "pa_decode_splitk": ("pa_decode.cu", "pa_decode_fp8.cu", "pa_decode_fp8_tc.cu",
+                         "pa_decode_common.cuh"),
     # pa_prefill also runs the decode kernel on the decode part of a mixed batch
     "pa_prefill": ("pa_prefill.cu", "pa_decode.cu", "pa_decode_common.cuh"),
 }

@@ -415,6 +415,16 @@ __device__ __forceinline__ uint32_t ex2_h2(float lo, float hi) {
     asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
     return y;
 }
+// acc.x += low f16 of h2, acc.y += high f16 (mixed-precision add, exact
+// conversion, one instruction each)
+__device__ __forceinline__ void add_f16x2_to_f32(float2& acc, uint32_t h2) {
+    asm("{\n\t.reg .f16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\t"
+        "add.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y)
+        : "r"(h2));
+}
 // max(a, b, c) in one instruction (three-input max.f32 of sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;

@@ -601,12 +601,16 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                             // packed f32x2: the scaled scores and the row sums
                             const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2x2, nmu2);
                             const uint32_t e2 = ex2_h2(a.x, a.y);
-                            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&e2));
-                            sum2[(c >> 1) & 1] = __fadd2_rn(sum2[(c >> 1) & 1], pf);
-                            if constexpr (FP8)
+                            if constexpr (FP8) {
+                                // the f16 pair straight into the f32 sums
+                                add_f16x2_to_f32(sum2[(c >> 1) & 1], e2);
                                 put_e4m3(c, e2);
-                            else
+                            } else {
+                                const float2 pf =
+                                    __half22float2(*reinterpret_cast<const __half2*>(&e2));
+                                sum2[(c >> 1) & 1] = __fadd2_rn(sum2[(c >> 1) & 1], pf);
                                 pk[c >> 1] = pack_bf16x2(pf.x, pf.y);
+                            }
                         }
                     } else {
 #pragma unroll
