@@ -36,7 +36,9 @@
 //               softmax runs; MMAs of one thread execute in issue order,
 //               which keeps QK_h(j+1) from overwriting P_h(j) before PV_h(j)
 //               has read it.  Warp 1 also zeroes V rows past the context.
-//   warp 3      copies the odd pages of every K/V ring entry (see warp 0).
+//   warp 3      copies the odd pages of every K/V ring entry (see warp 0);
+//               with E4M3 K/V it converts V tiles to f16 instead, and warp 0
+//               copies every page.
 //   warps 4-7   softmax for half 0, warps 8-11 for half 1: thread = query row
 //               = TMEM lane.  Reads its S row (tcgen05.ld), applies the
 //               causal / context mask, keeps the running max lazily (O is
@@ -84,11 +86,16 @@ struct PrefillCfg {
     static constexpr int kQBytes = 2 * kQTileBytes;  // two 128-row halves
     static constexpr int kKVBytes = kHalves * kRegion;
     // ring entries (each a K or a V tile)
-    static constexpr int kEntries = FP8 ? 10 : (D == 128 ? 5 : 8);
+    static constexpr int kEntries = FP8 ? 6 : (D == 128 ? 5 : 8);
+    // producer warps (warp 0, and warp 3 for bf16); for E4M3 warp 3 instead
+    // turns each V tile into f16, double-buffered, for an f16 PV
+    static constexpr int kProducers = FP8 ? 1 : 2;
+    static constexpr int kVhBytes = 2 * kRegion;     // f16 V tile: two 64-dim column blocks
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;
-    static constexpr int kOffBar = kOffKV + kEntries * kKVBytes;
-    static constexpr int kNumBars = 2 + 2 * kEntries + 9;
+    static constexpr int kOffVh = kOffKV + kEntries * kKVBytes;
+    static constexpr int kOffBar = kOffVh + (FP8 ? 2 * kVhBytes : 0);
+    static constexpr int kNumBars = 2 + 2 * kEntries + 9 + (FP8 ? 4 : 0);
     // after the TMEM slot and the abort flag: the last phase each producer warp
     // armed with a copy, per ring entry, and that of the Q buffer
     static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;
@@ -109,12 +116,12 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
 
 // WINDOW: the instantiation that takes a sliding window; the other one
 // carries no window arithmetic in its softmax.  FP8: E4M3 Q, K and V
-// ("基于Triton-TLE…", 二: FP8 prefill) -- QK^T and PV on kind::f8f6f4 (K = 32
-// per instruction): S = Q K^T straight from the E4M3 tiles (both K-major);
-// the softmax scales S by q_scale * k_scale, and writes P into tensor memory
-// as two E4M3 terms, P ~ P_hi + P_lo (P_hi = e4m3(P), P_lo = e4m3(P - P_hi):
-// about 2^-8 relative, the precision of a bf16 P); PV runs one MMA per term
-// with V read MN-major from its E4M3 tile; v_scale is applied to O in the
+// ("基于Triton-TLE…", 二: FP8 prefill) -- QK^T on kind::f8f6f4 (K = 32 per
+// instruction) straight from the E4M3 Q and K tiles (both K-major); the
+// softmax scales S by q_scale * k_scale and writes its f16 exponentials into
+// tensor memory as they are; warp 3 (not a producer here) turns every E4M3
+// V tile into an f16 tile (exact), double-buffered, and PV runs as a
+// kind::f16 MMA (f16 P, f16 V, MN-major).  v_scale is applied to O in the
 // epilogue.
 template <int D, bool WINDOW, bool FP8>
 __global__ void __launch_bounds__(384, 1)
@@ -136,6 +143,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     uint64_t* o_done = p_full + 2;            // [2]
     uint64_t* o_free = o_done + 2;            // [2]
     uint64_t* mma_done = o_free + 2;
+    uint64_t* vh_full = mma_done + 1;         // [2] E4M3: f16 V buffer written
+    uint64_t* vh_empty = vh_full + 2;         // [2] E4M3: f16 V buffer read by both PVs
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // [2][E] entries, then Q
@@ -154,7 +163,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         mbar_init(q_full, 1);
         mbar_init(q_empty, 2);                 // one commit from each MMA warp
         for (int e = 0; e < E; ++e) {
-            mbar_init(&kv_full[e], 2);            // the two producer warps
+            mbar_init(&kv_full[e], Cfg::kProducers);   // each producer warp arms it
             mbar_init(&kv_empty[e], 2);
         }
         for (int h = 0; h < 2; ++h) {
@@ -164,6 +173,12 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             mbar_init(&o_free[h], 128);
         }
         mbar_init(mma_done, 2);
+        if constexpr (FP8) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&vh_full[b], 1);
+                mbar_init(&vh_empty[b], 2);      // one commit from each MMA warp
+            }
+        }
         *abort_flag = 0;
         for (int i = 0; i < 2 * E + 1; ++i) armed[i] = -1;
         fence_mbar_init();
@@ -204,7 +219,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
 
     if (warp < 4) {
       regs_dec<Cfg::kRegsProducer>();
-      if (warp == 0 || warp == 3) {
+      if (warp == 0 || (warp == 3 && !FP8)) {
         // --------------------------------------------------------- producers
         // A tensor copy holds its issuing thread for hundreds of cycles, so
         // the boxes of every ring entry are split by page between warp 0 (even
@@ -212,6 +227,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         // its own bytes before its own copies, so neither waits for the
         // other.  Warp 0 also loads Q.
         const int pw = warp == 0 ? 0 : 1;
+        constexpr int kP = Cfg::kProducers;
         if (lane == 0) {
             prefetch_tmap(&tmq);
             prefetch_tmap(&tmk);
@@ -277,7 +293,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         page = -1;
                     }
                     pg[j] = page;
-                    if (page >= 0 && (j & 1) == pw) bytes += box_bytes;
+                    if (page >= 0 && (j % kP) == pw) bytes += box_bytes;
                 }
                 // K first (QK needs it first), then V, each into its own ring entry
 #pragma unroll
@@ -297,8 +313,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         mbar_arrive_expect_tx(&kv_full[e], bytes);   // this warp's pages
                     }
                     __syncwarp();
-                    if (go && lane < 4 * Cfg::kHalves) {
-                        const int j = pw + 2 * (lane / Cfg::kHalves), c = lane % Cfg::kHalves;
+                    if (go && lane < (8 / kP) * Cfg::kHalves) {
+                        const int j = pw + kP * (lane / Cfg::kHalves), c = lane % Cfg::kHalves;
                         int page = -1;
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj)
@@ -315,6 +331,72 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 }
             }
         }
+    } else if (FP8 && warp == 3) {
+        // --------------------------------------------- V converter (E4M3)
+        // Each V tile, as it lands in the ring, becomes an f16 tile in one of
+        // two buffers laid out as a bf16 V tile would be (two 64-dim column
+        // blocks, 128-byte swizzle), so that PV runs as an f16 MMA with P in
+        // f16 -- the softmax then writes its f16 exponentials as they are.
+        // Rows of keys past the context are written as zeros (E4M3 NaN codes
+        // in stale slots would otherwise poison 0 * V).  The ring entry goes
+        // back to the producer as soon as its bytes are in registers.
+        int e_it = 0, vt = 0;
+        TaskRec mine;
+        for (int k = k_begin; k < k_end; ++k) {
+            if (((k - k_begin) & 31) == 0)
+                mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
+            const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            const int u = rec.tk.x;
+            const int n = rec.tk.z - rec.tk.y;
+            const int ctx_b = rec.ctx;
+            for (int j = 0; j < n; ++j, ++vt) {
+                const int eV = e_it + 2 * j + 1;
+                const int kt = tile_of(u, rec.tk.y + j, ctx_b - rec.ql + rec.un.z);
+                const int first_bad = ctx_b - kt * kPrefillTile;   // rows >= this are zeros
+                wait(&kv_full[eV % E], (uint32_t)((eV / E) & 1));
+                wait(&vh_empty[vt & 1], (uint32_t)((vt >> 1) & 1) ^ 1u);
+                const uint8_t* src = smem + Cfg::kOffKV + (eV % E) * Cfg::kKVBytes;
+                uint8_t* dst = smem + Cfg::kOffVh + (vt & 1) * Cfg::kVhBytes;
+#pragma unroll 1
+                for (int rr = 0; rr < kPrefillTile / 32; ++rr) {
+                    const int r = rr * 32 + lane;
+                    const bool ok = r < first_bad;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        // source chunks 4 half .. 4 half + 3 = head dims [64 half, +64)
+                        uint4 w[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            w[c] = *reinterpret_cast<const uint4*>(src + swz128(r, 4 * half + c));
+                        uint8_t* blk = dst + half * Cfg::kRegion;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t x[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+                            uint32_t h[8];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                h[2 * q] = ok ? e4m3x2_to_f16x2((uint16_t)(x[q] & 0xffffu)) : 0u;
+                                h[2 * q + 1] = ok ? e4m3x2_to_f16x2((uint16_t)(x[q] >> 16)) : 0u;
+                            }
+                            *reinterpret_cast<uint4*>(blk + swz128(r, 2 * c)) =
+                                make_uint4(h[0], h[1], h[2], h[3]);
+                            *reinterpret_cast<uint4*>(blk + swz128(r, 2 * c + 1)) =
+                                make_uint4(h[4], h[5], h[6], h[7]);
+                        }
+                    }
+                }
+                __syncwarp();
+                // the E4M3 entry is free (both of its releases), the f16 tile ready
+                if (lane == 0) {
+                    mbar_arrive(&kv_empty[eV % E]);
+                    mbar_arrive(&kv_empty[eV % E]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&vh_full[vt & 1]);
+            }
+            e_it += 2 * n;
+        }
     } else if (warp == 1 || warp == 2) {
         // ------------------------------------------------------ MMA issuers
         // warp 1 issues every MMA of half 0, warp 2 those of half 1: each
@@ -328,14 +410,16 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         // per barrier phase).
         constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(128, 128, false, false)
                                           : idesc_bf16_f32(128, 128, false, false);
-        constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3_f32(128, D, false, true)
+        // E4M3: PV is an f16 MMA over the converter's f16 V tile and an f16 P
+        constexpr uint32_t idesc_pv = FP8 ? idesc_f16_f32(128, D, false, true)
                                           : idesc_bf16_f32(128, D, false, true);
         // Descriptor bases: the start-address field is the low bits of a
         // descriptor, so a byte offset within the buffer is added as offset >> 4.
         const uint64_t dQ = smem_desc_sw128(smem_u32(smem + Cfg::kOffQ), 16, 1024);
         const uint64_t dK = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), 16, 1024);
         const uint64_t dV = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), Cfg::kRegion, 1024);
-        int e_it = 0, task_it = 0;
+        const uint64_t dVh = smem_desc_sw128(smem_u32(smem + Cfg::kOffVh), Cfg::kRegion, 1024);
+        int e_it = 0, task_it = 0, vt = 0;
         int p_cnt[2] = {0, 0}, of_cnt[2] = {0, 0};
         TaskRec mine;
 
@@ -355,23 +439,14 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             tc_commit(&s_full[h]);
         };
         auto issue_pv = [&](int h, int e, bool first) {   // O_h += P_h V from ring entry e
-            const uint64_t b0 = dV + (uint64_t)((e * Cfg::kKVBytes) >> 4);
+            // (E4M3: e is the f16 V buffer)
+            const uint64_t b0 = FP8 ? dVh + (uint64_t)((e * Cfg::kVhBytes) >> 4)
+                                    : dV + (uint64_t)((e * Cfg::kKVBytes) >> 4);
             const uint32_t d = tmem + h * 256 + 128, a = tmem + h * 256;
-            if constexpr (FP8) {
-                // 32 keys per instruction; P's columns [16kk, 16kk + 8) hold the
-                // P_hi bytes of keys [32kk, 32kk + 32), the next 8 their P_lo
 #pragma unroll
-                for (int kk = 0; kk < kPrefillTile / 32; ++kk) {
-                    const uint64_t b = b0 + (uint64_t)((kk * 32 * 128) >> 4);
-                    tc_mma_ts_f8(d, a + kk * 16, b, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                    tc_mma_ts_f8(d, a + kk * 16 + 8, b, idesc_pv, 1u);
-                }
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < kPrefillTile / 16; ++kk)
-                    tc_mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
-                              (!first || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kPrefillTile / 16; ++kk)
+                tc_mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
+                          (!first || kk > 0) ? 1u : 0u);
             tc_commit(&o_done[h]);
         };
 
@@ -410,10 +485,13 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 __syncwarp();
                 token_pass();
             }
-            for (int j = 0; j < n; ++j) {
+            for (int j = 0; j < n; ++j, ++vt) {
                 const int eV = e_it + 2 * j + 1, eKn = e_it + 2 * j + 2;
-                wait(&kv_full[eV % E], (uint32_t)((eV / E) & 1));
-                {
+                if constexpr (FP8)
+                    wait(&vh_full[vt & 1], (uint32_t)((vt >> 1) & 1));   // f16 V ready
+                else
+                    wait(&kv_full[eV % E], (uint32_t)((eV / E) & 1));
+                if constexpr (!FP8) {
                     // zero V rows of keys past the context (P is 0 there, 0 * NaN is
                     // not): warp 1 writes, both MMA warps meet before their PV
                     const int kt = tile_of(u, rec.tk.y + j, ctx_b - rec.ql + rec.un.z);
@@ -448,10 +526,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 if (lane == 0) {
                     if (mine_half) {
                         tc_fence_after();
-                        issue_pv(h, eV % E, j == 0);
+                        issue_pv(h, FP8 ? (vt & 1) : eV % E, j == 0);
                         if (j + 1 < n) issue_qk(h, eKn % E);
                     }
-                    tc_commit(&kv_empty[eV % E]);
+                    // (E4M3: the converter released the V entry; PV read the f16 copy)
+                    tc_commit(FP8 ? &vh_empty[vt & 1] : &kv_empty[eV % E]);
                     if (j + 1 < n) tc_commit(&kv_empty[eKn % E]);
                     if (j + 1 == n - 1) tc_commit(q_empty);
                 }
@@ -580,21 +659,6 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     reg_fence32(s);
                     const int lim = limc - c4 * 32, low = lowc - c4 * 32;
                     uint32_t pk[16];
-                    // E4M3: the pair (P_c, P_c+1), as f16, becomes P_hi bytes
-                    // (columns 0-7 of the chunk's 16) and P_lo = e4m3(P - P_hi)
-                    // bytes (columns 8-15), four keys to a 32-bit column
-                    auto put_e4m3 = [&](int c, uint32_t e2) {
-                        const uint16_t hb = f16x2_to_e4m3x2(e2);
-                        const uint16_t lb = f16x2_to_e4m3x2(hsub2_u32(e2, e4m3x2_to_f16x2(hb)));
-                        const int w = c >> 2;
-                        if ((c & 2) == 0) {
-                            pk[w] = hb;
-                            pk[8 + w] = lb;
-                        } else {
-                            pk[w] |= (uint32_t)hb << 16;
-                            pk[8 + w] |= (uint32_t)lb << 16;
-                        }
-                    };
                     if (lim >= 31 && (!WINDOW || low <= 0)) {
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
@@ -602,9 +666,9 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                             const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2x2, nmu2);
                             const uint32_t e2 = ex2_h2(a.x, a.y);
                             if constexpr (FP8) {
-                                // the f16 pair straight into the f32 sums
+                                // f16 P as computed; the pair straight into the f32 sums
                                 add_f16x2_to_f32(sum2[(c >> 1) & 1], e2);
-                                put_e4m3(c, e2);
+                                pk[c >> 1] = e2;
                             } else {
                                 const float2 pf =
                                     __half22float2(*reinterpret_cast<const __half2*>(&e2));
@@ -620,10 +684,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                             const float e1 = (c + 1 <= lim && (!WINDOW || c + 1 >= low))
                                                  ? ex2(fmaf(s[c + 1], sl2, -mu)) : 0.f;
                             sum4[(c >> 1) & 3] += e0 + e1;
-                            if constexpr (FP8)
-                                put_e4m3(c, pack_f16x2_sat(e0, e1));
-                            else
-                                pk[c >> 1] = pack_bf16x2(e0, e1);
+                            pk[c >> 1] = FP8 ? pack_f16x2_sat(e0, e1) : pack_bf16x2(e0, e1);
                         }
                     }
                     tmem_st16(tS + c4 * 16, pk);
@@ -711,7 +772,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     // waited for all their MMAs (the mma_done commit).
     if (*abort_flag && threadIdx.x == 0) {
         for (int e = 0; e < E; ++e) {
-            const int a0 = armed[e], a1 = armed[E + e];
+            const int a0 = armed[e], a1 = Cfg::kProducers == 2 ? armed[E + e] : a0;
             const int ph = a0 > a1 ? a0 : a1;
             if (ph < 0) continue;
             if (a0 != a1) mbar_arrive(&kv_full[e]);
