@@ -88,7 +88,7 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, vp, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int64, vp, vp, vp,
-                ctypes.c_int64, ctypes.c_int]
+                ctypes.c_int64, ctypes.c_int, ctypes.c_int]
             lib.oracle_combine.restype = None
             lib.oracle_combine.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]
             lib.oracle_e4m3_to_double.restype = ctypes.c_double
@@ -208,11 +208,12 @@ class TaskMap:
 
 
 def assign(mode, num_seqs, num_q_heads, num_kv_heads, num_ctas, kv_tile, balance_rows,
-           context_lens, q_lens, block_mask=None, mask_tile=128, window=0):
+           context_lens, q_lens, block_mask=None, mask_tile=128, window=0, unit_cost=0):
     """Oracle Assign (the tile-by-tile procedure written in pa_oracle.c).
 
     mode 0 = decode units (b, hk); mode 1 = prefill / mixed units (b, hk, q tile).
     window > 0: a unit's tiles start at the first one its first query can see.
+    unit_cost: the fixed cost of a unit with tiles, in tile-weight units.
     """
     lib = _load()
     ctx = _arr(context_lens, np.int32)
@@ -242,7 +243,7 @@ def assign(mode, num_seqs, num_q_heads, num_kv_heads, num_ctas, kv_tile, balance
         (bm.shape[1] if bm is not None else 0), (bm.shape[2] if bm is not None else 0),
         int(mask_tile), _ptr(units), _ptr(ntiles), _ptr(active), int(max_kv_tiles),
         _ptr(cta_ptr), _ptr(tasks), int(task_cap), _ptr(nsplit), _ptr(slot0), _ptr(counts),
-        int(unit_cap), int(window))
+        int(unit_cap), int(window), int(unit_cost))
     if rc != 0:
         raise ValueError(f"oracle_assign failed with status {rc}")
     U, n_tasks, n_slots = (int(x) for x in counts)
@@ -259,7 +260,8 @@ MIXED_DECODE_ROWS = 16
 
 
 def assign_prefill(num_seqs, num_q_heads, num_kv_heads, num_ctas, balance_rows,
-                   context_lens, q_lens, block_mask=None, decode_ctas=None, window=0):
+                   context_lens, q_lens, block_mask=None, decode_ctas=None, window=0,
+                   unit_cost=0, decode_unit_cost=None):
     """Prefill-mode Assign as pa_assign(PA_MODE_PREFILL) defines it.
 
     Returns (prefill_map, decode_map).  Each map is the plain Assign over the
@@ -268,17 +270,22 @@ def assign_prefill(num_seqs, num_q_heads, num_kv_heads, num_ctas, balance_rows,
     is None when the batch has a block mask or G > MIXED_DECODE_ROWS (every
     sequence then stays in the prefill map).  decode_ctas: the decode map's CTA
     count (default num_ctas).  window: the sliding window, passed to both maps
-    (a unit's tiles start at the first one its first query can see)."""
+    (a unit's tiles start at the first one its first query can see).  unit_cost /
+    decode_unit_cost: the fixed cost per unit of the prefill / decode map (the
+    decode map's defaults to unit_cost)."""
+    if decode_unit_cost is None:
+        decode_unit_cost = unit_cost
     G = num_q_heads // num_kv_heads
     ql = [int(x) for x in q_lens]
     if block_mask is not None or G > MIXED_DECODE_ROWS:
         return assign(1, num_seqs, num_q_heads, num_kv_heads, num_ctas, 128, balance_rows,
-                      context_lens, ql, block_mask, window=window), None
+                      context_lens, ql, block_mask, window=window,
+                      unit_cost=unit_cost), None
     small_q = MIXED_DECODE_ROWS // G
     ql_pre = [q if q > small_q else 0 for q in ql]
     ql_dec = [q if q <= small_q else 0 for q in ql]
     pre = assign(1, num_seqs, num_q_heads, num_kv_heads, num_ctas, 128, balance_rows,
-                 context_lens, ql_pre, window=window)
+                 context_lens, ql_pre, window=window, unit_cost=unit_cost)
     dec = assign(0, num_seqs, num_q_heads, num_kv_heads, decode_ctas or num_ctas, 64,
-                 balance_rows, context_lens, ql_dec, window=window)
+                 balance_rows, context_lens, ql_dec, window=window, unit_cost=decode_unit_cost)
     return pre, dec

@@ -366,11 +366,14 @@ void oracle_combine(int S, int D, const double* o_parts, const double* lse_parts
  *     the mask tile) it is the ascending list of kt with kt*kv_tile < L_u and
  *     mask[b][q0/mask_tile][kt] != 0 ([HPC] 二.1 active-KV-tile list).
  *     n_u = length of the list.
- *  3. Weight w_u = max(1, ceil(R_u / balance_rows)).
- *  4. Cost prefix P_u = sum_{u'<u} n_u' w_u', total C.  CTA c owns the cost
- *     interval [a_c, a_{c+1}) with a_c = floor(c*C/N).  List position t of
- *     unit u sits at cost P_u + t*w_u and belongs to the CTA whose interval
- *     contains it.
+ *  3. Weight w_u = max(1, ceil(R_u / balance_rows)).  A unit with tiles also
+ *     carries a fixed cost h_u = unit_cost (0 for a unit without tiles): the
+ *     work a CTA spends on a unit besides its tiles (its queries in, its
+ *     rows out), in the units of a tile's weight.
+ *  4. Cost prefix P_u = sum_{u'<u} (h_u' + n_u' w_u'), total C.  CTA c owns
+ *     the cost interval [a_c, a_{c+1}) with a_c = floor(c*C/N).  List
+ *     position t of unit u sits at cost P_u + h_u + t*w_u and belongs to the
+ *     CTA whose interval contains it.
  *  5. A task is a maximal run of one unit's positions owned by one CTA.
  *     Tasks are ordered by CTA, then cost; cta_ptr[c] is the first task of
  *     CTA c.  The k-th task of a unit has split index k; S_u = task count.
@@ -392,14 +395,15 @@ int oracle_assign(int mode, int B, int Hq, int Hkv, int N, int kv_tile, int bala
                   int mask_kv_tiles, int mask_tile, int32_t* units, int32_t* unit_ntiles,
                   int32_t* active, int max_kv_tiles, int32_t* cta_ptr, int32_t* tasks,
                   int64_t task_cap, int32_t* unit_nsplit, int32_t* unit_slot0, int32_t* counts,
-                  int64_t unit_cap, int window)
+                  int64_t unit_cap, int window, int unit_cost)
 {
     int G, qtok, b, hk, c;
     int64_t U = 0, u, C, n_tasks = 0, slots = 0;
     int64_t* prefix;
     int64_t* bound;
     int64_t* weight;
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N <= 0 || kv_tile <= 0 || balance_rows <= 0)
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N <= 0 || kv_tile <= 0 || balance_rows <= 0 ||
+        unit_cost < 0)
         return -1;
     G = Hq / Hkv;
     if (mode == 1 && (G > 128 || 128 % G))
@@ -476,7 +480,7 @@ int oracle_assign(int mode, int B, int Hq, int Hkv, int N, int kv_tile, int bala
         weight[u] = (R + balance_rows - 1) / balance_rows;
         if (weight[u] < 1)
             weight[u] = 1;
-        prefix[u + 1] = prefix[u] + unit_ntiles[u] * weight[u];
+        prefix[u + 1] = prefix[u] + (unit_ntiles[u] > 0 ? unit_cost : 0) + unit_ntiles[u] * weight[u];
     }
     C = prefix[U];
     for (c = 0; c <= N; ++c)
@@ -490,7 +494,7 @@ int oracle_assign(int mode, int B, int Hq, int Hkv, int N, int kv_tile, int bala
         int t, cur_cta = -1;
         unit_nsplit[u] = 0;
         for (t = 0; t < unit_ntiles[u]; ++t) {
-            int64_t x = prefix[u] + t * w;
+            int64_t x = prefix[u] + unit_cost + t * w;
             int owner = 0;
             /* owner = the last CTA whose interval starts at or before x */
             while (owner + 1 < N && bound[owner + 1] <= x)

@@ -55,7 +55,8 @@ def test_worked_examples(oracle_mod, ex):
 
 # ------------------------------------------------------- brute force
 
-def brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask=None, mask_tile=128, window=0):
+def brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask=None, mask_tile=128, window=0,
+                unit_cost=0):
     G = Hq // Hkv
     units = []
     for b in range(B):
@@ -80,13 +81,16 @@ def brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask=None, mask_tile=128,
             reach = [t for t in reach if t < mask.shape[2] and mask[b, q0 // mask_tile, t]]
         lists.append(reach)
     weights = [max(1, -(-(G * u[3]) // rbal)) for u in units]
-    costs = list(itertools.accumulate([0] + [len(l) * w for l, w in zip(lists, weights)]))
+    # a unit with tiles carries unit_cost ahead of its first tile
+    fixed = [unit_cost if len(l) else 0 for l in lists]
+    costs = list(itertools.accumulate([0] + [h + len(l) * w
+                                             for h, l, w in zip(fixed, lists, weights)]))
     C = costs[-1]
     bounds = [c * C // N for c in range(N + 1)]
     owned = []                      # (cta, unit, position)
     for u, lst in enumerate(lists):
         for t in range(len(lst)):
-            x = costs[u] + t * weights[u]
+            x = costs[u] + fixed[u] + t * weights[u]
             owned.append((bisect.bisect_right(bounds, x) - 1 if C else 0, u, t))
     owned = [(min(c, N - 1), u, t) for c, u, t in owned]
     tasks = []
@@ -334,3 +338,48 @@ def test_prefill_split_with_window(oracle_mod, seed):
         for (b, hk, q0, nq), n in zip(dec.units.tolist(), dec.unit_ntiles.tolist()):
             first = max(0, ctx[b] - ql[b] - window + 1) // 64
             assert n == ((-(-ctx[b] // 64) - first) if nq > 0 else 0)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_unit_cost_matches_brute_force(oracle_mod, seed):
+    """A fixed cost per unit with tiles (our reading of "equal work per CTA":
+    a unit costs its CTA something besides its tiles), placed ahead of the
+    unit's first tile: the oracle and the brute force agree, every tile is
+    still covered once, and a CTA's tile work plus the fixed costs of the
+    units it starts stays within one tile weight plus one fixed cost of C/N."""
+    rng = np.random.default_rng(1000 + seed)
+    mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask = random_case(rng)
+    h = int(rng.choice([1, 2, 3, 7]))
+    tm = oracle_mod.assign(mode, B, Hq, Hkv, N, T, rbal, np.array(ctx, np.int32),
+                           np.array(ql, np.int32), mask, unit_cost=h)
+    bf = brute_force(mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask, unit_cost=h)
+    assert tm.units.tolist() == bf["units"]
+    assert tm.tasks.tolist() == bf["tasks"]
+    assert tm.cta_ptr.tolist() == bf["cta_ptr"]
+    assert tm.unit_nsplit.tolist() == bf["nsplit"]
+    assert tm.unit_slot0.tolist() == bf["slot0"]
+    for u, n in enumerate(tm.unit_ntiles):
+        runs = [t for t in tm.tasks.tolist() if t[0] == u]
+        pos = 0
+        for _, t0, t1, _ in runs:
+            assert t0 == pos and t1 > t0
+            pos = t1
+        assert pos == n
+    wmax = max(bf["weights"]) if bf["weights"] else 1
+    for c in range(N):
+        cost = 0
+        for k in range(tm.cta_ptr[c], tm.cta_ptr[c + 1]):
+            u, t0, t1, _ = tm.tasks[k]
+            cost += (t1 - t0) * bf["weights"][u] + (h if t0 == 0 else 0)
+        assert abs(cost - bf["C"] / N) <= wmax + h + 1e-9
+
+
+def test_unit_cost_zero_is_the_plain_map(oracle_mod):
+    """unit_cost = 0 leaves the map of the plain procedure unchanged."""
+    rng = np.random.default_rng(7)
+    mode, B, Hq, Hkv, N, T, rbal, ctx, ql, mask = random_case(rng)
+    a = oracle_mod.assign(mode, B, Hq, Hkv, N, T, rbal, np.array(ctx, np.int32),
+                          np.array(ql, np.int32), mask)
+    b = oracle_mod.assign(mode, B, Hq, Hkv, N, T, rbal, np.array(ctx, np.int32),
+                          np.array(ql, np.int32), mask, unit_cost=0)
+    assert a.tasks.tolist() == b.tasks.tolist() and a.cta_ptr.tolist() == b.cta_ptr.tolist()
