@@ -63,6 +63,8 @@ CONFIG_SET = [
     ("prefill_fp8_dense_q0_hnd", "prefill_fp8_dense_q0_hnd", 0),
 ]
 PARALLELISM = "independent batch per GPU x{world}"
+# pa_problem.unit_cost for every Assign of the run (0 = the library's choice)
+UNIT_COST = 0
 
 
 def load_peaks():
@@ -330,7 +332,7 @@ class Case:
             self.splits = B.pa_static_num_splits(self.bufs.problem, 0)
             self.runner = lambda w, bufs: B.run_decode_static(w, bufs)
         else:
-            self.bufs = B.make_buffers(self.w, self.mode)
+            self.bufs = B.make_buffers(self.w, self.mode, unit_cost=UNIT_COST)
             self.runner = B.run_decode if self.mode == B.PA_MODE_DECODE else B.run_prefill
 
     def step(self, ev=None, w=None, bufs=None):
@@ -365,6 +367,43 @@ class Case:
         if ev is not None:
             ev[1].record(self.stream)
         B.pa_combine(p, mode, bufs.assign_ws, bufs.partial_ws, bufs.out, bufs.lse)
+
+    def balance(self):
+        """One extra step (outside every timed region) with the task trace on:
+        how evenly the persistent CTAs share the compute launch.  Per CTA the
+        busy time runs from its first task's start to its last task's end."""
+        import torch
+        B = self.B
+        if is_static(self.name):
+            return None
+        cap = int(self.bufs.assign_ws.numel() // 16) + 1024
+        trace = torch.full((cap, 3), -1, dtype=torch.int64, device=self.bufs.out.device)
+        B.pa_set_task_trace(trace)
+        try:
+            self.step()
+            torch.cuda.synchronize()
+        finally:
+            B.pa_set_task_trace(None)
+        tm = B.pa_read_task_map(self.bufs.problem, self.mode, self.bufs.assign_ws)
+        T = tm["num_tasks"]
+        if T == 0 or T > cap:
+            return None
+        tr = trace[:T].cpu().numpy()
+        cp = tm["cta_ptr"]
+        busy = []
+        for c in range(len(cp) - 1):
+            if cp[c + 1] > cp[c]:
+                seg = tr[cp[c]:cp[c + 1]]
+                busy.append((seg[:, 1].max() - seg[:, 0].min()) / 1000.0)
+        busy = np.array(busy)
+        t0 = tr[:, 0].min()
+        return {"tasks": int(T), "ctas_with_tasks": int(len(busy)),
+                "cta_busy_us": {"min": round(float(busy.min()), 1),
+                                "mean": round(float(busy.mean()), 1),
+                                "max": round(float(busy.max()), 1)},
+                "max_over_mean": round(float(busy.max() / busy.mean()), 3),
+                "last_end_us": round(float((tr[:, 1].max() - t0) / 1000.0), 1),
+                "how": "task trace (pa_set_task_trace) of one extra step"}
 
     def device_error(self):
         ws = self.bufs.ws if is_static(self.name) else self.bufs.assign_ws
@@ -502,7 +541,7 @@ def e2e_measure(case, args, dist, dev):
             if hqs is not None:
                 wk.q_scale = torch.empty_like(w.q_scale)
         bk = case.bufs if k == 0 else (B.StaticBuffers(w, 0) if is_static(case.name)
-                                       else B.make_buffers(w, case.mode))
+                                       else B.make_buffers(w, case.mode, unit_cost=UNIT_COST))
         hout = torch.empty(bk.out.shape, dtype=bk.out.dtype).pin_memory()
         hlse = torch.empty(bk.lse.shape, dtype=bk.lse.dtype).pin_memory()
         sets.append((wk, bk, hout, hlse))
@@ -621,6 +660,9 @@ def config_entry(key, name, mtp, args, dev, peaks, uuid):
              "config": workload_config(case.w_cpu, name, 1)}
     if name == "tiny_mixed":
         entry["note"] = "launch-bound: parity workload, time reported only"
+    bal = case.balance()
+    if bal is not None:
+        entry["balance"] = bal
     if is_static(name):
         entry["static_splits"] = case.splits
         entry["note"] = ("static split-K (no Assign, no Combine; splits of a unit on one "
@@ -672,6 +714,9 @@ def run_native(args, rank, world, dist):
         "clocks": clk,
         "graph": graph,
     }
+    bal = case.balance()
+    if bal is not None:
+        line["balance"] = bal
     first = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(case.w_cpu, name, args.cpu_seconds)
@@ -762,6 +807,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window (bf16 decode workloads): keys p - window < j <= p")
+    ap.add_argument("--unit-cost", type=int, default=0,
+                    help="Assign's fixed cost per unit (pa_problem.unit_cost; 0 = the library's "
+                         "choice, < 0 = none)")
     ap.add_argument("--mtp", type=int, default=0,
                     help="decode workloads: q_len = 1 + MTP (default: 1 for bf16, 2 for E4M3)")
     ap.add_argument("--shrink", type=int, default=1,
@@ -769,6 +817,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    global UNIT_COST
+    UNIT_COST = args.unit_cost
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None

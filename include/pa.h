@@ -141,7 +141,19 @@ typedef struct pa_problem {
                                   pa_prefill_fp8, which needs kv_dtype PA_FP8_E4M3
                                   and head_dim 128; decode takes bf16 Q only     */
     int32_t q_scale_mode;      /* E4M3 Q: PA_SCALE_PER_TENSOR or PA_SCALE_PER_ROW    */
+    int32_t unit_cost;         /* Assign's fixed cost of a unit with tiles, in the
+                                  units of a tile's weight (the work a CTA spends
+                                  on a unit besides its tiles); 0 = the library's
+                                  choice (PA_DEFAULT_UNIT_COST_*), < 0 = none   */
 } pa_problem;
+
+/* The library's fixed cost per unit when pa_problem.unit_cost is 0, by Assign
+ * mode (the decode part of a mixed batch takes the decode value).  Measured
+ * on GB300: with none, the CTAs that draw many short units finish up to 30 %
+ * after the mean (per-task timings from pa_set_task_trace); these values
+ * bring the slowest within ~5 % on the decode and prefill batches. */
+#define PA_DEFAULT_UNIT_COST_DECODE 6
+#define PA_DEFAULT_UNIT_COST_PREFILL 4
 
 /* Human-readable name of a pa_status or PA_DEV_* code set. */
 PA_API const char* pa_status_string(int status);
@@ -413,6 +425,25 @@ PA_API pa_status pa_read_task_map(const pa_problem* problem, int mode, const voi
  * wait_limit_ns: 1e6 .. 1e9 (else PA_ERR_INVALID_ARG).
  */
 PA_API pa_status pa_test_inject_wait_timeout(int32_t skip_entry, int64_t wait_limit_ns);
+
+/*
+ * Task trace (diagnostics: how evenly the persistent CTAs share a launch's
+ * work; the pages describe no such call).  While a buffer is set, every
+ * compute launch that walks an Assign task map -- the decode kernel of
+ * pa_decode_splitk and pa_decode_noalloc, the tensor-core kernel of
+ * pa_prefill / pa_prefill_fp8; not the static path and not the decode part of
+ * a mixed batch -- records, for task k of its map (k < capacity):
+ *   trace[3k]     the %globaltimer (ns) when its CTA starts the task,
+ *   trace[3k + 1] the %globaltimer when the CTA is done with it,
+ *   trace[3k + 2] the CTA index.
+ * One thread per CTA writes; the rest of the kernel is unchanged.  Tasks
+ * number as in pa_read_task_map.  Entries of tasks that did not run keep their
+ * previous contents, so clear the buffer before the launch to be traced.
+ *   trace: int64 [capacity][3], DEVICE pointer, 8-byte aligned, or NULL to stop
+ *          tracing (then capacity must be 0).  The caller keeps it alive while set.
+ * The setting is process-wide and stays until changed.
+ */
+PA_API pa_status pa_set_task_trace(int64_t* trace, int64_t capacity);
 
 /* Read (and keep) the device error word of assign_ws into *code (host);
  * synchronises `stream`.  Returns PA_OK when *code == PA_DEV_OK, else

@@ -36,10 +36,23 @@ EXPORTED = (
     "pa_partial_workspace_size", "pa_assign", "pa_decode_splitk", "pa_combine", "pa_prefill",
     "pa_read_task_map", "pa_last_device_error", "pa_decode_noalloc",
     "pa_test_inject_wait_timeout", "pa_static_workspace_size", "pa_static_num_splits",
-    "pa_decode_static", "pa_prefill_fp8",
+    "pa_decode_static", "pa_prefill_fp8", "pa_set_task_trace",
 )
 
 PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # size of the library's fixed scratch
+# pa_problem.unit_cost = 0 takes these (PA_DEFAULT_UNIT_COST_DECODE / _PREFILL)
+PA_DEFAULT_UNIT_COST_DECODE = 6
+PA_DEFAULT_UNIT_COST_PREFILL = 4
+
+
+def effective_unit_cost(unit_cost: int, mode: int) -> int:
+    """The fixed cost per unit Assign uses for pa_problem.unit_cost in `mode`
+    (the decode part of a mixed batch takes the decode value)."""
+    if unit_cost > 0:
+        return unit_cost
+    if unit_cost < 0:
+        return 0
+    return PA_DEFAULT_UNIT_COST_DECODE if mode == PA_MODE_DECODE else PA_DEFAULT_UNIT_COST_PREFILL
 
 
 class PaError(RuntimeError):
@@ -72,6 +85,7 @@ class PaProblem(ctypes.Structure):
         ("window", ctypes.c_int32),
         ("q_dtype", ctypes.c_int32),
         ("q_scale_mode", ctypes.c_int32),
+        ("unit_cost", ctypes.c_int32),
     ]
 
 
@@ -113,6 +127,7 @@ def load(build_if_missing: bool = True):
             "pa_last_device_error": (i32, [vp, ctypes.POINTER(ctypes.c_int32), vp]),
             "pa_decode_noalloc": (i32, [PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pa_test_inject_wait_timeout": (i32, [ctypes.c_int32, ctypes.c_int64]),
+            "pa_set_task_trace": (i32, [vp, ctypes.c_int64]),
             "pa_static_workspace_size": (sz, [PP, ctypes.c_int32]),
             "pa_static_num_splits": (i32, [PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
             "pa_decode_static": (i32, [PP, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
@@ -153,7 +168,7 @@ def _check(status: int, where: str):
         raise PaError(status, where)
 
 
-def problem_from(w, num_ctas: int = 0, balance_rows: int = 0) -> PaProblem:
+def problem_from(w, num_ctas: int = 0, balance_rows: int = 0, unit_cost: int = 0) -> PaProblem:
     """pa_problem for a Workload (shapes only)."""
     ql = [int(x) for x in w.q_lens]
     ctx = [int(x) for x in w.context_lens]
@@ -168,7 +183,8 @@ def problem_from(w, num_ctas: int = 0, balance_rows: int = 0) -> PaProblem:
         mask_kv_tiles=(bm.shape[2] if bm is not None else 0),
         num_ctas=num_ctas, balance_rows=balance_rows, sm_scale=float(w.sm_scale),
         window=int(getattr(w, "window", 0)), q_dtype=int(getattr(w, "q_dtype", PA_BF16)),
-        q_scale_mode=int(getattr(w, "q_scale_mode", PA_SCALE_PER_TENSOR)))
+        q_scale_mode=int(getattr(w, "q_scale_mode", PA_SCALE_PER_TENSOR)),
+        unit_cost=int(unit_cost))
 
 
 # ------------------------------------------------------------ entry points
@@ -262,6 +278,17 @@ def pa_prefill_fp8(problem, q, q_scale, k_cache, v_cache, block_table, context_l
         _stream(stream)), "pa_prefill_fp8")
 
 
+def pa_set_task_trace(trace: Optional[torch.Tensor]):
+    """Record per-task start/end times of the following launches into
+    ``trace`` (int64 [capacity, 3] on the device), or stop with None."""
+    if trace is None:
+        _check(load().pa_set_task_trace(None, 0), "pa_set_task_trace")
+        return
+    if trace.dtype != torch.int64 or trace.dim() != 2 or trace.shape[1] != 3:
+        raise ValueError("trace must be int64 [capacity, 3]")
+    _check(load().pa_set_task_trace(_p(trace), int(trace.shape[0])), "pa_set_task_trace")
+
+
 def pa_read_task_map(problem, mode, assign_ws, stream=None) -> dict:
     """Copy the task map out of the Assign workspace (synchronises)."""
     lib = load()
@@ -318,10 +345,11 @@ class Buffers:
         self.lse = torch.empty((total_q, Hq), dtype=torch.float32, device=device)
 
 
-def make_buffers(w, mode: Optional[int] = None, num_ctas: int = 0, balance_rows: int = 0):
+def make_buffers(w, mode: Optional[int] = None, num_ctas: int = 0, balance_rows: int = 0,
+                 unit_cost: int = 0):
     if mode is None:
         mode = PA_MODE_DECODE if w.mode == "decode" else PA_MODE_PREFILL
-    prob = problem_from(w, num_ctas=num_ctas, balance_rows=balance_rows)
+    prob = problem_from(w, num_ctas=num_ctas, balance_rows=balance_rows, unit_cost=unit_cost)
     return Buffers(prob, mode, w.q.device, w.total_q, w.num_q_heads, w.head_dim)
 
 

@@ -366,10 +366,17 @@ int combine_grid(const WsLayout& L) {
     return grid < 1 ? 1 : (int)grid;
 }
 
+std::atomic<int64_t*> g_trace{nullptr};
+std::atomic<int64_t> g_trace_cap{0};
 std::atomic<int32_t> g_test_skip{-1};
 std::atomic<uint64_t> g_test_limit{0};
 
 }  // namespace
+
+void take_task_trace(int64_t** trace, int64_t* capacity) {
+    *trace = g_trace.load();
+    *capacity = *trace != nullptr ? g_trace_cap.load() : 0;
+}
 
 void take_test_hook(int32_t* skip_entry, uint64_t* wait_limit_ns) {
     const int32_t s = g_test_skip.exchange(-1);
@@ -406,6 +413,10 @@ bool layout_for(const pa_problem& p, int mode, int N, int rows_cap, WsLayout& L)
     L.has_mask = p.mask_q_tiles > 0 ? 1 : 0;
     L.rows_cap = rows_cap;
     L.balance_rows = p.balance_rows > 0 ? p.balance_rows : kDefaultBalanceRows;
+    L.unit_cost = p.unit_cost > 0 ? p.unit_cost
+                  : p.unit_cost < 0 ? 0
+                  : (mode == PA_MODE_DECODE ? PA_DEFAULT_UNIT_COST_DECODE
+                                            : PA_DEFAULT_UNIT_COST_PREFILL);
     L.total_q = p.total_q_tokens;
     L.max_q_len = p.max_q_len;
     L.max_ctx = p.max_context_len;
@@ -791,6 +802,14 @@ pa_status pa_prefill_fp8(const pa_problem* problem, const void* q, const float* 
     return prefill_body(problem, q, q_scale, k_cache, v_cache, block_table, context_lens, q_lens,
                         k_scale, v_scale, block_mask, assign_ws, assign_ws_bytes, partial_ws,
                         partial_ws_bytes, out, lse, stream);
+}
+
+pa_status pa_set_task_trace(int64_t* trace, int64_t capacity) {
+    if (capacity < 0 || (trace == nullptr) != (capacity == 0) || !aligned(trace, 8))
+        return PA_ERR_INVALID_ARG;
+    g_trace_cap.store(capacity);
+    g_trace.store(trace);
+    return PA_OK;
 }
 
 pa_status pa_test_inject_wait_timeout(int32_t skip_entry, int64_t wait_limit_ns) {

@@ -284,7 +284,12 @@ __device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm, int32_
 
     // cost prefix
     int64_t cost = 0;
-    for (int u = u0; u < u1; ++u) cost += (int64_t)n_of(u) * w_of(u);
+    // a unit with tiles also costs L.unit_cost, ahead of its first tile
+    const int64_t h = L.unit_cost;
+    for (int u = u0; u < u1; ++u) {
+        const int n = n_of(u);
+        cost += (n > 0 ? h : 0) + (int64_t)n * w_of(u);
+    }
     int64_t C;
     const int64_t run0 = block_exscan(cost, &C, sm);
 
@@ -296,9 +301,10 @@ __device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm, int32_
             const int n = n_of(u);
             const int64_t w = w_of(u);
             prefix[u] = run;
+            const int64_t hu = n > 0 ? h : 0;
             int S = 0;
-            for_each_owner(run, n, w, C, N, [&](int, int, int) { ++S; });
-            run += (int64_t)n * w;
+            for_each_owner(run + hu, n, w, C, N, [&](int, int, int) { ++S; });
+            run += hu + (int64_t)n * w;
             nsplit[u] = S;
             // completion counters of the in-kernel finalizer of split units
 #pragma unroll
@@ -321,12 +327,13 @@ __device__ void assign_map_body(const WsLayout& L, void* ws, int64_t* sm, int32_
             const int s0 = S > 1 ? (int)s_run : -1;
             slot0[u] = s0;
             int k = 0;
-            for_each_owner(run, n, w, C, N, [&](int c, int tlo, int thi) {
+            const int64_t hu = n > 0 ? h : 0;
+            for_each_owner(run + hu, n, w, C, N, [&](int c, int tlo, int thi) {
                 tasks[t_run + k] = make_int4(u, tlo, thi, S > 1 ? s0 + k : -1);
                 task_cta[t_run + k] = c;
                 ++k;
             });
-            run += (int64_t)n * w;
+            run += hu + (int64_t)n * w;
             t_run += S;
             s_run += S > 1 ? S : 0;
             if (S != 1 && nq_of(u) > 0) fix[f_run++] = u;

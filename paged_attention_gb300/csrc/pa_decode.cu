@@ -170,10 +170,12 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
         int it = 0, task_it = 0, mround = 0;
         const uint32_t rank = use_cluster ? cluster_ctarank() : 0u;
         TaskRec mine;
+        const bool tracer = threadIdx.x == Cfg::kProducerWarps * 32;   // task trace
         for (int k = k_begin; k < k_end; ++k, ++task_it) {
             if (((k - k_begin) & 31) == 0)
                 mine = fetch_task_rec<STATIC>(P, k + lane, k_end, lane, err_hdr);
             const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            if (tracer) trace_task_start(P.trace, P.trace_cap, k);
             const int4 tk = rec.tk;
             const int4 un = rec.un;
             const int hk = un.y, q0 = un.z, nq = un.w;
@@ -459,6 +461,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                 }
             }
             named_bar_sync(5 + rt, 128 * NG);
+            if (tracer) trace_task_end(P.trace, P.trace_cap, k);
         }
     }
     grid_launch_dependents();
@@ -640,6 +643,11 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
     P.test_skip_it = -1;
     P.wait_limit_ns = kWaitLimitNs;
     if (take_hook) take_test_hook(&P.test_skip_it, &P.wait_limit_ns);
+    // the task trace follows the Assign map's task numbering: not on the
+    // static path, nor on the decode part of a mixed batch
+    P.trace = nullptr;
+    P.trace_cap = 0;
+    if (take_hook && static_splits == 0) take_task_trace(&P.trace, &P.trace_cap);
     if (is_fp8(p)) {
         if (p.head_dim != 128) return cudaErrorInvalidValue;
         return launch_decode_fp8(P, decode_fp8_row_tiles(unit_rows(p)), tq, tk, tv, stream);

@@ -34,6 +34,8 @@ struct DecodeParams {
     int32_t test_skip_it;     // test hook: CTA 0 leaves this KV tile's stage unfilled (-1 none)
     int32_t static_splits;    // 0: tasks from the Assign map; S > 0: static split-K, S splits
     int32_t cluster_size;     // static split-K on clusters of S CTAs (DSM merge); else 1
+    int64_t* trace;           // task trace (pa_set_task_trace), or nullptr
+    int64_t trace_cap;
     float sm_scale;
     uint64_t wait_limit_ns;
 };

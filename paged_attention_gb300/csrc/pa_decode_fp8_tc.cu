@@ -442,6 +442,7 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                 mine = fetch_task_rec<false>(P, k + lane, k_end, lane, err_hdr);
             fetched = false;
             const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            if (threadIdx.x == 0) trace_task_start(P.trace, P.trace_cap, k);
             const int4 tk = rec.tk;
             const int hk = rec.un.y, nq = rec.un.w;
             const int R = G * nq;
@@ -701,6 +702,7 @@ decode_fp8_tc_kernel(const __grid_constant__ DecodeParams P, const __grid_consta
                     }
                 }
             }
+            if (threadIdx.x == 0) trace_task_end(P.trace, P.trace_cap, k);
         }
     }
 

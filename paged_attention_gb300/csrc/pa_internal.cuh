@@ -69,6 +69,7 @@ struct WsLayout {
     int32_t has_mask;
     int32_t rows_cap;     // partial rows per slot
     int32_t balance_rows;
+    int32_t unit_cost;        // Assign's fixed cost of a unit with tiles (tile-weight units)
     int32_t total_q;
     int32_t max_q_len, max_ctx;
     int32_t mask_q_tiles, mask_kv_tiles;
@@ -96,6 +97,8 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 // entry CTA 0's producer should leave unfilled (-1: none) and the wait limit
 // for the next compute launch, and disarms the hook.
 void take_test_hook(int32_t* skip_entry, uint64_t* wait_limit_ns);
+// The task trace set by pa_set_task_trace (nullptr, 0 when none).
+void take_task_trace(int64_t** trace, int64_t* capacity);
 
 template <typename T>
 __host__ __device__ inline T* ws_ptr(void* ws, int64_t off) {
@@ -617,6 +620,20 @@ __device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h2) {
     asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(d) : "r"(h2));
     return d;
 }
+// Task trace (diagnostics, pa_set_task_trace): task k of the map is recorded
+// as trace[3k] = the time its CTA starts it, trace[3k + 1] = the time it is
+// done (%globaltimer, ns), trace[3k + 2] = the CTA.  One thread per CTA calls
+// these; nothing is written without a trace buffer.
+__device__ __forceinline__ void trace_task_start(int64_t* trace, int64_t cap, int k) {
+    if (trace != nullptr && k < cap) {
+        trace[3 * (int64_t)k] = (int64_t)globaltimer();
+        trace[3 * (int64_t)k + 2] = (int64_t)blockIdx.x;
+    }
+}
+__device__ __forceinline__ void trace_task_end(int64_t* trace, int64_t cap, int k) {
+    if (trace != nullptr && k < cap) trace[3 * (int64_t)k + 1] = (int64_t)globaltimer();
+}
+
 // Two f32 values -> two E4M3 bytes (lo in the low byte), round to nearest,
 // saturating to +-448.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {

@@ -73,6 +73,8 @@ struct PrefillParams {
     const float* k_scale;
     const float* v_scale;
     int32_t q_scale_per_row;
+    int64_t* trace;          // task trace (pa_set_task_trace), or nullptr
+    int64_t trace_cap;
     float sm_scale;
     uint64_t wait_limit_ns;
 };
@@ -562,6 +564,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             if (((k - k_begin) & 31) == 0)
                 mine = load_task_rec(tasks, units, P.ctx, P.ql, cu_q, k + lane, k_end);
             const TaskRec rec = shfl_task_rec(mine, (k - k_begin) & 31);
+            if (threadIdx.x == 128) trace_task_start(P.trace, P.trace_cap, k);   // half 0, row 0
             const int u = rec.tk.x, hk = rec.un.y, q0 = rec.un.z;
             const int R = G * rec.un.w;
             if (h == 1 && R <= kPrefillHalfRows) continue;   // half 1 idle for this unit
@@ -758,6 +761,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             }
             tc_fence_before();
             mbar_arrive(&o_free[h]);
+            if (threadIdx.x == 128) trace_task_end(P.trace, P.trace_cap, k);
         }
     }
 
@@ -843,6 +847,7 @@ cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, cons
     P.q_scale_per_row = p.q_scale_mode == PA_SCALE_PER_ROW ? 1 : 0;
     P.sm_scale = p.sm_scale;
     take_test_hook(&P.test_skip_it, &P.wait_limit_ns);
+    take_task_trace(&P.trace, &P.trace_cap);
     const bool win = p.window > 0;
     const bool fp8 = p.q_dtype == PA_FP8_E4M3;
     cudaError_t e = cudaErrorInvalidValue;

@@ -127,6 +127,9 @@ def test_noalloc_host_checks(lib):
     assert B.PA_NOALLOC_SCRATCH_BYTES == 32 * 1024 * 1024
     header = open(os.path.join(ROOT, "include", "pa.h")).read()
     assert "#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)" in header
+    # the binding's copy of the default fixed cost per unit
+    assert f"#define PA_DEFAULT_UNIT_COST_DECODE {B.PA_DEFAULT_UNIT_COST_DECODE}\n" in header
+    assert f"#define PA_DEFAULT_UNIT_COST_PREFILL {B.PA_DEFAULT_UNIT_COST_PREFILL}\n" in header
 
 
 def test_static_workspace_sizes_host_only(lib):
@@ -174,3 +177,14 @@ def test_fp8_prefill_host_checks(lib):
     st = lib.pa_prefill_fp8(ctypes.byref(p), fake, None, *([fake] * 7), None, fake, 1 << 30,
                             fake, 1 << 30, fake, fake, None)
     assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_task_trace_host_checks(lib):
+    """pa_set_task_trace: a buffer with a capacity, or NULL with 0."""
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.pa_set_task_trace(None, 5) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_set_task_trace(fake, 0) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_set_task_trace(fake, -1) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_set_task_trace(ctypes.c_void_p((1 << 20) + 4), 3) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_set_task_trace(fake, 3) == B.PA_OK         # never dereferenced here
+    assert lib.pa_set_task_trace(None, 0) == B.PA_OK

@@ -17,9 +17,12 @@ from gpu_util import task_map_equal
 pytestmark = pytest.mark.gpu
 
 
-def check(w, mode, num_ctas=0, balance_rows=0):
+def check(w, mode, num_ctas=0, balance_rows=0, unit_cost=0):
     wd = w.to("cuda")
-    bufs = B.make_buffers(wd, mode, num_ctas=num_ctas, balance_rows=balance_rows)
+    bufs = B.make_buffers(wd, mode, num_ctas=num_ctas, balance_rows=balance_rows,
+                          unit_cost=unit_cost)
+    h = B.effective_unit_cost(unit_cost, mode)
+    hd = B.effective_unit_cost(unit_cost, B.PA_MODE_DECODE)
     N = B.pa_num_ctas(bufs.problem, mode)
     B.pa_assign(bufs.problem, mode, wd.context_lens, wd.q_lens,
                 wd.block_mask if mode == B.PA_MODE_PREFILL else None, bufs.assign_ws)
@@ -28,7 +31,7 @@ def check(w, mode, num_ctas=0, balance_rows=0):
     if mode == B.PA_MODE_DECODE:
         tm = oracle.assign(mode, w.num_seqs, w.num_q_heads, w.num_kv_heads, N, 64,
                            balance_rows or 128, w.context_lens, w.q_lens,
-                           window=int(getattr(w, "window", 0)))
+                           window=int(getattr(w, "window", 0)), unit_cost=h)
         task_map_equal(gpu, tm, with_active=False)
         return gpu
     # prefill mode: the prefill map and the decode part (its own CTA count: the
@@ -41,7 +44,8 @@ def check(w, mode, num_ctas=0, balance_rows=0):
     pre, dec = oracle.assign_prefill(w.num_seqs, w.num_q_heads, w.num_kv_heads, N,
                                      balance_rows or 128, w.context_lens, w.q_lens,
                                      w.block_mask, decode_ctas=Nd,
-                                     window=int(getattr(w, "window", 0)))
+                                     window=int(getattr(w, "window", 0)), unit_cost=h,
+                                     decode_unit_cost=hd)
     task_map_equal(gpu, pre, with_active=w.block_mask is not None)
     gpu_d = B.pa_read_task_map(bufs.problem, B.PA_MAP_DECODE_PART, bufs.assign_ws)
     if dec is None:
@@ -137,3 +141,15 @@ def test_prefill_map_with_sliding_window(window, sparse):
     h = W.hybrid_bf16(shrink=8)
     h.window = window
     check(h, B.PA_MODE_PREFILL, num_ctas=37)
+
+
+@pytest.mark.parametrize("unit_cost", [-1, 1, 3, 16])
+def test_decode_map_unit_cost(unit_cost):
+    """Explicit fixed costs per unit (and none): bit-exact with the oracle."""
+    check(W.decode_bf16(mtp=1), B.PA_MODE_DECODE, unit_cost=unit_cost)
+
+
+@pytest.mark.parametrize("unit_cost", [-1, 2, 5])
+def test_prefill_maps_unit_cost(unit_cost):
+    check(W.hybrid_bf16(shrink=4), B.PA_MODE_PREFILL, unit_cost=unit_cost)
+    check(W.prefill_bf16(sparse=True, shrink=4), B.PA_MODE_PREFILL, unit_cost=unit_cost)

@@ -38,8 +38,10 @@ def check(w, num_ctas=0):
     pd.max_q_len = min(pd.max_q_len, max(1, oracle.MIXED_DECODE_ROWS // G))
     split = G <= oracle.MIXED_DECODE_ROWS
     Nd = B.pa_num_ctas(pd, B.PA_MODE_DECODE) if split else N
-    pre, dec = oracle.assign_prefill(w.num_seqs, w.num_q_heads, w.num_kv_heads, N, 128,
-                                     w.context_lens, w.q_lens, decode_ctas=Nd)
+    pre, dec = oracle.assign_prefill(
+        w.num_seqs, w.num_q_heads, w.num_kv_heads, N, 128, w.context_lens, w.q_lens,
+        decode_ctas=Nd, unit_cost=B.effective_unit_cost(bufs.problem.unit_cost, B.PA_MODE_PREFILL),
+        decode_unit_cost=B.effective_unit_cost(bufs.problem.unit_cost, B.PA_MODE_DECODE))
     task_map_equal(B.pa_read_task_map(bufs.problem, B.PA_MODE_PREFILL, bufs.assign_ws), pre,
                    with_active=False)
     gd = B.pa_read_task_map(bufs.problem, B.PA_MAP_DECODE_PART, bufs.assign_ws)
