@@ -216,6 +216,33 @@ bool encode_kv_map_one_box(const pa_problem& p, const void* base, CUtensorMap* m
     return r == CUDA_SUCCESS;
 }
 
+// bf16 K/V with head_dim 128 for the prefill kernel, as (d % 64, slot % 8,
+// column block, slot / 8, page) with the head folded into the column-block
+// coordinate (NHD: chunk = 2 head + d / 64) or into the page coordinate (HND:
+// page * H + head).  A box of a page's rows lands as 8-token groups, each the
+// two 128-byte-swizzled [8 x 128 B] column blocks: one copy per page.
+bool encode_kv_map_grouped(const pa_problem& p, const void* base, CUtensorMap* map) {
+    auto fn = encode_fn();
+    if (!fn || p.kv_dtype != PA_BF16 || p.head_dim != 128) return false;
+    const cuuint64_t D = p.head_dim, ps = p.page_size, H = p.num_kv_heads, NP = p.num_pages;
+    cuuint64_t dims[5], strides[4];
+    if (p.layout == PA_NHD) {
+        const cuuint64_t tok = H * D * 2;
+        dims[0] = 64; dims[1] = 8; dims[2] = 2 * H; dims[3] = ps / 8; dims[4] = NP;
+        strides[0] = tok; strides[1] = 128; strides[2] = 8 * tok; strides[3] = ps * tok;
+    } else {
+        dims[0] = 64; dims[1] = 8; dims[2] = 2; dims[3] = ps / 8; dims[4] = NP * H;
+        strides[0] = D * 2; strides[1] = 128; strides[2] = 8 * D * 2; strides[3] = ps * D * 2;
+    }
+    const cuuint32_t rows = p.page_size < 64 ? p.page_size : 64;
+    cuuint32_t box[5] = {64, 8, 2, rows / 8, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Q viewed as (d, head, token): box = 128 bytes of d (64 bf16 or 128 E4M3
 // elements) x G heads x box_tokens tokens
 bool encode_q_map(const pa_problem& p, const void* base, int box_tokens, CUtensorMap* map) {
@@ -507,23 +534,29 @@ pa_status prefill_body(const pa_problem* problem, const void* q, const float* q_
     if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
     if (partial_ws_bytes < (size_t)M.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
         return PA_ERR_WORKSPACE;
+    // K/V maps: by 8-token group for bf16 with head_dim 128, else (d, slot,
+    // head, page) boxes of up to 64 slots
+    const bool grouped = p.kv_dtype == PA_BF16 && p.head_dim == 128;
     CUtensorMap tq, tk, tv;
     if (!encode_q_map(p, q, kPrefillHalfRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
-        !encode_kv_map(p, k_cache, &tk) ||
-        !encode_kv_map(p, v_cache, &tv))
+        !(grouped ? encode_kv_map_grouped(p, k_cache, &tk) : encode_kv_map(p, k_cache, &tk)) ||
+        !(grouped ? encode_kv_map_grouped(p, v_cache, &tv) : encode_kv_map(p, v_cache, &tv)))
         return PA_ERR_INVALID_ARG;
     const cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
     if (M.split) {
-        // the decode-shaped sequences first, on the decode kernel; its 4-D
-        // K/V maps are the prefill kernel's
+        // the decode-shaped sequences first, on the decode kernel, with its
+        // own K/V maps
         CUtensorMap tqd, tkd, tvd;
         if (!encode_q_map(M.pd, q, M.pd.max_q_len > 0 ? M.pd.max_q_len : 1, &tqd))
             return PA_ERR_INVALID_ARG;
         const bool one_box = encode_kv_map_one_box(M.pd, k_cache, &tkd) &&
                              encode_kv_map_one_box(M.pd, v_cache, &tvd);
+        if (!one_box &&
+            (!encode_kv_map(M.pd, k_cache, &tkd) || !encode_kv_map(M.pd, v_cache, &tvd)))
+            return PA_ERR_INVALID_ARG;
         // (the wait-timeout test hook is left for the prefill kernel)
-        e = launch_decode_from_api(M.pd, M.Ld, tqd, one_box ? tkd : tk, one_box ? tvd : tv,
+        e = launch_decode_from_api(M.pd, M.Ld, tqd, tkd, tvd,
                                    one_box, block_table, context_lens, q_lens, k_scale, v_scale,
                                    const_cast<void*>(assign_ws),
                                    static_cast<char*>(partial_ws) + M.part_off, out, lse, s,

@@ -67,6 +67,11 @@ struct PrefillParams {
     int32_t max_pages_per_seq;
     int32_t rows_per_box;    // min(page_size, 64)
     int32_t boxes_per_tile;  // 128 / rows_per_box
+    // coordinates of a grouped K/V box (bf16, D = 128): chunk = kv_chunk_mul *
+    // head; last coordinate = page * kv_page_mul + head * kv_head_add
+    int32_t kv_chunk_mul;
+    int32_t kv_page_mul;
+    int32_t kv_head_add;
     int32_t test_skip_it;    // test hook: CTA 0 leaves this K/V ring entry unfilled (-1 none)
     // E4M3 Q/K/V: Q scale (one, or one per (token, q head)), one K and one V scale
     const float* q_scale;
@@ -87,6 +92,13 @@ struct PrefillCfg {
     static constexpr int kQTileBytes = kHalves * kRegion;
     static constexpr int kQBytes = 2 * kQTileBytes;  // two 128-row halves
     static constexpr int kKVBytes = kHalves * kRegion;
+    // K/V tiles are stored by 8-token group: group g holds its kHalves
+    // column blocks of 8 rows x 128 bytes (1 KB each) at g * kGroupStride.
+    // One tensor copy of a page then fills whole groups of both column
+    // blocks, and the 8-row groups of each column block still sit at one
+    // uniform stride, as the MMA descriptors need.  With one column block
+    // (E4M3, or bf16 with D = 64) this is the plain row-major tile.
+    static constexpr int kGroupStride = kHalves * 1024;
     // ring entries (each a K or a V tile)
     static constexpr int kEntries = FP8 ? 6 : (D == 128 ? 5 : 8);
     // producer warps (warp 0, and warp 3 for bf16); for E4M3 warp 3 instead
@@ -98,10 +110,10 @@ struct PrefillCfg {
     static constexpr int kOffVh = kOffKV + kEntries * kKVBytes;
     static constexpr int kOffBar = kOffVh + (FP8 ? 2 * kVhBytes : 0);
     static constexpr int kNumBars = 2 + 2 * kEntries + 9 + (FP8 ? 4 : 0);
-    // after the TMEM slot and the abort flag: the last phase each producer warp
-    // armed with a copy, per ring entry, and that of the Q buffer
+    // after the TMEM slot and the abort flag: the last phase armed with a copy,
+    // per ring entry, and that of the Q buffer
     static constexpr int kOffArmed = kOffBar + kNumBars * 8 + 16;
-    static constexpr int kSmemBytes = kOffArmed + (4 * (2 * kEntries + 1) + 15) / 16 * 16 + 1024;
+    static constexpr int kSmemBytes = kOffArmed + (4 * (kEntries + 1) + 15) / 16 * 16 + 1024;
     static constexpr int kThreads = 384;
     static constexpr int kRegsLaunch = 168;          // 65536 / 384, rounded down to 8
     static constexpr int kRegsProducer = 88;
@@ -149,7 +161,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     uint64_t* vh_empty = vh_full + 2;         // [2] E4M3: f16 V buffer read by both PVs
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // [2][E] entries, then Q
+    int* armed = reinterpret_cast<int*>(smem + Cfg::kOffArmed);   // [E] entries, then Q
     const WsLayout& L = P.L;
     int32_t* header = ws_ptr<int32_t>(P.ws, L.off_header);
     int32_t* err_hdr = ws_ptr<int32_t>(P.ws, L.off_err_header);   // device faults
@@ -165,7 +177,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         mbar_init(q_full, 1);
         mbar_init(q_empty, 2);                 // one commit from each MMA warp
         for (int e = 0; e < E; ++e) {
-            mbar_init(&kv_full[e], Cfg::kProducers);   // each producer warp arms it
+            mbar_init(&kv_full[e], 1);      // armed by the warp that fills it
             mbar_init(&kv_empty[e], 2);
         }
         for (int h = 0; h < 2; ++h) {
@@ -182,7 +194,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             }
         }
         *abort_flag = 0;
-        for (int i = 0; i < 2 * E + 1; ++i) armed[i] = -1;
+        for (int i = 0; i < E + 1; ++i) armed[i] = -1;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -224,10 +236,10 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
       if (warp == 0 || (warp == 3 && !FP8)) {
         // --------------------------------------------------------- producers
         // A tensor copy holds its issuing thread for hundreds of cycles, so
-        // the boxes of every ring entry are split by page between warp 0 (even
-        // pages) and warp 3 (odd pages).  Each arms the entry's barrier for
-        // its own bytes before its own copies, so neither waits for the
-        // other.  Warp 0 also loads Q.
+        // with two producer warps (bf16) warp 0 fills the K entries and warp 3
+        // the V entries, each issuing one page per lane: the two copy chains
+        // run side by side.  With one (E4M3) warp 0 fills both.  Warp 0 also
+        // loads Q.
         const int pw = warp == 0 ? 0 : 1;
         constexpr int kP = Cfg::kProducers;
         if (lane == 0) {
@@ -254,7 +266,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 // h's column block c (one tensor copy per lane)
                 const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
                 if (lane == 0 && go) {
-                    armed[2 * E] = task_it;
+                    armed[E] = task_it;
                     mbar_arrive_expect_tx(q_full, (uint32_t)H * Cfg::kQTileBytes);
                 }
                 __syncwarp();
@@ -295,38 +307,42 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         page = -1;
                     }
                     pg[j] = page;
-                    if (page >= 0 && (j % kP) == pw) bytes += box_bytes;
+                    if (page >= 0) bytes += box_bytes;
                 }
                 // K first (QK needs it first), then V, each into its own ring entry
 #pragma unroll
                 for (int kv = 0; kv < 2; ++kv, ++e_it) {
+                    if (kP == 2 && kv != pw) continue;   // the other warp's entry
                     const int e = e_it % E;
                     wait(&kv_empty[e], (uint32_t)((e_it / E) & 1) ^ 1u);
-                    // lane 0 arms the entry for this warp's bytes; then each lane
-                    // issues one box (page j = pw + 2 (lane / kHalves), column block
-                    // lane % kHalves).  A tensor copy holds its issuing thread for
-                    // hundreds of cycles, so small pages need many issuing lanes.
+                    // lane 0 arms the entry; then lane j issues box j: both column
+                    // blocks of its tokens in one copy, laid out by 8-token group.
                     // test hook: CTA 0 leaves one entry unfilled, so that the MMA
                     // warps' bounded wait runs out (the abort path, without a fault)
                     const bool skip = P.test_skip_it == e_it && blockIdx.x == 0;
                     const bool go = __shfl_sync(0xffffffffu, *abort_flag, 0) == 0 && !skip;
                     if (lane == 0 && go) {
-                        armed[pw * E + e] = e_it / E;
-                        mbar_arrive_expect_tx(&kv_full[e], bytes);   // this warp's pages
+                        armed[e] = e_it / E;
+                        mbar_arrive_expect_tx(&kv_full[e], bytes);
                     }
                     __syncwarp();
-                    if (go && lane < (8 / kP) * Cfg::kHalves) {
-                        const int j = pw + kP * (lane / Cfg::kHalves), c = lane % Cfg::kHalves;
+                    if (go && lane < 8) {
+                        const int j = lane;
                         int page = -1;
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj)
                             if (jj == j) page = pg[jj];
                         if (page >= 0) {
                             const int slot0 = (kt * kPrefillTile + j * rpb) % ps;
-                            tma_load_4d(smem + Cfg::kOffKV + e * Cfg::kKVBytes + c * Cfg::kRegion +
-                                            j * rpb * 128,
-                                        kv ? &tmv : &tmk, &kv_full[e], (128 / Cfg::kElem) * c,
-                                        slot0, hk, page);
+                            uint8_t* dst = smem + Cfg::kOffKV + e * Cfg::kKVBytes +
+                                           (j * rpb / 8) * Cfg::kGroupStride;
+                            if constexpr (Cfg::kHalves == 2)
+                                tma_load_5d(dst, kv ? &tmv : &tmk, &kv_full[e], 0, 0,
+                                            hk * P.kv_chunk_mul, slot0 / 8,
+                                            page * P.kv_page_mul + hk * P.kv_head_add);
+                            else
+                                tma_load_4d(dst, kv ? &tmv : &tmk, &kv_full[e], 0, slot0, hk,
+                                            page);
                         }
                     }
                     __syncwarp();
@@ -418,8 +434,10 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         // Descriptor bases: the start-address field is the low bits of a
         // descriptor, so a byte offset within the buffer is added as offset >> 4.
         const uint64_t dQ = smem_desc_sw128(smem_u32(smem + Cfg::kOffQ), 16, 1024);
-        const uint64_t dK = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), 16, 1024);
-        const uint64_t dV = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), Cfg::kRegion, 1024);
+        // K (K-major) and V (MN-major) tiles: 8-row groups kGroupStride apart,
+        // the second column block 1 KB after the first
+        const uint64_t dK = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), 16, Cfg::kGroupStride);
+        const uint64_t dV = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), 1024, Cfg::kGroupStride);
         const uint64_t dVh = smem_desc_sw128(smem_u32(smem + Cfg::kOffVh), Cfg::kRegion, 1024);
         int e_it = 0, task_it = 0, vt = 0;
         int p_cnt[2] = {0, 0}, of_cnt[2] = {0, 0};
@@ -432,11 +450,13 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
             // each instruction takes 32 bytes of every row's K dimension
 #pragma unroll
             for (int kk = 0; kk < D * Cfg::kElem / 32; ++kk) {
-                const uint64_t koff = (uint64_t)((((kk >> 2) * Cfg::kRegion) + (kk & 3) * 32) >> 4);
+                // column block kk / 4: kRegion further on in Q, 1 KB in K
+                const uint64_t qoff = (uint64_t)((((kk >> 2) * Cfg::kRegion) + (kk & 3) * 32) >> 4);
+                const uint64_t koff = (uint64_t)((((kk >> 2) * 1024) + (kk & 3) * 32) >> 4);
                 if constexpr (FP8)
-                    tc_mma_ss_f8(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
+                    tc_mma_ss_f8(d, a0 + qoff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
                 else
-                    tc_mma_ss(d, a0 + koff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
+                    tc_mma_ss(d, a0 + qoff, b0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
             }
             tc_commit(&s_full[h]);
         };
@@ -446,8 +466,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                                     : dV + (uint64_t)((e * Cfg::kKVBytes) >> 4);
             const uint32_t d = tmem + h * 256 + 128, a = tmem + h * 256;
 #pragma unroll
+            // 16 keys per instruction: two 8-row groups of V (the f16 copy of an
+            // E4M3 V tile is plain row-major: two 1 KB groups per column block)
+            constexpr int kStep = FP8 ? 2 * 1024 : 2 * Cfg::kGroupStride;
             for (int kk = 0; kk < kPrefillTile / 16; ++kk)
-                tc_mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
+                tc_mma_ts(d, a + kk * 8, b0 + (uint64_t)((kk * kStep) >> 4), idesc_pv,
                           (!first || kk > 0) ? 1u : 0u);
             tc_commit(&o_done[h]);
         };
@@ -506,8 +529,9 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                                  idx += 32) {
                                 const int r = r0 + idx / (Cfg::kHalves * 8);
                                 const int rem = idx % (Cfg::kHalves * 8);
-                                *reinterpret_cast<uint4*>(sVp + (rem >> 3) * Cfg::kRegion +
-                                                          swz128(r, rem & 7)) =
+                                *reinterpret_cast<uint4*>(sVp + (r >> 3) * Cfg::kGroupStride +
+                                                          (rem >> 3) * 1024 +
+                                                          swz128(r & 7, rem & 7)) =
                                     make_uint4(0u, 0u, 0u, 0u);
                             }
                             fence_proxy_async_smem();
@@ -769,20 +793,14 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     // After an abort, wait (bounded) for every copy the producers armed before
-    // the CTA exits.  Nothing arms a barrier after the abort; an entry's phase
-    // needs both producer warps' arrivals, and one of them may have stopped a
-    // phase short (it never runs more than one phase ahead of the other), so
-    // the missing arrival is added before waiting.  The MMA warps already
-    // waited for all their MMAs (the mma_done commit).
+    // the CTA exits.  Nothing arms a barrier after the abort, and each armed
+    // phase is one warp's arrival with its copies' bytes, so waiting for the
+    // last armed phase of every entry waits for every copy in flight.  The MMA
+    // warps already waited for all their MMAs (the mma_done commit).
     if (*abort_flag && threadIdx.x == 0) {
-        for (int e = 0; e < E; ++e) {
-            const int a0 = armed[e], a1 = Cfg::kProducers == 2 ? armed[E + e] : a0;
-            const int ph = a0 > a1 ? a0 : a1;
-            if (ph < 0) continue;
-            if (a0 != a1) mbar_arrive(&kv_full[e]);
-            mbar_wait(&kv_full[e], (uint32_t)(ph & 1), kDrainLimitNs);
-        }
-        if (armed[2 * E] >= 0) mbar_wait(q_full, (uint32_t)(armed[2 * E] & 1), kDrainLimitNs);
+        for (int e = 0; e < E; ++e)
+            if (armed[e] >= 0) mbar_wait(&kv_full[e], (uint32_t)(armed[e] & 1), kDrainLimitNs);
+        if (armed[E] >= 0) mbar_wait(q_full, (uint32_t)(armed[E] & 1), kDrainLimitNs);
     }
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
@@ -841,6 +859,9 @@ cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, cons
     P.max_pages_per_seq = p.max_pages_per_seq;
     P.rows_per_box = p.page_size < 64 ? p.page_size : 64;
     P.boxes_per_tile = kPrefillTile / P.rows_per_box;
+    P.kv_chunk_mul = p.layout == PA_NHD ? 2 : 0;
+    P.kv_page_mul = p.layout == PA_NHD ? 1 : p.num_kv_heads;
+    P.kv_head_add = p.layout == PA_NHD ? 0 : 1;
     P.q_scale = qs;
     P.k_scale = ks;
     P.v_scale = vs;
