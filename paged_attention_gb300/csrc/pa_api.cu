@@ -22,7 +22,7 @@ int decode_threads(const pa_problem& p);
 const void* decode_kernel_ptr(const pa_problem& p);
 cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
                                    const CUtensorMap& tq, const CUtensorMap& tk,
-                                   const CUtensorMap& tv, bool kv_one_box,
+                                   const CUtensorMap& tv,
                                    const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
@@ -188,39 +188,12 @@ bool encode_kv_map(const pa_problem& p, const void* base, CUtensorMap* map) {
     return r == CUDA_SUCCESS;
 }
 
-// bf16 K/V with pages of >= 64 tokens as (d % 64, slot, d / 64, head, page): one
-// box of 64 slots x both 64-element column blocks lands as two 128-byte-swizzled
-// [64 x 128 B] regions, i.e. the whole decode tile in one copy.
-bool encode_kv_map_one_box(const pa_problem& p, const void* base, CUtensorMap* map) {
-    auto fn = encode_fn();
-    if (!fn || p.kv_dtype != PA_BF16 || p.head_dim != 128 || p.page_size < 64) return false;
-    const cuuint64_t D = p.head_dim, ps = p.page_size, H = p.num_kv_heads, NP = p.num_pages;
-    cuuint64_t dims[5] = {64, ps, 2, H, NP};
-    cuuint64_t strides[4];
-    if (p.layout == PA_NHD) {
-        strides[0] = H * D * 2;
-        strides[1] = 128;
-        strides[2] = D * 2;
-        strides[3] = ps * H * D * 2;
-    } else {
-        strides[0] = D * 2;
-        strides[1] = 128;
-        strides[2] = ps * D * 2;
-        strides[3] = H * ps * D * 2;
-    }
-    cuuint32_t box[5] = {64, 64, 2, 1, 1};
-    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// bf16 K/V with head_dim 128 for the prefill kernel, as (d % 64, slot % 8,
-// column block, slot / 8, page) with the head folded into the column-block
-// coordinate (NHD: chunk = 2 head + d / 64) or into the page coordinate (HND:
-// page * H + head).  A box of a page's rows lands as 8-token groups, each the
-// two 128-byte-swizzled [8 x 128 B] column blocks: one copy per page.
+// bf16 K/V with head_dim 128, as (d % 64, slot % 8, column block, slot / 8,
+// page) with the head folded into the column-block coordinate (NHD: chunk =
+// 2 head + d / 64) or into the page coordinate (HND: page * H + head).  A box
+// of up to 64 of a page's rows lands as 8-token groups, each the two
+// 128-byte-swizzled [8 x 128 B] column blocks: one copy per page (or per 64
+// tokens of a larger page), for the decode and the prefill kernels alike.
 bool encode_kv_map_grouped(const pa_problem& p, const void* base, CUtensorMap* map) {
     auto fn = encode_fn();
     if (!fn || p.kv_dtype != PA_BF16 || p.head_dim != 128) return false;
@@ -241,6 +214,15 @@ bool encode_kv_map_grouped(const pa_problem& p, const void* base, CUtensorMap* m
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// The K and V maps of a call: by 8-token group for bf16 with head_dim 128,
+// else (d, slot, head, page) boxes of up to 64 slots.
+bool encode_kv_maps(const pa_problem& p, const void* k, const void* v, CUtensorMap* tk,
+                    CUtensorMap* tv) {
+    if (p.kv_dtype == PA_BF16 && p.head_dim == 128)
+        return encode_kv_map_grouped(p, k, tk) && encode_kv_map_grouped(p, v, tv);
+    return encode_kv_map(p, k, tk) && encode_kv_map(p, v, tv);
 }
 
 // Q viewed as (d, head, token): box = 128 bytes of d (64 bf16 or 128 E4M3
@@ -534,30 +516,21 @@ pa_status prefill_body(const pa_problem* problem, const void* q, const float* q_
     if (assign_ws_bytes < (size_t)M.total_bytes) return PA_ERR_WORKSPACE;
     if (partial_ws_bytes < (size_t)M.partial_bytes || !partial_ws || !aligned(partial_ws, 16))
         return PA_ERR_WORKSPACE;
-    // K/V maps: by 8-token group for bf16 with head_dim 128, else (d, slot,
-    // head, page) boxes of up to 64 slots
-    const bool grouped = p.kv_dtype == PA_BF16 && p.head_dim == 128;
     CUtensorMap tq, tk, tv;
     if (!encode_q_map(p, q, kPrefillHalfRows / (p.num_q_heads / p.num_kv_heads), &tq) ||
-        !(grouped ? encode_kv_map_grouped(p, k_cache, &tk) : encode_kv_map(p, k_cache, &tk)) ||
-        !(grouped ? encode_kv_map_grouped(p, v_cache, &tv) : encode_kv_map(p, v_cache, &tv)))
+        !encode_kv_maps(p, k_cache, v_cache, &tk, &tv))
         return PA_ERR_INVALID_ARG;
     const cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
     if (M.split) {
-        // the decode-shaped sequences first, on the decode kernel, with its
-        // own K/V maps
-        CUtensorMap tqd, tkd, tvd;
+        // the decode-shaped sequences first, on the decode kernel (same K/V
+        // maps)
+        CUtensorMap tqd;
         if (!encode_q_map(M.pd, q, M.pd.max_q_len > 0 ? M.pd.max_q_len : 1, &tqd))
             return PA_ERR_INVALID_ARG;
-        const bool one_box = encode_kv_map_one_box(M.pd, k_cache, &tkd) &&
-                             encode_kv_map_one_box(M.pd, v_cache, &tvd);
-        if (!one_box &&
-            (!encode_kv_map(M.pd, k_cache, &tkd) || !encode_kv_map(M.pd, v_cache, &tvd)))
-            return PA_ERR_INVALID_ARG;
         // (the wait-timeout test hook is left for the prefill kernel)
-        e = launch_decode_from_api(M.pd, M.Ld, tqd, tkd, tvd,
-                                   one_box, block_table, context_lens, q_lens, k_scale, v_scale,
+        e = launch_decode_from_api(M.pd, M.Ld, tqd, tk, tv,
+                                   block_table, context_lens, q_lens, k_scale, v_scale,
                                    const_cast<void*>(assign_ws),
                                    static_cast<char*>(partial_ws) + M.part_off, out, lse, s,
                                    false);
@@ -667,10 +640,8 @@ pa_status pa_decode_splitk(const pa_problem* problem, const void* q, const void*
         return PA_ERR_WORKSPACE;
     CUtensorMap tq, tk, tv;
     if (!encode_q_map(p, q, p.max_q_len > 0 ? p.max_q_len : 1, &tq)) return PA_ERR_INVALID_ARG;
-    bool one_box = encode_kv_map_one_box(p, k_cache, &tk) && encode_kv_map_one_box(p, v_cache, &tv);
-    if (!one_box && (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv)))
-        return PA_ERR_INVALID_ARG;
-    cudaError_t e = launch_decode_from_api(p, L, tq, tk, tv, one_box,
+    if (!encode_kv_maps(p, k_cache, v_cache, &tk, &tv)) return PA_ERR_INVALID_ARG;
+    cudaError_t e = launch_decode_from_api(p, L, tq, tk, tv,
                                            block_table,
                                            context_lens, q_lens, k_scale, v_scale,
                                            const_cast<void*>(assign_ws), partial_ws, out, lse,
@@ -734,9 +705,7 @@ pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void
     if (part_off + L.partial_bytes > (int64_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
     CUtensorMap tq, tk, tv;
     if (!encode_q_map(p, q, p.max_q_len > 0 ? p.max_q_len : 1, &tq)) return PA_ERR_INVALID_ARG;
-    bool one_box = encode_kv_map_one_box(p, k_cache, &tk) && encode_kv_map_one_box(p, v_cache, &tv);
-    if (!one_box && (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv)))
-        return PA_ERR_INVALID_ARG;
+    if (!encode_kv_maps(p, k_cache, v_cache, &tk, &tv)) return PA_ERR_INVALID_ARG;
     char* scratch = nullptr;
     st = noalloc_scratch(&scratch);
     if (st != PA_OK) return st;
@@ -747,7 +716,7 @@ pa_status pa_decode_noalloc(const pa_problem* problem, const void* q, const void
     // every word read below
     cudaError_t e = launch_assign(L, context_lens, q_lens, nullptr, ws, s);
     if (e == cudaSuccess)
-        e = launch_decode_from_api(p, L, tq, tk, tv, one_box, block_table,
+        e = launch_decode_from_api(p, L, tq, tk, tv, block_table,
                                    context_lens, q_lens, k_scale, v_scale, ws, partial, out, lse,
                                    s);
     // (the bf16 decode kernel finalizes split units itself; E4M3 needs Combine)
@@ -799,10 +768,8 @@ pa_status pa_decode_static(const pa_problem* problem, int32_t num_splits, const 
     if (p.kv_dtype == PA_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
     CUtensorMap tq, tk, tv;
     if (!encode_q_map(p, q, p.max_q_len > 0 ? p.max_q_len : 1, &tq)) return PA_ERR_INVALID_ARG;
-    bool one_box = encode_kv_map_one_box(p, k_cache, &tk) && encode_kv_map_one_box(p, v_cache, &tv);
-    if (!one_box && (!encode_kv_map(p, k_cache, &tk) || !encode_kv_map(p, v_cache, &tv)))
-        return PA_ERR_INVALID_ARG;
-    cudaError_t e = launch_decode_from_api(p, L, tq, tk, tv, one_box, block_table, context_lens,
+    if (!encode_kv_maps(p, k_cache, v_cache, &tk, &tv)) return PA_ERR_INVALID_ARG;
+    cudaError_t e = launch_decode_from_api(p, L, tq, tk, tv, block_table, context_lens,
                                            q_lens, k_scale, v_scale, ws,
                                            static_cast<char*>(ws) + L.total_bytes, out, lse, s,
                                            true, S, cluster);

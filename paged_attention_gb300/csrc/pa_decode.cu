@@ -52,6 +52,9 @@ struct DecodeCfg {
     static constexpr int kHalves = D * kElem / 128;          // 128-B column blocks of a K/V row
     static constexpr int kHalfBytes = kDecodeTile * 128;      // one column block of a tile
     static constexpr int kKBytes = kHalves * kHalfBytes;
+    // K/V tiles by 8-token group: group g holds its kHalves column blocks of
+    // 8 rows x 128 bytes at g * kGroupStride (one block: plain row-major)
+    static constexpr int kGroupStride = kHalves * 1024;
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kQRows = 16 * RT;
     static constexpr int kQHalves = D / 64;                   // Q is bf16
@@ -89,6 +92,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, RT, NG, STAGES>::kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap tmq,
               const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     using Cfg = DecodeCfg<D, RT, NG, STAGES, STATIC>;
+    // byte offset in a K/V tile of row `row`, 16-byte chunk c of its 8 * kHalves
+    auto kv_off = [](int row, int c) -> uint32_t {
+        return (uint32_t)((row >> 3) * Cfg::kGroupStride + (c >> 3) * 1024) + swz(row & 7, c & 7);
+    };
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -229,15 +236,14 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
                         const int tr = idx / (Cfg::kHalves * 8);
                         const int rem = idx % (Cfg::kHalves * 8);
                         if (tok_s0 + tr >= ctx_b)
-                            *reinterpret_cast<uint4*>(stV + (rem >> 3) * Cfg::kHalfBytes +
-                                                      swz(16 * ts + tr, rem & 7)) =
+                            *reinterpret_cast<uint4*>(stV + kv_off(16 * ts + tr, rem)) =
                                 make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
                 const uint32_t kbase = smem_u32(stK), vbase = smem_u32(stV);
-                const int rowbase = 16 * ts, halfstride = Cfg::kHalfBytes;
+                const int rowbase = 16 * ts;
 
                 // S = Q K^T : 16 rows x 16 tokens, even / odd k-steps in two chains
                 float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -248,7 +254,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const int dch = 2 * kk + (mi & 1);
-                        const uint32_t addr = kbase + (dch >> 3) * halfstride + swz(trow, dch & 7);
+                        const uint32_t addr = kbase + kv_off(trow, dch);
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4(addr, b0, b1, b2, b3);
                         if (kk & 1) {
@@ -332,7 +338,7 @@ decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CU
 #pragma unroll
                     for (int jd = 0; jd < D / 8; jd += 2) {
                         const int dch = jd + (mi >> 1);
-                        const uint32_t addr = vbase + (dch >> 3) * halfstride + swz(trow, dch & 7);
+                        const uint32_t addr = vbase + kv_off(trow, dch);
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4_t(addr, b0, b1, b2, b3);
                         mma_bf16_16816(o[jd], pa, b0, b1);
@@ -612,7 +618,7 @@ int decode_cluster_grid(const pa_problem& p, int C) {
 
 cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
                                    const CUtensorMap& tq, const CUtensorMap& tk,
-                                   const CUtensorMap& tv, bool kv_one_box,
+                                   const CUtensorMap& tv,
                                    const int32_t* block_table,
                                    const int32_t* ctx, const int32_t* ql, const float* ks,
                                    const float* vs, void* ws, void* partial, void* out, float* lse,
@@ -636,7 +642,9 @@ cudaError_t launch_decode_from_api(const pa_problem& p, const WsLayout& L,
     P.rows_per_box = p.page_size < kDecodeTile ? p.page_size : kDecodeTile;
     P.boxes_per_tile = kDecodeTile / P.rows_per_box;
     P.q_box_tokens = p.max_q_len > 0 ? p.max_q_len : 1;
-    P.kv_one_box = kv_one_box ? 1 : 0;
+    P.kv_chunk_mul = p.layout == PA_NHD ? 2 : 0;
+    P.kv_page_mul = p.layout == PA_NHD ? 1 : p.num_kv_heads;
+    P.kv_head_add = p.layout == PA_NHD ? 0 : 1;
     P.sm_scale = p.sm_scale;
     P.static_splits = static_splits;
     P.cluster_size = cluster_size;

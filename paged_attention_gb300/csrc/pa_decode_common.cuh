@@ -30,7 +30,12 @@ struct DecodeParams {
     int32_t rows_per_box;     // min(page_size, 64)
     int32_t boxes_per_tile;   // 64 / rows_per_box
     int32_t q_box_tokens;     // tokens per Q TMA box (max q_len)
-    int32_t kv_one_box;       // 1: one 5-D TMA box fills both column blocks of a tile
+    // bf16 K/V with head_dim 128 come in boxes of a page's rows by 8-token
+    // group (see pa_api's grouped K/V map): chunk coordinate kv_chunk_mul *
+    // head, last coordinate page * kv_page_mul + head * kv_head_add
+    int32_t kv_chunk_mul;
+    int32_t kv_page_mul;
+    int32_t kv_head_add;
     int32_t test_skip_it;     // test hook: CTA 0 leaves this KV tile's stage unfilled (-1 none)
     int32_t static_splits;    // 0: tasks from the Assign map; S > 0: static split-K, S splits
     int32_t cluster_size;     // static split-K on clusters of S CTAs (DSM merge); else 1
@@ -328,12 +333,23 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
             // one box per lane: a tensor copy holds its issuing thread for
             // hundreds of cycles, the SM takes a new one every ~90
             if (go) {
-                if (Cfg::kHalves == 2 && P.kv_one_box) {
-                    // pages of >= 64 tokens: one box = both column blocks (lane 0 K, lane 1 V)
-                    const int slot0 = (kt * kDecodeTile) % ps;
-                    if (lane < 2 && pg[0] >= 0)
-                        tma_load_5d(lane ? stV : stK, lane ? tmv : tmk, &full[s], 0, slot0, 0, hk,
-                                    pg[0]);
+                if constexpr (Cfg::kHalves == 2) {
+                    // two column blocks: lane = (kv, box j), one copy per page
+                    // (or per 64 tokens of a larger page) holding both blocks,
+                    // laid out by 8-token group
+                    if (lane < 2 * nbox) {
+                        const int kv = lane / nbox, j = lane - kv * nbox;
+                        int page = -1;
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            if (jj == j) page = pg[jj];
+                        if (page >= 0) {
+                            const int slot0 = (kt * kDecodeTile + j * rpb) % ps;
+                            tma_load_5d((kv ? stV : stK) + (j * rpb / 8) * Cfg::kGroupStride,
+                                        kv ? tmv : tmk, &full[s], 0, 0, hk * P.kv_chunk_mul,
+                                        slot0 / 8, page * P.kv_page_mul + hk * P.kv_head_add);
+                        }
+                    }
                 } else if (lane < 8 * TPS * Cfg::kHalves) {
                     // lane = (kv, tile m, box j, column block h)
                     const int kv = lane / (4 * TPS * Cfg::kHalves);
