@@ -440,7 +440,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
         const uint64_t dV = smem_desc_sw128(smem_u32(smem + Cfg::kOffKV), 1024, Cfg::kGroupStride);
         const uint64_t dVh = smem_desc_sw128(smem_u32(smem + Cfg::kOffVh), Cfg::kRegion, 1024);
         int e_it = 0, task_it = 0, vt = 0;
-        int p_cnt[2] = {0, 0}, of_cnt[2] = {0, 0};
+        int p_cnt = 0, of_cnt = 0;   // phases of this warp's half
         TaskRec mine;
 
         auto issue_qk = [&](int h, int e) {   // S_h = Q_h K^T from ring entry e
@@ -541,11 +541,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 }
                 if (j + 1 < n) wait(&kv_full[eKn % E], (uint32_t)((eKn / E) & 1));
                 if (mine_half) {
-                    wait(&p_full[h], (uint32_t)(p_cnt[h] & 1));
-                    ++p_cnt[h];
+                    wait(&p_full[h], (uint32_t)(p_cnt & 1));
+                    ++p_cnt;
                     if (j == 0) {
-                        wait(&o_free[h], (uint32_t)(of_cnt[h] & 1) ^ 1u);
-                        ++of_cnt[h];
+                        wait(&o_free[h], (uint32_t)(of_cnt & 1) ^ 1u);
+                        ++of_cnt;
                     }
                 }
                 token_wait();
@@ -635,7 +635,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 // pass 1: row max of the raw scores (sm_scale >= 0 keeps the order),
                 // 32 columns at a time; the two softmax warps on each SM
                 // sub-partition hide each other's TMEM latency
-                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // (four scalar chains, no array: nothing of the loop in local memory)
+                float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {
                     float s[32];
@@ -643,23 +644,20 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     tmem_wait_ld();
                     reg_fence32(s);
                     const int lim = limc - c4 * 32, low = lowc - c4 * 32;
-                    if (lim >= 31 && (!WINDOW || low <= 0)) {
-#pragma unroll
-                        for (int c = 0; c < 32; c += 8) {   // three-input max: 2 scores a step
-                            mx4[0] = fmax3(mx4[0], s[c], s[c + 1]);
-                            mx4[1] = fmax3(mx4[1], s[c + 2], s[c + 3]);
-                            mx4[2] = fmax3(mx4[2], s[c + 4], s[c + 5]);
-                            mx4[3] = fmax3(mx4[3], s[c + 6], s[c + 7]);
-                        }
-                    } else {
+                    if (!(lim >= 31 && (!WINDOW || low <= 0))) {
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            mx4[c & 3] = fmaxf(mx4[c & 3], (c <= lim && (!WINDOW || c >= low))
-                                                               ? s[c] : -INFINITY);
+                            if (!(c <= lim && (!WINDOW || c >= low))) s[c] = -INFINITY;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {   // three-input max: 2 scores a step
+                        mxa = fmax3(mxa, s[c], s[c + 1]);
+                        mxb = fmax3(mxb, s[c + 2], s[c + 3]);
+                        mxc = fmax3(mxc, s[c + 4], s[c + 5]);
+                        mxd = fmax3(mxd, s[c + 6], s[c + 7]);
                     }
                 }
-                const float mx =
-                    fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+                const float mx = fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * sl2;
                 // lazy max: move m (and rescale O, l) only when it grows by > 2^8
                 float alpha = 1.f;
                 bool resc = false;
@@ -672,11 +670,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 }
                 const float mu = m == -INFINITY ? 0.f : m;
                 // pass 2: P = exp2(s * scale - m) in bf16, two exponentials per MUFU
-                // operation on full chunks (f16 holds x <= 8 to 2^-9 relative, below
-                // P's own bf16 rounding); keys [32c, 32c+32) go to S columns
-                // [16c, 16c+16), which every later chunk has already read
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-                float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                // operation (x <= 8 since m trails the row max by at most 8, and f16
+                // holds such x to 2^-9 relative, below P's own bf16 rounding); keys
+                // [32c, 32c+32) go to S columns [16c, 16c+16), which every later
+                // chunk has already read
+                float2 suma = make_float2(0.f, 0.f), sumb = make_float2(0.f, 0.f);
                 const float2 sl2x2 = make_float2(sl2, sl2), nmu2 = make_float2(-mu, -mu);
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {
@@ -685,33 +683,30 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     tmem_wait_ld();
                     reg_fence32(s);
                     const int lim = limc - c4 * 32, low = lowc - c4 * 32;
+                    // keys outside [low, lim] (a diagonal, context-end or window
+                    // chunk) become -inf, whose exponential is 0: every chunk then
+                    // takes the same path
+                    if (!(lim >= 31 && (!WINDOW || low <= 0))) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (!(c <= lim && (!WINDOW || c >= low))) s[c] = -INFINITY;
+                    }
                     uint32_t pk[16];
-                    if (lim >= 31 && (!WINDOW || low <= 0)) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 2) {
-                            // packed f32x2: the scaled scores and the row sums
-                            const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2x2, nmu2);
-                            const uint32_t e2 = ex2_h2(a.x, a.y);
-                            if constexpr (FP8) {
-                                // f16 P as computed; the pair straight into the f32 sums
-                                add_f16x2_to_f32(sum2[(c >> 1) & 1], e2);
-                                pk[c >> 1] = e2;
-                            } else {
-                                const float2 pf =
-                                    __half22float2(*reinterpret_cast<const __half2*>(&e2));
-                                sum2[(c >> 1) & 1] = __fadd2_rn(sum2[(c >> 1) & 1], pf);
-                                pk[c >> 1] = pack_bf16x2(pf.x, pf.y);
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 32; c += 2) {
-                            const float e0 = (c <= lim && (!WINDOW || c >= low))
-                                                 ? ex2(fmaf(s[c], sl2, -mu)) : 0.f;
-                            const float e1 = (c + 1 <= lim && (!WINDOW || c + 1 >= low))
-                                                 ? ex2(fmaf(s[c + 1], sl2, -mu)) : 0.f;
-                            sum4[(c >> 1) & 3] += e0 + e1;
-                            pk[c >> 1] = FP8 ? pack_f16x2_sat(e0, e1) : pack_bf16x2(e0, e1);
+                    for (int c = 0; c < 32; c += 2) {
+                        // packed f32x2: the scaled scores and the row sums
+                        const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), sl2x2, nmu2);
+                        const uint32_t e2 = ex2_h2(a.x, a.y);
+                        float2& acc = ((c >> 1) & 1) ? sumb : suma;
+                        if constexpr (FP8) {
+                            // f16 P as computed; the pair straight into the f32 sums
+                            add_f16x2_to_f32(acc, e2);
+                            pk[c >> 1] = e2;
+                        } else {
+                            const float2 pf =
+                                __half22float2(*reinterpret_cast<const __half2*>(&e2));
+                            acc = __fadd2_rn(acc, pf);
+                            pk[c >> 1] = pack_bf16x2(pf.x, pf.y);
                         }
                     }
                     tmem_st16(tS + c4 * 16, pk);
@@ -734,8 +729,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         tmem_st32(tO + c4 * 32, o);
                     }
                 }
-                l = l * alpha + (((sum4[0] + sum4[1]) + (sum4[2] + sum4[3])) +
-                                 ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y)));
+                l = l * alpha + ((suma.x + suma.y) + (sumb.x + sumb.y));
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&p_full[h]);
