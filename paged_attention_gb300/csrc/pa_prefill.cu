@@ -207,6 +207,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (mbar_try_wait(bar, parity)) return;   // the usual case, checked first
         if (*abort_flag) return;
         if (!mbar_wait_or_abort(bar, parity, lim, abort_flag)) {
             *abort_flag = 1;
@@ -622,16 +623,17 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 ++s_cnt;
                 tc_fence_after();
                 if (!warp_live) {
-                    if (j > 0) {
-                        wait(&o_done[h], (uint32_t)(o_cnt & 1));
-                        ++o_cnt;
-                    }
+                    if (j > 0) ++o_cnt;   // PV of the previous tile: nothing to wait for
                     tc_fence_before();
                     mbar_arrive(&p_full[h]);
                     continue;
                 }
                 const int limc = row_ok ? key_last - kt * kPrefillTile : -1;   // valid: c <= limc
                 const int lowc = key_first - kt * kPrefillTile;                // and c >= lowc
+                // every key of the tile visible to every row of the warp: no mask
+                // work in either pass (a warp-uniform test, once a tile)
+                const bool tile_full = __all_sync(
+                    0xffffffffu, limc >= kPrefillTile - 1 && (!WINDOW || lowc <= 0));
                 // pass 1: row max of the raw scores (sm_scale >= 0 keeps the order),
                 // 32 columns at a time; the two softmax warps on each SM
                 // sub-partition hide each other's TMEM latency
@@ -643,8 +645,8 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     tmem_ld32(tS + c4 * 32, s);
                     tmem_wait_ld();
                     reg_fence32(s);
-                    const int lim = limc - c4 * 32, low = lowc - c4 * 32;
-                    if (!(lim >= 31 && (!WINDOW || low <= 0))) {
+                    if (!tile_full) {
+                        const int lim = limc - c4 * 32, low = lowc - c4 * 32;
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
                             if (!(c <= lim && (!WINDOW || c >= low))) s[c] = -INFINITY;
@@ -682,11 +684,11 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     tmem_ld32(tS + c4 * 32, s);
                     tmem_wait_ld();
                     reg_fence32(s);
-                    const int lim = limc - c4 * 32, low = lowc - c4 * 32;
-                    // keys outside [low, lim] (a diagonal, context-end or window
-                    // chunk) become -inf, whose exponential is 0: every chunk then
+                    // keys outside [lowc, limc] (a diagonal, context-end or window
+                    // tile) become -inf, whose exponential is 0: every chunk then
                     // takes the same path
-                    if (!(lim >= 31 && (!WINDOW || low <= 0))) {
+                    if (!tile_full) {
+                        const int lim = limc - c4 * 32, low = lowc - c4 * 32;
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
                             if (!(c <= lim && (!WINDOW || c >= low))) s[c] = -INFINITY;
@@ -711,12 +713,12 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                     }
                     tmem_st16(tS + c4 * 16, pk);
                 }
-                if (j > 0) {
-                    wait(&o_done[h], (uint32_t)(o_cnt & 1));   // PV of the previous tile
-                    ++o_cnt;
-                }
-                tc_fence_after();
+                // O is rescaled only after the previous tile's PV has written it;
+                // without a rescale nothing here touches O (PV of this tile is
+                // issued after the arrival below, behind the previous one)
                 if (__any_sync(0xffffffffu, resc)) {
+                    if (j > 0) wait(&o_done[h], (uint32_t)(o_cnt & 1));
+                    tc_fence_after();
                     const float f = resc ? alpha : 1.f;
 #pragma unroll 1
                     for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -729,6 +731,7 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                         tmem_st32(tO + c4 * 32, o);
                     }
                 }
+                if (j > 0) ++o_cnt;   // that PV's phase, waited for or not
                 l = l * alpha + ((suma.x + suma.y) + (sumb.x + sumb.y));
                 tmem_wait_st();
                 tc_fence_before();
