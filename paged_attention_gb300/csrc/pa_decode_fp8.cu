@@ -188,6 +188,7 @@ decode_fp8_kernel(const __grid_constant__ DecodeParams P, const __grid_constant_
     if (use_cluster) cluster_sync_all();   // every peer's barriers initialised
 
     auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (mbar_try_wait(bar, parity)) return;   // the usual case, checked first
         if (*abort_flag) return;
         if (!mbar_wait_or_abort(bar, parity, lim, abort_flag)) {
             *abort_flag = 1;
