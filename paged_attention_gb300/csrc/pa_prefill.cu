@@ -21,9 +21,9 @@
 // launched with, setmaxnreg leaves warpgroup 0 with 88 and gives the two
 // softmax warpgroups 200 each: 128*88 + 256*200 <= 384*168.
 //   warp 0      TMA producer: the unit's Q halves once per task, then for
-//               every active 128-token KV tile its K and its V, page by page,
-//               each into its own entry of a ring (128-byte swizzle); warp 0
-//               copies the even pages of an entry, warp 3 the odd ones.
+//               every active 128-token KV tile its K, one copy per page,
+//               into its own entry of a ring (128-byte swizzle, rows stored
+//               by 8-token group); warp 3 fills the V entries the same way.
 //   warps 1-2   warp 1 allocates the 512 TMEM columns; lane 0 of warp 1+h
 //               issues every MMA of half h:
 //               S_h = Q_h K^T (M=128, N=128, K=D, both operands K-major in
@@ -36,12 +36,13 @@
 //               softmax runs; MMAs of one thread execute in issue order,
 //               which keeps QK_h(j+1) from overwriting P_h(j) before PV_h(j)
 //               has read it.  Warp 1 also zeroes V rows past the context.
-//   warp 3      copies the odd pages of every K/V ring entry (see warp 0);
-//               with E4M3 K/V it converts V tiles to f16 instead, and warp 0
-//               copies every page.
+//   warp 3      fills the V entries of the ring (see warp 0); with E4M3 K/V
+//               it converts V tiles to f16 instead, and warp 0 fills every
+//               entry.
 //   warps 4-7   softmax for half 0, warps 8-11 for half 1: thread = query row
 //               = TMEM lane.  Reads its S row (tcgen05.ld), applies the
-//               causal / context mask, keeps the running max lazily (O is
+//               causal / context / window mask on the tiles that need it
+//               (a warp-uniform test per tile), keeps the running max lazily (O is
 //               rescaled in TMEM only when the max grows by more than 2^8),
 //               writes P (bf16) back into TMEM, and at the end of the task
 //               normalises O and writes the output row (or split partial)
