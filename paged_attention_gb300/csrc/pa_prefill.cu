@@ -74,6 +74,7 @@ struct PrefillParams {
     int32_t kv_page_mul;
     int32_t kv_head_add;
     int32_t test_skip_it;    // test hook: CTA 0 leaves this K/V ring entry unfilled (-1 none)
+    int32_t store_v8;        // bit 0: out, bit 1: the partials are 32-byte aligned
     // E4M3 Q/K/V: Q scale (one, or one per (token, q head)), one K and one V scale
     const float* q_scale;
     const float* k_scale;
@@ -754,23 +755,46 @@ prefill_kernel(const __grid_constant__ PrefillParams P, const __grid_constant__ 
                 tmem_ld32(tO + c4 * 32, o);
                 tmem_wait_ld();
                 reg_fence32(o);
+                // 32-byte stores where the buffer allows (the rows' scattered
+                // stores are the epilogue's cost: half as many instructions)
                 if (row_ok) {
                     if (rec.tk.w < 0) {
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            P.out + ((int64_t)token * Hq + head) * D + c4 * 32);
+                        __nv_bfloat16* dst = P.out + ((int64_t)token * Hq + head) * D + c4 * 32;
+                        if (P.store_v8 & 1) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
-                                                pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                                                pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                                                pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                            for (int q = 0; q < 2; ++q) {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    w[e] = pack_bf16x2(o[16 * q + 2 * e] * inv, o[16 * q + 2 * e + 1] * inv);
+                                st_global_v8(dst + 16 * q, w);
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                reinterpret_cast<uint4*>(dst)[q] = make_uint4(
+                                    pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                    pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                    pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                    pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                        }
                     } else {
-                        float4* dst = reinterpret_cast<float4*>(
-                            P.part_o + ((int64_t)rec.tk.w * L.rows_cap + r) * D + c4 * 32);
+                        float* dst = P.part_o + ((int64_t)rec.tk.w * L.rows_cap + r) * D + c4 * 32;
+                        if (P.store_v8 & 2) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv,
-                                                 o[4 * q + 2] * inv, o[4 * q + 3] * inv);
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(o[8 * q + e] * inv);
+                                st_global_v8(dst + 8 * q, w);
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                reinterpret_cast<float4*>(dst)[q] =
+                                    make_float4(o[4 * q] * inv, o[4 * q + 1] * inv,
+                                                o[4 * q + 2] * inv, o[4 * q + 3] * inv);
+                        }
                     }
                 }
             }
@@ -860,6 +884,10 @@ cudaError_t launch_prefill_from_api(const pa_problem& p, const WsLayout& L, cons
     P.kv_chunk_mul = p.layout == PA_NHD ? 2 : 0;
     P.kv_page_mul = p.layout == PA_NHD ? 1 : p.num_kv_heads;
     P.kv_head_add = p.layout == PA_NHD ? 0 : 1;
+    // a row's 32-element chunk starts 64 (bf16) or 128 (fp32) bytes apart
+    // from the buffer's start, so 32-byte stores need only a 32-byte base
+    P.store_v8 = ((reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0) |
+                 ((reinterpret_cast<uintptr_t>(partial) & 31u) == 0 ? 2 : 0);
     P.q_scale = qs;
     P.k_scale = ks;
     P.v_scale = vs;

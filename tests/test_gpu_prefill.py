@@ -195,6 +195,26 @@ def test_masked_tiles_never_loaded():
     assert torch.equal(o1, b2.out)
 
 
+@pytest.mark.parametrize("num_ctas", [0, 300])
+def test_prefill_outputs_only_16_byte_aligned(num_ctas):
+    """The epilogue stores 32 bytes at a time where out and the partials are
+    32-byte aligned, 16 bytes otherwise: both give the same bits (300 CTAs
+    split every unit, so the partials' stores are covered too)."""
+    w = W.hybrid_bf16(shrink=16).to("cuda")
+    a = B.make_buffers(w, B.PA_MODE_PREFILL, num_ctas=num_ctas)
+    B.run_prefill(w, a)
+    b = B.make_buffers(w, B.PA_MODE_PREFILL, num_ctas=num_ctas)
+    big_o = torch.empty(b.out.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    b.out = big_o[8:].view(b.out.shape)                  # 16 bytes past a 32-byte boundary
+    big_p = torch.empty(b.partial_ws.numel() + 48, dtype=torch.uint8, device="cuda")
+    b.partial_ws = big_p[16:16 + b.partial_ws.numel()]
+    assert b.out.data_ptr() % 32 == 16 and b.partial_ws.data_ptr() % 32 == 16
+    B.run_prefill(w, b)
+    torch.cuda.synchronize()
+    assert B.pa_last_device_error(a.assign_ws) == 0 and B.pa_last_device_error(b.assign_ws) == 0
+    assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
+
+
 def test_prefill_deterministic():
     w = W.hybrid_bf16(shrink=8).to("cuda")
     a = B.run_prefill(w)
