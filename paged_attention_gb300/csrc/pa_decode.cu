@@ -14,9 +14,10 @@
 //                     it % P: per task the unit's Q rows (G heads x q_len
 //                     tokens) into one of two Q slots; per 64-token KV tile
 //                     the page ids (32 at a time, one coalesced warp load) and
-//                     one TMA box per page (5-D: both column blocks at once
-//                     for pages >= 64) of K and of V into a multi-stage ring
-//                     (128-byte swizzle).
+//                     one TMA box per page of K and of V (a 64-token tile of a
+//                     larger page is one box) into a multi-stage ring
+//                     (128-byte swizzle); with two column blocks (bf16,
+//                     D = 128) a box carries both, stored by 8-token group.
 //   warps P..         consumers, NG groups x RT row tiles x 4 token slices.
 //                     Group g takes the CTA's tiles with index % NG == g, so
 //                     NG tiles are in flight at once.  Warp (g, rt, ts) owns

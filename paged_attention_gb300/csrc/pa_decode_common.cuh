@@ -351,7 +351,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& P, const CUte
                         }
                     }
                 } else if (lane < 8 * TPS * Cfg::kHalves) {
-                    // lane = (kv, tile m, box j, column block h)
+                    // one column block: lane = (kv, tile m, box j)
                     const int kv = lane / (4 * TPS * Cfg::kHalves);
                     const int jm = (lane / Cfg::kHalves) % (4 * TPS), h = lane % Cfg::kHalves;
                     const int m = jm / 4, j = jm % 4;
