@@ -86,3 +86,26 @@ def test_bench_windowed_visible_keys():
     got = [bench.visible_keys_per_row(w, b, range(int(w.q_lens[b]))).tolist()
            for b in range(w.num_seqs)]
     assert got == [[50, 50, 50], [37], [50, 50]]
+
+
+def test_traffic_is_reported_only_for_the_kernel_it_was_taken_on(tmp_path, monkeypatch):
+    """bench.py's roofline.traffic comes from profiles/traffic.json only while
+    the entry's fingerprint matches the kernel sources (else null), and an
+    entry without a q_len serves the workload's own q_len only."""
+    import json
+    import bench
+    fp = build_mod.kernel_fingerprint("pa_prefill")
+    fd = build_mod.kernel_fingerprint("pa_decode_splitk")
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({
+        "pa_prefill:prefill_dense": {"source_hash": fp, "dram_bytes_per_launch": 123},
+        "pa_prefill:prefill_sparse": {"source_hash": "0" * 16, "dram_bytes_per_launch": 456},
+        "pa_decode_splitk:decode_fp8": {"source_hash": fd, "mtp": 2,
+                                        "dram_bytes_per_launch": 789},
+    }))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("pa_prefill", "prefill_dense") == 123
+    assert bench.load_traffic("pa_prefill", "prefill_sparse") is None      # stale
+    assert bench.load_traffic("pa_prefill", "hybrid") is None              # absent
+    assert bench.load_traffic("pa_decode_splitk", "decode_fp8", 2) == 789
+    assert bench.load_traffic("pa_decode_splitk", "decode_fp8", 3) is None  # other q_len
