@@ -43,7 +43,9 @@
  *     workspace, skips the offending access and finishes; the outputs of that
  *     call are then unspecified.  Read the code with pa_last_device_error.
  *   - Tensors are dense and row-major with the shapes given; every base
- *     pointer must be 16-byte aligned.
+ *     pointer must be 16-byte aligned.  The prefill epilogue stores 32 bytes
+ *     at a time into out and the partial workspace when they are 32-byte
+ *     aligned (16 otherwise; same results, a little slower).
  *   - With total_q_tokens == 0 there is no query row: pa_decode_splitk,
  *     pa_decode_noalloc, pa_prefill and pa_combine return PA_OK without
  *     launching anything, and their buffers may be NULL (pa_assign still
