@@ -479,6 +479,20 @@ class Case:
                           "pa_prefill")
         roof["kernel_ms"] = round(kern_ms, 4)
         roof["algorithmic_" + self.kind + "_per_launch"] = int(self.work)
+        if self.name == "hybrid":
+            # the batch's two parts run one after the other, each on its own
+            # roofline: the decode part's bytes at HBM rate, the chunk's FLOPs
+            # at the bf16 rate
+            from paged_attention_gb300 import workloads as W
+            dec_bytes, pre_flops = W.mixed_batch_parts(self.w_cpu)
+            bound_ms = (dec_bytes / (peaks["hbm_gbs"] * 1e9) +
+                        pre_flops / (peaks["bf16_tflops"] * 1e12)) * 1e3
+            roof["parts"] = {"decode_part_bytes": int(dec_bytes),
+                             "prefill_part_flops": int(pre_flops),
+                             "bound_ms": round(bound_ms, 4),
+                             "frac": round(bound_ms / kern_ms, 4),
+                             "how": "bytes at the measured HBM rate plus FLOPs at the "
+                                    "measured bf16 peak, against the kernel pair's time"}
         roof["traffic"] = load_traffic(roof["kernel"], self.name,
                                        self.w_cpu.meta.get("mtp"))
         return roof

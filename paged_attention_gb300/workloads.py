@@ -430,3 +430,30 @@ def visible_pairs(w: Workload) -> int:
 def prefill_algorithmic_flops(w: Workload) -> int:
     """4 * D * Hq * (visible query-key pairs): QK^T and PV, 2 flops per MAC."""
     return 4 * w.head_dim * w.num_q_heads * visible_pairs(w)
+
+
+def mixed_batch_parts(w: Workload):
+    """A mixed batch without a block mask as the library runs it: the
+    sequences with 1 <= G * q_len <= 16 rows go to the decode kernel, the
+    others to the prefill kernel.  Returns (decode-part algorithmic bytes,
+    prefill-part algorithmic FLOPs); the two parts' own bounds on the HBM and
+    tensor rooflines add up to the batch's bound when they run one after the
+    other."""
+    import dataclasses
+    ctx = w.context_lens.tolist()
+    ql = w.q_lens.tolist()
+    small = [1 <= w.gqa * q <= 16 and w.block_mask is None for q in ql]
+
+    def part(keep):
+        idx = [i for i, k in enumerate(keep) if k]
+        c = [ctx[i] for i in idx]
+        q = [ql[i] for i in idx]
+        mask = w.block_mask[idx] if w.block_mask is not None else None
+        return dataclasses.replace(w, context_lens=torch.tensor(c, dtype=torch.int32),
+                                   q_lens=torch.tensor(q, dtype=torch.int32),
+                                   num_seqs=len(c), block_mask=mask)
+
+    dec = part(small)
+    pre = part([not k for k in small])
+    return (decode_algorithmic_bytes(dec) if dec.num_seqs else 0,
+            prefill_algorithmic_flops(pre) if pre.num_seqs else 0)

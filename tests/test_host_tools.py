@@ -109,3 +109,32 @@ def test_traffic_is_reported_only_for_the_kernel_it_was_taken_on(tmp_path, monke
     assert bench.load_traffic("pa_prefill", "hybrid") is None              # absent
     assert bench.load_traffic("pa_decode_splitk", "decode_fp8", 2) == 789
     assert bench.load_traffic("pa_decode_splitk", "decode_fp8", 3) is None  # other q_len
+
+
+def test_mixed_batch_parts_split_the_work():
+    """The hybrid batch's decode part holds the sequences with 1 <= G * q_len
+    <= 16 (the library's split), the prefill part the others: bytes and FLOPs
+    are additive over sequences, so the parts add up to the whole batch's; a
+    masked batch has no decode part."""
+    import dataclasses
+    import torch
+    w = W.hybrid_bf16(shrink=16)
+    dec_bytes, pre_flops = W.mixed_batch_parts(w)
+    small = [1 <= w.gqa * int(q) <= 16 for q in w.q_lens]
+    assert 0 < sum(small) < len(small)
+
+    def part(keep):
+        c = [int(x) for x, k in zip(w.context_lens, keep) if k]
+        q = [int(x) for x, k in zip(w.q_lens, keep) if k]
+        return dataclasses.replace(w, context_lens=torch.tensor(c, dtype=torch.int32),
+                                   q_lens=torch.tensor(q, dtype=torch.int32), num_seqs=len(c))
+
+    big = [not k for k in small]
+    assert dec_bytes == W.decode_algorithmic_bytes(part(small))
+    assert pre_flops == W.prefill_algorithmic_flops(part(big))
+    assert (W.decode_algorithmic_bytes(part(small)) + W.decode_algorithmic_bytes(part(big))
+            == W.decode_algorithmic_bytes(w))
+    assert (W.prefill_algorithmic_flops(part(small)) + pre_flops
+            == W.prefill_algorithmic_flops(w))
+    ws = W.prefill_bf16(sparse=True, shrink=32)
+    assert W.mixed_batch_parts(ws) == (0, W.prefill_algorithmic_flops(ws))
